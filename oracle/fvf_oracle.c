@@ -1,0 +1,250 @@
+/*
+ * fvf_oracle.c -- plain, slow, obviously correct CPU oracle for the three
+ * per-cell field sweeps.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check
+ * and the benchmark's CPU-baseline leg call it; the GPU library never links,
+ * includes or calls anything here, and nothing here includes the GPU code.
+ *
+ * Build: gcc -O2 -ffp-contract=off [-fopenmp] -fPIC -shared.  Contraction is
+ * switched off so that every `a*b + c` below is a separately rounded multiply
+ * and add, as the Fortran reference on the Qiita page performs them.
+ *
+ * Sources (pages, by title and section):
+ *  [Q]  Qiita, "Fortran 2018でGPUを高速化する Part 3 -- GPUカーネルの
+ *       メモリアクセスとFP32・FP64を比較する" ("Fortran 2018 GPU acceleration,
+ *       part 3"): section 3 (the 5-point update and alpha), section 4
+ *       (column-major layout, i contiguous), section 5.1 (all-cells variant,
+ *       edges written 0 each step), section 5.4 (ping-pong: odd steps u->v,
+ *       even steps v->u), appendix A (CPU reference program: j outer loop,
+ *       i inner loop, same update).
+ *  [M]  MFlowCode/MFC pull request #2087, "Collapse only spatial loops in
+ *       per-variable GPU kernels": "Changes" (the WENO input pack
+ *       v_rs_weno(j,k,l,i) = v_vf(i)%sf(j,k,l) and the x/y/z flux
+ *       differences in s_compute_advection_source_term, inverse spacing taken
+ *       once per cell).
+ *
+ * Conventions (0-based C indices; the pages use 1-based Fortran):
+ *  - 2D field u(i,j), 0 <= i < nx, 0 <= j < ny, stored at u[i + nx*j].
+ *  - A 3D field with interior extents (n1,n2,n3) and ghost width g is stored
+ *    with extents N_a = n_a + 2g on every axis with n_a > 1 and N_a = 1 on an
+ *    axis with n_a == 1 (a 2D problem has n3 == 1).  Element (j,k,l) of the
+ *    stored box sits at j + N1*(k + N2*l); interior cell (j,k,l) is stored
+ *    element (j+g1, k+g2, l+g3) with g_a = g where n_a > 1, else 0.
+ */
+#include <stddef.h>
+#include <stdint.h>
+
+/* ---------------------------------------------------------------------- */
+/* 2D explicit diffusion                                                  */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * One application of the update of [Q] section 3:
+ *     dst(i,j) = src(i,j) + alpha*(src(i-1,j) + src(i+1,j)
+ *                                  + src(i,j-1) + src(i,j+1) - 4*src(i,j))
+ * for interior cells, and dst = 0 on the four edges ([Q] section 5.1 and the
+ * appendix-A CPU program).  C evaluates the bracket left to right, exactly as
+ * Fortran does: ((((W + E) + S) + N) - 4c), then alpha times that, then c plus
+ * the product, each operation rounded to nearest even.
+ */
+static void step_f64(const double *src, double *dst, int64_t nx, int64_t ny,
+                     double alpha, int nthreads)
+{
+    int64_t j;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (j = 0; j < ny; ++j) {
+        for (int64_t i = 0; i < nx; ++i) {
+            const int64_t c = i + nx * j;
+            if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1) {
+                dst[c] = 0.0;
+            } else {
+                dst[c] = src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]
+                                           + src[c + nx] - 4.0 * src[c]);
+            }
+        }
+    }
+}
+
+static void step_f32(const float *src, float *dst, int64_t nx, int64_t ny,
+                     float alpha, int nthreads)
+{
+    int64_t j;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (j = 0; j < ny; ++j) {
+        for (int64_t i = 0; i < nx; ++i) {
+            const int64_t c = i + nx * j;
+            if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1) {
+                dst[c] = 0.0f;
+            } else {
+                dst[c] = src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]
+                                           + src[c + nx] - 4.0f * src[c]);
+            }
+        }
+    }
+}
+
+/*
+ * nsteps applications with the ping-pong of [Q] section 5.4: step s
+ * (1-based) reads u and writes v when s is odd, reads v and writes u when s
+ * is even.  The result is in v after an odd count and in u after an even
+ * count.  Returns 1 when the result is in v, 0 when it is in u.
+ */
+int oracle_diffuse2d_f64(double *u, double *v, int64_t nx, int64_t ny,
+                         double alpha, int64_t nsteps, int nthreads)
+{
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        if (s % 2 == 1)
+            step_f64(u, v, nx, ny, alpha, nthreads);
+        else
+            step_f64(v, u, nx, ny, alpha, nthreads);
+    }
+    return (int)(nsteps % 2);
+}
+
+/* FP32 variant; alpha is the FP32 value (0.1_real32 in [Q] section 6.1). */
+int oracle_diffuse2d_f32(float *u, float *v, int64_t nx, int64_t ny,
+                         float alpha, int64_t nsteps, int nthreads)
+{
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        if (s % 2 == 1)
+            step_f32(u, v, nx, ny, alpha, nthreads);
+        else
+            step_f32(v, u, nx, ny, alpha, nthreads);
+    }
+    return (int)(nsteps % 2);
+}
+
+/* ---------------------------------------------------------------------- */
+/* 3D box helpers                                                         */
+/* ---------------------------------------------------------------------- */
+
+static int64_t stored_extent(int64_t n, int64_t g) { return n > 1 ? n + 2 * g : 1; }
+static int64_t ghost_offset(int64_t n, int64_t g) { return n > 1 ? g : 0; }
+
+/* ---------------------------------------------------------------------- */
+/* WENO input pack                                                        */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * The pack of [M] "Changes": out(j,k,l,i) = field_i(j,k,l), written as a
+ * plain element copy.  The page shows the x direction only; for y and z the
+ * first index of the output runs along the swept axis, i.e. the output is
+ * the field with the swept axis and the j axis exchanged:
+ *   dir 0 (x): out(a, b, c, i) = field_i(a,      b+g2, c+g3), extents (N1, n2, n3)
+ *   dir 1 (y): out(a, b, c, i) = field_i(b+g1,   a,    c+g3), extents (N2, n1, n3)
+ *   dir 2 (z): out(a, b, c, i) = field_i(c+g1,   b+g2, a   ), extents (N3, n2, n1)
+ * where the swept axis covers its ghost cells and the two transverse axes
+ * cover the interior only.  out(a,b,c,i) is stored at
+ * a + M1*(b + M2*(c + M3*i)) with (M1,M2,M3) the extents above.
+ * Returns 0, or -1 for an unknown direction.
+ */
+int oracle_weno_pack(const double *const *fields, int nv, int64_t n1, int64_t n2,
+                     int64_t n3, int64_t g, int dir, double *out)
+{
+    const int64_t N1 = stored_extent(n1, g), N2 = stored_extent(n2, g);
+    const int64_t N3 = stored_extent(n3, g);
+    const int64_t g1 = ghost_offset(n1, g), g2 = ghost_offset(n2, g);
+    const int64_t g3 = ghost_offset(n3, g);
+    int64_t M1, M2, M3;
+    if (dir == 0) {
+        M1 = N1; M2 = n2; M3 = n3;
+    } else if (dir == 1) {
+        M1 = N2; M2 = n1; M3 = n3;
+    } else if (dir == 2) {
+        M1 = N3; M2 = n2; M3 = n1;
+    } else {
+        return -1;
+    }
+    for (int i = 0; i < nv; ++i) {
+        const double *f = fields[i];
+        for (int64_t c = 0; c < M3; ++c) {
+            for (int64_t b = 0; b < M2; ++b) {
+                for (int64_t a = 0; a < M1; ++a) {
+                    int64_t j, k, l;
+                    if (dir == 0) {
+                        j = a; k = b + g2; l = c + g3;
+                    } else if (dir == 1) {
+                        j = b + g1; k = a; l = c + g3;
+                    } else {
+                        j = c + g1; k = b + g2; l = a;
+                    }
+                    out[a + M1 * (b + M2 * (c + M3 * (int64_t)i))] =
+                        f[j + N1 * (k + N2 * l)];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Flux-difference source                                                 */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * The x/y/z flux differences of [M] "Changes"
+ * (s_compute_advection_source_term):
+ *   dir 0: rhs(j,k,l,i) = inv_d(j) * (F(j-1,k,l,i) - F(j,k,l,i))
+ *   dir 1: rhs(j,k,l,i) = inv_d(k) * (F(j,k-1,l,i) - F(j,k,l,i))
+ *   dir 2: rhs(j,k,l,i) = inv_d(l) * (F(j,k,l-1,i) - F(j,k,l,i))
+ * over interior cells 0 <= j < n1, 0 <= k < n2, 0 <= l < n3.  The face array
+ * has one more entry than cells along the swept axis: face f (-1 <= f <= n-1)
+ * is stored at position f+1 on that axis, and the array is contiguous with
+ * the variable index slowest.  rhs(j,k,l,i) is stored at
+ * j + n1*(k + n2*(l + n3*i)).  One subtraction, then one multiplication.
+ * Returns 0, or -1 for an unknown direction.
+ */
+int oracle_advect_rhs(const double *flux, const double *inv_d, int nv, int64_t n1,
+                      int64_t n2, int64_t n3, int dir, double *rhs)
+{
+    int64_t F1 = n1, F2 = n2, F3 = n3;
+    if (dir == 0)
+        F1 = n1 + 1;
+    else if (dir == 1)
+        F2 = n2 + 1;
+    else if (dir == 2)
+        F3 = n3 + 1;
+    else
+        return -1;
+    for (int i = 0; i < nv; ++i) {
+        for (int64_t l = 0; l < n3; ++l) {
+            for (int64_t k = 0; k < n2; ++k) {
+                for (int64_t j = 0; j < n1; ++j) {
+                    /* stored positions of the low face (f = cell-1) and the
+                     * high face (f = cell) of this cell along the swept axis */
+                    int64_t jl = j, kl = k, ll = l, jh = j, kh = k, lh = l;
+                    double w;
+                    if (dir == 0) {
+                        jl = j; jh = j + 1; w = inv_d[j];
+                    } else if (dir == 1) {
+                        kl = k; kh = k + 1; w = inv_d[k];
+                    } else {
+                        ll = l; lh = l + 1; w = inv_d[l];
+                    }
+                    const double lo = flux[jl + F1 * (kl + F2 * (ll + F3 * (int64_t)i))];
+                    const double hi = flux[jh + F1 * (kh + F2 * (lh + F3 * (int64_t)i))];
+                    rhs[j + n1 * (k + n2 * (l + n3 * (int64_t)i))] = w * (lo - hi);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Number of OpenMP threads the diffusion loops may use (1 without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,220 @@
+"""Pins of the CPU oracle's WENO pack and flux-difference source (MFC pull
+request #2087, "Collapse only spatial loops in per-variable GPU kernels",
+"Changes").
+
+The expected values come from independent formulations (numpy slicing and
+transposition of the Fortran-ordered boxes, coordinate-tagged fields), exact
+special cases (constant and linear fluxes) and invariants (telescoping sums,
+bit-for-bit copies of NaN payloads and signed zeros).
+"""
+from __future__ import annotations
+
+import itertools
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from finite_volume_field_gb300 import inputs
+
+SHAPES = [((3, 4, 5), 1), ((3, 4, 5), 2), ((5, 4, 1), 2), ((6, 3, 2), 3), ((2, 7, 3), 1)]
+
+
+def _box(flat, stored):
+    """View a Fortran-ordered stored box as a numpy array indexed [l, k, j]."""
+    N1, N2, N3 = stored
+    return np.asarray(flat).reshape(N3, N2, N1)
+
+
+def _numpy_pack(fields, extents, g, direction):
+    """The pack written with numpy slices and transposes of [l, k, j] arrays."""
+    n1, n2, n3 = extents
+    st = inputs.stored_extents(extents, g)
+    g1, g2, g3 = (g if n > 1 else 0 for n in extents)
+    parts = []
+    for f in fields:
+        A = _box(f, st)
+        if direction == 0:      # out[c, b, a] = A[c+g3, b+g2, a]
+            S = A[g3:g3 + n3, g2:g2 + n2, :]
+        elif direction == 1:    # out[c, b, a] = A[c+g3, a, b+g1]
+            S = A[g3:g3 + n3, :, g1:g1 + n1].transpose(0, 2, 1)
+        else:                   # out[c, b, a] = A[a, b+g2, c+g1]
+            S = A[:, g2:g2 + n2, g1:g1 + n1].transpose(2, 1, 0)
+        parts.append(np.ascontiguousarray(S).reshape(-1))
+    return np.concatenate(parts)
+
+
+@pytest.mark.parametrize("extents,g", SHAPES)
+@pytest.mark.parametrize("direction", [0, 1, 2])
+@pytest.mark.parametrize("nv", [1, 3])
+def test_pack_matches_numpy_formulation(extents, g, direction, nv):
+    if extents[direction] == 1:
+        pytest.skip("no sweep along an axis of extent 1")
+    st = inputs.stored_extents(extents, g)
+    fields = inputs.normal_fields(inputs.config_seed(0), nv, extents, g)
+    got = oracle.weno_pack(fields, extents, g, direction)
+    want = _numpy_pack(fields, extents, g, direction)
+    assert got.shape == want.shape
+    assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+    M = oracle.pack_extents(extents, g, direction)
+    assert got.size == M[0] * M[1] * M[2] * nv
+    assert st[direction] == M[0]
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_pack_coordinate_tags(direction):
+    """Each source element carries its own (i, j, k, l) as an exact number;
+    decoding the output must give the swept axis (with its ghosts) first, the
+    other axes' interior cells next, and the variable slowest."""
+    extents, g = (4, 5, 6), 2
+    n1, n2, n3 = extents
+    N1, N2, N3 = inputs.stored_extents(extents, g)
+    nv = 3
+    fields = []
+    for i in range(nv):
+        l, k, j = np.meshgrid(np.arange(N3), np.arange(N2), np.arange(N1), indexing="ij")
+        fields.append((i * 1e9 + j * 1e6 + k * 1e3 + l).astype(np.float64).reshape(-1))
+    out = oracle.weno_pack(fields, extents, g, direction)
+    M1, M2, M3 = oracle.pack_extents(extents, g, direction)
+    for i, c, b, a in itertools.product(range(nv), range(M3), range(M2), range(M1)):
+        val = int(out[a + M1 * (b + M2 * (c + M3 * i))])
+        ti, r = divmod(val, 10**9)
+        tj, r = divmod(r, 10**6)
+        tk, tl = divmod(r, 10**3)
+        if direction == 0:
+            want = (a, b + g, c + g)
+        elif direction == 1:
+            want = (b + g, a, c + g)
+        else:
+            want = (c + g, b + g, a)
+        assert (ti, tj, tk, tl) == (i, *want)
+
+
+def test_pack_copies_bits_exactly():
+    """NaN payloads, signed zeros, infinities and subnormals survive the pack
+    bit for bit (it is a copy, not arithmetic)."""
+    extents, g = (3, 4, 5), 1
+    n = int(np.prod(inputs.stored_extents(extents, g)))
+    bits = inputs.random_bits(7, 0, n)
+    special = np.array([0x7FF8000000000001, 0xFFF0000000000000, 0x8000000000000000,
+                        0x0000000000000001, 0x7FF4DEADBEEF0000, 0x7FF0000000000000],
+                       dtype=np.uint64)
+    bits[: special.size] = special
+    bits[-special.size:] = special
+    for direction in range(3):
+        f = bits.view(np.float64)
+        got = oracle.weno_pack([f], extents, g, direction)
+        want = _numpy_pack([f], extents, g, direction)
+        assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+
+
+def test_pack_round_trip_recovers_sub_box():
+    """Scattering the pack back through the inverse permutation restores the
+    swept-axis-with-ghosts by interior-transverse sub-box exactly."""
+    extents, g = (5, 6, 7), 2
+    st = inputs.stored_extents(extents, g)
+    f = inputs.normal_fields(3, 1, extents, g)[0]
+    A = _box(f, st)
+    for direction in range(3):
+        out = oracle.weno_pack([f], extents, g, direction)
+        M1, M2, M3 = oracle.pack_extents(extents, g, direction)
+        O = out.reshape(M3, M2, M1)
+        if direction == 0:
+            back = O
+            ref = A[g:-g, g:-g, :]
+        elif direction == 1:
+            back = O.transpose(0, 2, 1)
+            ref = A[g:-g, :, g:-g]
+        else:
+            back = O.transpose(2, 1, 0)
+            ref = A[:, g:-g, g:-g]
+        assert np.array_equal(back, ref)
+
+
+# ---------------------------------------------------------------------------
+# Flux difference
+# ---------------------------------------------------------------------------
+
+def _numpy_rhs(flux, inv_d, nv, extents, direction):
+    """The flux difference with numpy differences along the swept axis of a
+    [i, l, k, j] array: rhs = inv_d * (F[low face] - F[high face])."""
+    n1, n2, n3 = extents
+    F1, F2, F3 = oracle.flux_extents(extents, direction)
+    F = np.asarray(flux).reshape(nv, F3, F2, F1)
+    if direction == 0:
+        return (inv_d[None, None, None, :] * (F[..., :-1] - F[..., 1:])).reshape(-1)
+    if direction == 1:
+        return (inv_d[None, None, :, None] * (F[:, :, :-1, :] - F[:, :, 1:, :])).reshape(-1)
+    return (inv_d[None, :, None, None] * (F[:, :-1] - F[:, 1:])).reshape(-1)
+
+
+@pytest.mark.parametrize("extents", [(3, 4, 5), (5, 4, 1), (1, 6, 2), (7, 1, 3)])
+@pytest.mark.parametrize("direction", [0, 1, 2])
+@pytest.mark.parametrize("nv", [1, 3])
+def test_rhs_matches_numpy_formulation(extents, direction, nv):
+    seed = inputs.config_seed(0)
+    flux = inputs.face_fluxes(seed, nv, extents, direction)
+    inv_d = inputs.inverse_spacing(seed, extents[direction], stream=200 + direction)
+    got = oracle.advect_rhs(flux, inv_d, nv, extents, direction)
+    want = _numpy_rhs(flux, inv_d, nv, extents, direction)
+    assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_rhs_constant_flux_is_positive_zero(direction):
+    """A constant flux has no difference: rhs is +0.0 exactly (inv_d > 0)."""
+    extents, nv = (4, 5, 6), 2
+    F = np.full(int(np.prod(oracle.flux_extents(extents, direction))) * nv, 3.25)
+    inv_d = inputs.inverse_spacing(1, extents[direction])
+    rhs = oracle.advect_rhs(F, inv_d, nv, extents, direction)
+    assert np.all(rhs.view(np.uint64) == 0)
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_rhs_linear_flux_gives_minus_inv_d(direction):
+    """F(f) = f along the swept axis (face f stored at position f + 1):
+    F(c-1) - F(c) = -1 exactly, so rhs = -inv_d(c) exactly; the sign fixes
+    which face is subtracted from which."""
+    extents, nv = (4, 5, 6), 2
+    F1, F2, F3 = oracle.flux_extents(extents, direction)
+    l, k, j = np.meshgrid(np.arange(F3), np.arange(F2), np.arange(F1), indexing="ij")
+    pos = (j, k, l)[direction] - 1.0
+    F = np.tile(pos.reshape(-1), nv)
+    inv_d = inputs.inverse_spacing(5, extents[direction])
+    rhs = oracle.advect_rhs(F, inv_d, nv, extents, direction)
+    n1, n2, n3 = extents
+    R = rhs.reshape(nv, n3, n2, n1)
+    shape = [1, 1, 1, 1]
+    shape[3 - direction] = -1
+    assert np.array_equal(R, np.broadcast_to(-inv_d.reshape(shape), R.shape))
+
+
+def test_rhs_telescopes():
+    """Summing rhs/inv_d along the swept axis gives F(-1) - F(n-1) up to
+    rounding (the interior faces cancel)."""
+    extents, nv = (9, 4, 3), 2
+    flux = inputs.face_fluxes(11, nv, extents, 0)
+    inv_d = inputs.inverse_spacing(11, 9)
+    rhs = oracle.advect_rhs(flux, inv_d, nv, extents, 0).reshape(nv, 3, 4, 9)
+    F = flux.reshape(nv, 3, 4, 10)
+    s = np.array([[[math.fsum((rhs[i, l, k, :] / inv_d).tolist()) for k in range(4)]
+                   for l in range(3)] for i in range(nv)])
+    assert np.allclose(s, F[..., 0] - F[..., -1], rtol=0, atol=1e-13)
+
+
+def test_multivar_sequence_shapes():
+    """The 2D multi-variable sequence (pack x, pack y, rhs x, rhs y) on a
+    small box returns outputs of the sizes the layouts imply."""
+    extents, g, nv = (12, 8, 1), 2, 7
+    seed = inputs.config_seed(5)
+    fields = inputs.multivar_fields_2d(seed, extents, g)
+    fx = inputs.face_fluxes(seed, nv, extents, 0)
+    fy = inputs.face_fluxes(seed, nv, extents, 1)
+    wx = inputs.inverse_spacing(seed, 12, stream=200)
+    wy = inputs.inverse_spacing(seed, 8, stream=201)
+    px, py, rx, ry = oracle.multivar_sweep_2d(fields, fx, fy, wx, wy, nv, extents, g)
+    assert px.size == 16 * 8 * 7 and py.size == 12 * 12 * 7
+    assert rx.size == ry.size == 12 * 8 * 7
+    assert np.all(fields[5] >= 0) and np.all(fields[5] < 1)
+    assert np.all(fields[0] > 0)
