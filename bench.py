@@ -1,0 +1,578 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 field sweeps.
+
+One step is one pass of every sweep on the hot path, each on its seeded
+synthetic workload, all inputs resident in HBM:
+  * diffusion, 8192 x 8192, alpha 0.1, 200 steps, FP32 and FP64 (interior
+    uniform [0,1), zero edges)        -- the headline workload;
+  * WENO pack x, y, z: 8 fields of 201^3 cells + 3 ghost layers (207^3);
+  * flux difference x, y, z: nv 8 on 201^3 cells;
+  * the 2D multi-variable sequence on 4800 x 1200 cells, nv 7, ghost 2:
+    pack x, pack y, flux x, flux y, repeated 100 times.
+
+``value`` is achieved HBM GB/s: the step's compulsory bytes (one read of every
+input element and one write of every output element per sweep) over the
+step's device time, summed over all ranks.  Every working set exceeds the
+129 MB L2, so no flush is needed between iterations.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]``;
+under torchrun each rank runs the whole workload on its own GPU (independent
+replicas, weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+from finite_volume_field_gb300 import inputs  # noqa: E402
+
+METRIC = "achieved HBM GB/s and Gcell-var/s per sweep, % of GB300 HBM roofline"
+WORKLOAD = ("2D 5-point diffusion 8192x8192, alpha 0.1, 200 steps, FP32 and FP64 "
+            "(plus one pass of each other hot-path sweep: WENO pack x/y/z nv=8 207^3, "
+            "flux difference x/y/z nv=8 201^3, 4800x1200 nv=7 pack+flux sequence x100)")
+FALLBACK_HBM_GBS = 6800.0
+FP64_NOMINAL_TFLOPS = 1.25   # FP64 rate of the part (FMA counted as 2 flops)
+
+# ---------------------------------------------------------------------------
+# Workload definition (sizes, compulsory bytes, cell-var counts)
+# ---------------------------------------------------------------------------
+
+DIFF_N, DIFF_STEPS = 8192, 200
+PACK_EXT, PACK_G, PACK_NV = (201, 201, 201), 3, 8
+RHS_EXT, RHS_NV = (201, 201, 201), 8
+SEQ_EXT, SEQ_G, SEQ_NV, SEQ_REPS = (4800, 1200, 1), 2, 7, 100
+
+
+def _prod(t):
+    p = 1
+    for x in t:
+        p *= int(x)
+    return p
+
+
+def pack_extents(ext, g, d):
+    N = inputs.stored_extents(ext, g)
+    return [(N[0], ext[1], ext[2]), (N[1], ext[0], ext[2]), (N[2], ext[1], ext[0])][d]
+
+
+def pack_bytes(ext, g, nv, d):
+    return 16 * _prod(pack_extents(ext, g, d)) * nv
+
+
+def rhs_bytes(ext, nv, d):
+    f = list(ext)
+    f[d] += 1
+    return 8 * (_prod(f) * nv + _prod(ext) * nv + ext[d])
+
+
+def rows():
+    """Per sweep: compulsory bytes, cell-var updates and launches per step."""
+    r = {}
+    cells = (DIFF_N - 2) ** 2
+    for name, p in (("diffuse_fp32", 4), ("diffuse_fp64", 8)):
+        r[name] = dict(bytes=DIFF_STEPS * 2 * DIFF_N * DIFF_N * p, cellvars=DIFF_STEPS * cells,
+                       launches=DIFF_STEPS, per_launch_bytes=2 * DIFF_N * DIFF_N * p,
+                       per_launch_cells=cells)
+    for d, ax in enumerate("xyz"):
+        b = pack_bytes(PACK_EXT, PACK_G, PACK_NV, d)
+        cv = _prod(pack_extents(PACK_EXT, PACK_G, d)) * PACK_NV
+        r[f"pack_{ax}"] = dict(bytes=b, cellvars=cv, launches=1, per_launch_bytes=b,
+                               per_launch_cells=cv)
+    for d, ax in enumerate("xyz"):
+        b = rhs_bytes(RHS_EXT, RHS_NV, d)
+        cv = _prod(RHS_EXT) * RHS_NV
+        r[f"rhs_{ax}"] = dict(bytes=b, cellvars=cv, launches=1, per_launch_bytes=b,
+                              per_launch_cells=cv)
+    b = (pack_bytes(SEQ_EXT, SEQ_G, SEQ_NV, 0) + pack_bytes(SEQ_EXT, SEQ_G, SEQ_NV, 1)
+         + rhs_bytes(SEQ_EXT, SEQ_NV, 0) + rhs_bytes(SEQ_EXT, SEQ_NV, 1))
+    cv = (_prod(pack_extents(SEQ_EXT, SEQ_G, 0)) + _prod(pack_extents(SEQ_EXT, SEQ_G, 1))
+          + 2 * _prod(SEQ_EXT)) * SEQ_NV
+    r["seq2d"] = dict(bytes=SEQ_REPS * b, cellvars=SEQ_REPS * cv, launches=4 * SEQ_REPS,
+                      per_launch_bytes=b / 4, per_launch_cells=cv / 4)
+    return r
+
+
+# ---------------------------------------------------------------------------
+# Host inputs (seeded; shared recipe with the tests)
+# ---------------------------------------------------------------------------
+
+def host_inputs():
+    s2, s3, s4, s5 = (inputs.config_seed(k) for k in (2, 3, 4, 5))
+    h = {}
+    h["u32"] = inputs.diffusion_field(DIFF_N, DIFF_N, np.float32, seed=s2, stream=0)
+    h["u64"] = inputs.diffusion_field(DIFF_N, DIFF_N, np.float64, seed=s2, stream=1)
+    h["pack_fields"] = inputs.normal_fields(s3, PACK_NV, PACK_EXT, PACK_G)
+    h["rhs_flux"] = [inputs.face_fluxes(s4, RHS_NV, RHS_EXT, d) for d in range(3)]
+    h["rhs_invd"] = [inputs.inverse_spacing(s4, RHS_EXT[d], stream=200 + d) for d in range(3)]
+    h["seq_fields"] = inputs.multivar_fields_2d(s5, SEQ_EXT, SEQ_G)
+    h["seq_flux"] = [inputs.face_fluxes(s5, SEQ_NV, SEQ_EXT, d) for d in range(2)]
+    h["seq_invd"] = [inputs.inverse_spacing(s5, SEQ_EXT[d], stream=200 + d) for d in range(2)]
+    return h
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+
+class Sweeps:
+    """Device buffers of one rank and the enqueueing of one step."""
+
+    def __init__(self, torch, host, device, stream):
+        self.t = torch
+        self.dev = device
+        self.stream = stream
+        f64 = torch.float64
+        d = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        self.inputs = {}   # name -> device tensor that a host->device copy refills
+        self.outputs = {}  # name -> device tensor read back after a step
+        self.u32, self.u64 = d(host["u32"]), d(host["u64"])
+        self.v32, self.v64 = torch.zeros_like(self.u32), torch.zeros_like(self.u64)
+        self.inputs.update(u32=self.u32, u64=self.u64)
+        self.outputs.update(u32=self.u32, u64=self.u64)   # 200 steps: result back in u
+        self.pack_fields = [d(f) for f in host["pack_fields"]]
+        for i, f in enumerate(self.pack_fields):
+            self.inputs[f"pack_field{i}"] = f
+        self.pack_out = []
+        for k in range(3):
+            o = torch.empty(_prod(pack_extents(PACK_EXT, PACK_G, k)) * PACK_NV, dtype=f64,
+                            device=device)
+            self.pack_out.append(o)
+            self.outputs[f"pack_out{k}"] = o
+        self.rhs_flux = [d(f) for f in host["rhs_flux"]]
+        self.rhs_invd = [d(w) for w in host["rhs_invd"]]
+        self.rhs_out = [torch.empty(_prod(RHS_EXT) * RHS_NV, dtype=f64, device=device)
+                        for _ in range(3)]
+        for k in range(3):
+            self.inputs[f"rhs_flux{k}"] = self.rhs_flux[k]
+            self.inputs[f"rhs_invd{k}"] = self.rhs_invd[k]
+            self.outputs[f"rhs_out{k}"] = self.rhs_out[k]
+        self.seq_fields = [d(f) for f in host["seq_fields"]]
+        self.seq_flux = [d(f) for f in host["seq_flux"]]
+        self.seq_invd = [d(w) for w in host["seq_invd"]]
+        self.seq_px = torch.empty(_prod(pack_extents(SEQ_EXT, SEQ_G, 0)) * SEQ_NV, dtype=f64,
+                                  device=device)
+        self.seq_py = torch.empty(_prod(pack_extents(SEQ_EXT, SEQ_G, 1)) * SEQ_NV, dtype=f64,
+                                  device=device)
+        self.seq_rx = torch.empty(_prod(SEQ_EXT) * SEQ_NV, dtype=f64, device=device)
+        self.seq_ry = torch.empty_like(self.seq_rx)
+        for i, f in enumerate(self.seq_fields):
+            self.inputs[f"seq_field{i}"] = f
+        for k in range(2):
+            self.inputs[f"seq_flux{k}"] = self.seq_flux[k]
+            self.inputs[f"seq_invd{k}"] = self.seq_invd[k]
+        self.outputs.update(seq_px=self.seq_px, seq_py=self.seq_py, seq_rx=self.seq_rx,
+                            seq_ry=self.seq_ry)
+
+    def step(self, ev=None):
+        """Enqueue one step on self.stream; ev maps row name -> (start, end)
+        CUDA events recorded around that row."""
+        from finite_volume_field_gb300 import api
+        s = self.stream
+
+        def mark(name, which):
+            if ev is not None:
+                ev[name][which].record(s)
+
+        mark("diffuse_fp32", 0)
+        api.diffuse2d_step(self.u32, self.v32, DIFF_N, DIFF_N, 0.1, DIFF_STEPS, api.FVF_FP32, s)
+        mark("diffuse_fp32", 1)
+        mark("diffuse_fp64", 0)
+        api.diffuse2d_step(self.u64, self.v64, DIFF_N, DIFF_N, 0.1, DIFF_STEPS, api.FVF_FP64, s)
+        mark("diffuse_fp64", 1)
+        for k, ax in enumerate("xyz"):
+            mark(f"pack_{ax}", 0)
+            api.weno_pack(self.pack_fields, PACK_NV, PACK_EXT, PACK_G, k, self.pack_out[k], s)
+            mark(f"pack_{ax}", 1)
+        for k, ax in enumerate("xyz"):
+            mark(f"rhs_{ax}", 0)
+            api.advect_rhs(self.rhs_flux[k], self.rhs_invd[k], RHS_NV, RHS_EXT, k,
+                           self.rhs_out[k], s)
+            mark(f"rhs_{ax}", 1)
+        mark("seq2d", 0)
+        for _ in range(SEQ_REPS):
+            api.weno_pack(self.seq_fields, SEQ_NV, SEQ_EXT, SEQ_G, 0, self.seq_px, s)
+            api.weno_pack(self.seq_fields, SEQ_NV, SEQ_EXT, SEQ_G, 1, self.seq_py, s)
+            api.advect_rhs(self.seq_flux[0], self.seq_invd[0], SEQ_NV, SEQ_EXT, 0, self.seq_rx, s)
+            api.advect_rhs(self.seq_flux[1], self.seq_invd[1], SEQ_NV, SEQ_EXT, 1, self.seq_ry, s)
+        mark("seq2d", 1)
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.lines = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append(line.strip())
+
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_uuid(torch, device_index):
+    try:
+        u = torch.cuda.get_device_properties(device_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else f"GPU-{s}"
+    except Exception:
+        return None
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return json.loads(p.read_text()), "measured"
+        except ValueError:
+            pass
+    return {"hbm_gbs": FALLBACK_HBM_GBS}, "fallback"
+
+
+def ncu_traffic(kernel: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, if
+    the summary was taken on the kernel source as it is now (else None)."""
+    p = ROOT / "profiles" / "ncu_traffic.txt"
+    if not p.exists():
+        return None
+    src_hash = source_hash()
+    for line in p.read_text().splitlines():
+        m = re.match(r"^(\S+)\s+(\d+)\s+(\S+)", line.strip())
+        if m and m.group(1) == kernel and m.group(3) == src_hash:
+            return int(m.group(2))
+    return None
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted((ROOT / "finite_volume_field_gb300" / "csrc").glob("*")):
+        if f.suffix in (".cu", ".cuh", ".h"):
+            h.update(f.name.encode())
+            h.update(f.read_bytes())
+    return h.hexdigest()[:12]
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(host, diffusion_steps=2):
+    """Time the CPU oracle, as it stands, on a bounded sample of the step:
+    ``diffusion_steps`` of each precision on the full 8192^2 grid (OpenMP over
+    rows, all host threads), one pass of pack x/y/z and flux x/y/z, one
+    repetition of the 2D sequence (single-threaded loops).  Returns (bytes,
+    cellvars, seconds, threads)."""
+    import oracle
+    threads = oracle.max_threads()
+    tot_b = tot_cv = tot_s = 0.0
+    for key, p in (("u32", 4), ("u64", 8)):
+        t0 = time.perf_counter()
+        oracle.diffuse2d(host[key], diffusion_steps, nthreads=threads)
+        tot_s += time.perf_counter() - t0
+        tot_b += diffusion_steps * 2 * DIFF_N * DIFF_N * p
+        tot_cv += diffusion_steps * (DIFF_N - 2) ** 2
+    for k in range(3):
+        t0 = time.perf_counter()
+        oracle.weno_pack(host["pack_fields"], PACK_EXT, PACK_G, k)
+        oracle.advect_rhs(host["rhs_flux"][k], host["rhs_invd"][k], RHS_NV, RHS_EXT, k)
+        tot_s += time.perf_counter() - t0
+        tot_b += pack_bytes(PACK_EXT, PACK_G, PACK_NV, k) + rhs_bytes(RHS_EXT, RHS_NV, k)
+        tot_cv += (_prod(pack_extents(PACK_EXT, PACK_G, k)) * PACK_NV + _prod(RHS_EXT) * RHS_NV)
+    t0 = time.perf_counter()
+    oracle.multivar_sweep_2d(host["seq_fields"], host["seq_flux"][0], host["seq_flux"][1],
+                             host["seq_invd"][0], host["seq_invd"][1], SEQ_NV, SEQ_EXT, SEQ_G)
+    tot_s += time.perf_counter() - t0
+    r = rows()["seq2d"]
+    tot_b += r["bytes"] / SEQ_REPS
+    tot_cv += r["cellvars"] / SEQ_REPS
+    return tot_b, tot_cv, tot_s, threads
+
+
+ORACLE_SAMPLE_DESC = ("2 diffusion steps per precision on 8192^2 (OpenMP rows, all host threads) "
+                      "+ one pass of pack x/y/z (8x207^3) and flux x/y/z (8x201^3) + one repetition "
+                      "of the 4800x1200 sequence (single-threaded); GB/s = compulsory bytes / wall time")
+
+
+# ---------------------------------------------------------------------------
+# Arms
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    host = host_inputs()
+    for _ in range(args.warmup):
+        oracle_sample(host, diffusion_steps=1)
+    samples = []
+    for _ in range(args.steps):
+        samples.append(oracle_sample(host, diffusion_steps=1))
+    b = sum(s[0] for s in samples)
+    cv = sum(s[1] for s in samples)
+    sec = sum(s[2] for s in samples)
+    threads = samples[0][3]
+    gbs = b / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32+f64",
+        "data": "synthetic", "gcell_var_per_s": cv / sec / 1e9,
+        "config": {"workload": WORKLOAD, "reference": "CPU oracle (plain C, -O2 -ffp-contract=off)",
+                   "sample": ORACLE_SAMPLE_DESC.replace("2 diffusion", "1 diffusion")},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": ORACLE_SAMPLE_DESC.replace("2 diffusion", "1 diffusion")},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def aggregate(per_rank, world):
+    """Combine per-rank measurements: device time is the max over ranks,
+    throughput counts the work of every rank."""
+    ms = max(r["ms_per_step"] for r in per_rank)
+    e2e_ms = max(r["e2e_ms_per_step"] for r in per_rank)
+    launches = sum(r["launches"] for r in per_rank)
+    return ms, e2e_ms, launches
+
+
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    from finite_volume_field_gb300 import api, buildlib
+    if not api.LIB_PATH.exists():
+        buildlib.build()
+    api.load()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    host = host_inputs()
+    stream = torch.cuda.Stream(device)
+    sw = Sweeps(torch, host, device, stream)
+    R = rows()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            sw.step()
+    barrier()
+
+    # One set of row events per timed step, read after the loop (no host
+    # synchronisation inside the timed region).
+    evs = [{name: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for name in R} for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    sampler.start()
+    time.sleep(0.5)
+    barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = api.launch_count()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for k in range(args.steps):
+            sw.step(evs[k])
+        end.record(stream)
+    barrier()
+    per_row = {name: [e[name][0].elapsed_time(e[name][1]) for e in evs] for name in R}
+    launches = api.launch_count() - launches0
+    clocks = sampler.stop()
+    total_ms = start.elapsed_time(end)
+    ms_per_step = total_ms / args.steps
+
+    # End to end through the public API: pinned host inputs copied in, the
+    # step, every output copied back, all inside the timed region.
+    pinned_in = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v.cpu())
+                 for k, v in sw.inputs.items()}
+    pinned_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                  for k, v in sw.outputs.items()}
+    h2d = sum(t.numel() * t.element_size() for t in pinned_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in pinned_out.values())
+    e2e_steps = max(1, min(args.steps, 3))
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k, t in pinned_in.items():
+                sw.inputs[k].copy_(t, non_blocking=True)
+            sw.step()
+            for k, t in pinned_out.items():
+                t.copy_(sw.outputs[k], non_blocking=True)
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+
+    mine = {"ms_per_step": ms_per_step, "e2e_ms_per_step": e2e_ms, "launches": launches}
+    if world > 1:
+        import torch.distributed as dist
+        gathered = [None] * world
+        dist.all_gather_object(gathered, mine)
+    else:
+        gathered = [mine]
+    ms, e2e_ms, launches = aggregate(gathered, world)
+
+    if rank == 0:
+        step_bytes = sum(r["bytes"] for r in R.values())
+        step_cv = sum(r["cellvars"] for r in R.values())
+        value = world * step_bytes / (ms * 1e-3) / 1e9
+        peaks, peak_kind = measured_peaks()
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+        sweeps = {}
+        for name, r in R.items():
+            t = statistics.median(per_row[name])
+            sweeps[name] = {
+                "ms": round(t, 4), "launches": r["launches"],
+                "gbs": round(r["bytes"] / (t * 1e-3) / 1e9, 1),
+                "gcell_var_per_s": round(r["cellvars"] / (t * 1e-3) / 1e9, 2),
+                "frac_hbm": round(r["bytes"] / (t * 1e-3) / 1e9 / hbm, 4),
+            }
+        dom = max((n for n in R if n != "seq2d"), key=lambda n: sweeps[n]["ms"])
+        r = R[dom]
+        launch_ms = sweeps[dom]["ms"] / r["launches"]
+        roof = {"kernel": dom, "bound": "hbm",
+                "achieved": round(r["per_launch_bytes"] / (launch_ms * 1e-3) / 1e9, 1),
+                "peak": hbm, "unit": "GB/s", "peak_source": f"{peak_kind} hbm_gbs",
+                "traffic": ncu_traffic(dom), "launch_ms": round(launch_ms, 5),
+                "algorithmic_bytes_per_launch": r["per_launch_bytes"]}
+        roof["frac"] = round(roof["achieved"] / hbm, 4)
+        if dom == "diffuse_fp64":
+            # 6 FP64 pipe instructions per cell (3 adds, 1 fma, 1 mul, 1 add),
+            # counted FMA-equivalent (2 flops each) against the part's FP64 rate.
+            fp64_tf = 12 * r["per_launch_cells"] / (launch_ms * 1e-3) / 1e12
+            roof["fp64_pipe"] = {"achieved": round(fp64_tf, 4), "peak": FP64_NOMINAL_TFLOPS,
+                                 "unit": "TFLOP/s", "frac": round(fp64_tf / FP64_NOMINAL_TFLOPS, 4),
+                                 "peak_source": "nominal FP64 rate (FMA = 2 flops)"}
+            if roof["fp64_pipe"]["frac"] > roof["frac"]:
+                roof.update(bound="alu", achieved=roof["fp64_pipe"]["achieved"],
+                            peak=FP64_NOMINAL_TFLOPS, unit="TFLOP/s",
+                            frac=roof["fp64_pipe"]["frac"],
+                            peak_source="nominal FP64 rate, FMA-equivalent")
+        line = {
+            "impl": "gb300", "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32+f64", "data": "synthetic",
+            "gcell_var_per_s": round(world * step_cv / (ms * 1e-3) / 1e9, 3),
+            "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                       "l2": "no flush: every launch's working set (>= 0.5 GB) exceeds the 129 MB L2",
+                       "bytes_per_step": step_bytes, "hbm_peak_gbs": hbm,
+                       "hbm_peak_source": peak_kind},
+            "sweeps": sweeps,
+            "roofline": roof,
+            "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            b, cv, sec, threads = oracle_sample(host)
+            line["cpu_baseline"] = {"value": round(b / sec / 1e9, 3), "unit": "GB/s",
+                                    "cores": threads, "kind": "oracle",
+                                    "sample": ORACLE_SAMPLE_DESC,
+                                    "gcell_var_per_s": round(cv / sec / 1e9, 4),
+                                    "seconds": round(sec, 2)}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (it is only taken at N=1 anyway)")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

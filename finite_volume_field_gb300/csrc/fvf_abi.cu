@@ -1,0 +1,231 @@
+// fvf_abi.cu -- the extern "C" entry points declared in include/fvf.h:
+// argument validation on the host, then dispatch to the kernel launchers.
+//
+// Nothing is launched unless every argument passed validation.  Beyond the
+// arithmetic checks (sizes, alignment, overlap), every array pointer is
+// checked to be device memory of the current device and, through the driver's
+// cuMemGetAddressRange, to lie with its whole extent inside one allocation, so
+// a wrong size or a host pointer becomes a status code instead of a device
+// fault.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fvf.h"
+#include "fvf_internal.cuh"
+
+#define FVF_API extern "C" __attribute__((visibility("default")))
+
+namespace fvf {
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local int g_last_cuda_error = 0;
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+namespace {
+
+using GetRangeFn = CUresult (*)(CUdeviceptr *, size_t *, CUdeviceptr);
+
+GetRangeFn get_range_fn() {
+    static std::once_flag once;
+    static GetRangeFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetRangeFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Checks that [p, p + bytes) is device (or managed) memory of the current
+// device inside a single allocation.
+int check_device_array(const void *p, uint64_t bytes) {
+    cudaPointerAttributes a;
+    std::memset(&a, 0, sizeof(a));
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return FVF_ERR_NOT_DEVICE;
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
+        return FVF_ERR_NOT_DEVICE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || a.device != dev) return FVF_ERR_NOT_DEVICE;
+    if (GetRangeFn fn = get_range_fn()) {
+        CUdeviceptr base = 0;
+        size_t size = 0;
+        if (fn(&base, &size, (CUdeviceptr)(uintptr_t)p) != CUDA_SUCCESS) return FVF_ERR_NOT_DEVICE;
+        const uint64_t off = (uint64_t)((uintptr_t)p - (uintptr_t)base);
+        if (off > size || bytes > size - off) return FVF_ERR_RANGE;
+    }
+    return FVF_OK;
+}
+
+bool overlaps(const void *a, uint64_t abytes, const void *b, uint64_t bbytes) {
+    const uintptr_t a0 = (uintptr_t)a, b0 = (uintptr_t)b;
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+// a*b with overflow check against a cap (products of sizes, in elements).
+bool mul_ok(int64_t a, int64_t b, int64_t *out) {
+    const int64_t cap = (int64_t)1 << 60;
+    if (a < 0 || b < 0) return false;
+    if (a != 0 && b > cap / a) return false;
+    *out = a * b;
+    return true;
+}
+
+int cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return FVF_OK;
+    g_last_cuda_error = (int)e;
+    return FVF_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fvf
+
+using namespace fvf;
+
+FVF_API int diffuse2d_step(void *u, void *v, int64_t nx, int64_t ny, double alpha,
+                           int64_t nsteps, int dtype, void *stream) {
+    if (dtype != FVF_FP32 && dtype != FVF_FP64) return FVF_ERR_DTYPE;
+    if (nx < 0 || ny < 0 || nsteps < 0) return FVF_ERR_SIZE;
+    int64_t cells = 0;
+    if (!mul_ok(nx, ny, &cells)) return FVF_ERR_SIZE;
+    if (!std::isfinite(alpha)) return FVF_ERR_ALPHA;
+    if (dtype == FVF_FP32 && !std::isfinite((float)alpha)) return FVF_ERR_ALPHA;
+    if (cells == 0 || nsteps == 0) return FVF_OK;
+    if (!u || !v) return FVF_ERR_NULL;
+    const uint64_t esize = dtype == FVF_FP64 ? 8 : 4;
+    if ((uintptr_t)u % esize || (uintptr_t)v % esize) return FVF_ERR_ALIGN;
+    const uint64_t bytes = (uint64_t)cells * esize;
+    int st = check_device_array(u, bytes);
+    if (st == FVF_OK) st = check_device_array(v, bytes);
+    if (st != FVF_OK) return st;
+    if (overlaps(u, bytes, v, bytes)) return FVF_ERR_ALIAS;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_diffuse2d(u, v, nx, ny, alpha, nsteps, dtype == FVF_FP64,
+                                           (cudaStream_t)stream, &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
+FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int ghost,
+                      int dir, double *out, void *stream) {
+    if (!extents) return FVF_ERR_NULL;
+    if (dir < 0 || dir > 2) return FVF_ERR_DIR;
+    if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
+    if (ghost < 0) return FVF_ERR_SIZE;
+    Box box;
+    for (int a = 0; a < 3; ++a) {
+        if (extents[a] < 0) return FVF_ERR_SIZE;
+        box.n[a] = extents[a];
+        box.g[a] = extents[a] > 1 ? ghost : 0;
+        box.N[a] = extents[a] > 1 ? extents[a] + 2 * (int64_t)ghost : extents[a];
+    }
+    int64_t stored = 0, t = 0, cells_out = 0, elems_out = 0;
+    if (!mul_ok(box.N[0], box.N[1], &t) || !mul_ok(t, box.N[2], &stored)) return FVF_ERR_SIZE;
+    const int64_t M[3][3] = {{box.N[0], box.n[1], box.n[2]},
+                             {box.N[1], box.n[0], box.n[2]},
+                             {box.N[2], box.n[1], box.n[0]}};
+    if (!mul_ok(M[dir][0], M[dir][1], &t) || !mul_ok(t, M[dir][2], &cells_out) ||
+        !mul_ok(cells_out, nv, &elems_out))
+        return FVF_ERR_SIZE;
+    if (elems_out == 0) return FVF_OK;
+    if (!fields || !out) return FVF_ERR_NULL;
+    if ((uintptr_t)out % 8) return FVF_ERR_ALIGN;
+    const uint64_t out_bytes = (uint64_t)elems_out * 8, in_bytes = (uint64_t)stored * 8;
+    FieldTable table;
+    std::memset(&table, 0, sizeof(table));
+    for (int i = 0; i < nv; ++i) {
+        if (!fields[i]) return FVF_ERR_NULL;
+        if ((uintptr_t)fields[i] % 8) return FVF_ERR_ALIGN;
+        table.p[i] = fields[i];
+    }
+    int st = check_device_array(out, out_bytes);
+    for (int i = 0; i < nv && st == FVF_OK; ++i) st = check_device_array(fields[i], in_bytes);
+    if (st != FVF_OK) return st;
+    for (int i = 0; i < nv; ++i)
+        if (overlaps(fields[i], in_bytes, out, out_bytes)) return FVF_ERR_ALIAS;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_weno_pack(table, nv, box, dir, out, (cudaStream_t)stream, &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
+FVF_API int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
+                       int dir, double *rhs, void *stream) {
+    if (!extents) return FVF_ERR_NULL;
+    if (dir < 0 || dir > 2) return FVF_ERR_DIR;
+    if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
+    int64_t n[3], F[3];
+    for (int a = 0; a < 3; ++a) {
+        if (extents[a] < 0) return FVF_ERR_SIZE;
+        n[a] = extents[a];
+        F[a] = extents[a] + (a == dir ? 1 : 0);
+    }
+    int64_t t = 0, cells = 0, faces = 0, elems = 0, felems = 0;
+    if (!mul_ok(n[0], n[1], &t) || !mul_ok(t, n[2], &cells) || !mul_ok(cells, nv, &elems))
+        return FVF_ERR_SIZE;
+    if (!mul_ok(F[0], F[1], &t) || !mul_ok(t, F[2], &faces) || !mul_ok(faces, nv, &felems))
+        return FVF_ERR_SIZE;
+    if (elems == 0) return FVF_OK;
+    if (!flux || !inv_d || !rhs) return FVF_ERR_NULL;
+    if ((uintptr_t)flux % 8 || (uintptr_t)inv_d % 8 || (uintptr_t)rhs % 8) return FVF_ERR_ALIGN;
+    const uint64_t rbytes = (uint64_t)elems * 8, fbytes = (uint64_t)felems * 8;
+    const uint64_t wbytes = (uint64_t)n[dir] * 8;
+    int st = check_device_array(flux, fbytes);
+    if (st == FVF_OK) st = check_device_array(inv_d, wbytes);
+    if (st == FVF_OK) st = check_device_array(rhs, rbytes);
+    if (st != FVF_OK) return st;
+    if (overlaps(rhs, rbytes, flux, fbytes) || overlaps(rhs, rbytes, inv_d, wbytes))
+        return FVF_ERR_ALIAS;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_advect_rhs(flux, inv_d, nv, n, dir, rhs, (cudaStream_t)stream,
+                                            &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
+FVF_API const char *fvf_status_string(int status) {
+    switch (status) {
+        case FVF_OK: return "ok";
+        case FVF_ERR_NULL: return "null pointer";
+        case FVF_ERR_SIZE: return "invalid size";
+        case FVF_ERR_DTYPE: return "invalid dtype";
+        case FVF_ERR_DIR: return "invalid direction";
+        case FVF_ERR_NV: return "invalid number of variables";
+        case FVF_ERR_ALIAS: return "output overlaps an input";
+        case FVF_ERR_ALPHA: return "alpha is not finite";
+        case FVF_ERR_ALIGN: return "misaligned pointer";
+        case FVF_ERR_NOT_DEVICE: return "pointer is not device memory of the current device";
+        case FVF_ERR_RANGE: return "array runs past the end of its allocation";
+        case FVF_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+FVF_API int fvf_last_cuda_error(void) { return g_last_cuda_error; }
+
+FVF_API uint64_t fvf_launch_count(void) { return g_launches.load(); }

@@ -1,0 +1,43 @@
+// fvf_internal.cuh -- launchers shared between the C-ABI layer (fvf_abi.cu)
+// and the kernel files.  Not part of the public interface (include/fvf.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fvf {
+
+constexpr int kMaxNv = 64;
+
+// Pointer table of the pack's input fields, passed to the kernel by value
+// (kernel parameter space), so concurrent calls never share state.
+struct FieldTable {
+    const double *p[kMaxNv];
+};
+
+// Box geometry of a 3D sweep: interior extents n, stored extents N (n + 2g on
+// axes with n > 1, else 1) and ghost offsets g (g where n > 1, else 0).
+struct Box {
+    int64_t n[3];
+    int64_t N[3];
+    int64_t g[3];
+};
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Each launcher enqueues its kernels on `stream`, adds the number of kernels
+// it launched to *launches and returns the first launch error (cudaSuccess
+// if none).  Arguments have already been validated by the caller.
+cudaError_t launch_diffuse2d(void *u, void *v, int64_t nx, int64_t ny, double alpha,
+                             int64_t nsteps, bool fp64, cudaStream_t stream,
+                             uint64_t *launches);
+
+cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
+                             double *out, cudaStream_t stream, uint64_t *launches);
+
+cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
+                              const int64_t n[3], int dir, double *rhs,
+                              cudaStream_t stream, uint64_t *launches);
+
+}  // namespace fvf

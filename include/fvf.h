@@ -1,0 +1,158 @@
+/*
+ * fvf.h -- C ABI of libfvf.so, the GB300 (sm_103a) library of per-cell field
+ * sweeps: the explicit 2D 5-point diffusion step with ping-pong buffers, the
+ * multi-variable WENO input pack and the finite-volume flux-difference
+ * source.
+ *
+ * Sources of the operations (pages, by title and section):
+ *   [Q] Qiita, "Fortran 2018でGPUを高速化する Part 3" ("Fortran 2018 GPU
+ *       acceleration, part 3"): section 3 (update formula, alpha = 0.1,
+ *       stability alpha <= 1/4), section 4 (column-major layout), section 5.1
+ *       (edges written 0 each step), section 5.4 (ping-pong), section 6.1
+ *       (alpha = 0.1_real32 in FP32).
+ *   [M] MFlowCode/MFC pull request #2087, "Collapse only spatial loops in
+ *       per-variable GPU kernels": "Changes" (s_pack_weno_input_arr,
+ *       s_compute_advection_source_term) and "Why this is faster" (one thread
+ *       per spatial cell, variables looped inside the thread).
+ *
+ * Conventions common to every entry point
+ *   - All array pointers are DEVICE pointers owned by the caller (for
+ *     instance torch CUDA tensors) on the current CUDA device; the library
+ *     allocates no device memory and keeps no pointer after returning.
+ *     Pointers to host memory are rejected (FVF_ERR_NOT_DEVICE).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Calls only enqueue work on it and return; nothing is
+ *     synchronised.  A device fault surfaces at the caller's next
+ *     synchronisation, as for any CUDA launch.
+ *   - Every argument is validated on the host before anything is launched.
+ *     On any nonzero status nothing has been enqueued (except FVF_ERR_CUDA,
+ *     which reports a failed launch).  fvf_status_string() names a status.
+ *   - A 3D field with interior extents (n1, n2, n3) and ghost width g is
+ *     stored with extents N_a = n_a + 2g on every axis with n_a > 1 and
+ *     N_a = 1 on an axis with n_a == 1 (so a 2D problem passes n3 = 1).
+ *     Element (j,k,l) of the stored box is at j + N1*(k + N2*l): j is
+ *     contiguous, as in the Fortran arrays of [M].
+ *   - Floating-point results are bit-identical to the plain CPU evaluation
+ *     of the same formulas in the stated operation order with every
+ *     operation rounded to nearest even (no contraction of a multiply and an
+ *     add), except that NaN payloads are not preserved by arithmetic.
+ */
+#ifndef FVF_H_
+#define FVF_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+#define FVF_OK               0  /* success (work enqueued, or nothing to do)      */
+#define FVF_ERR_NULL         1  /* a required pointer is NULL                     */
+#define FVF_ERR_SIZE         2  /* a size is negative, or a product overflows     */
+#define FVF_ERR_DTYPE        3  /* dtype is neither FVF_FP32 nor FVF_FP64         */
+#define FVF_ERR_DIR          4  /* dir is not 0, 1 or 2                           */
+#define FVF_ERR_NV           5  /* nv outside 0..FVF_MAX_NV                       */
+#define FVF_ERR_ALIAS        6  /* an output overlaps an input or the other buffer */
+#define FVF_ERR_ALPHA        7  /* alpha is not finite                            */
+#define FVF_ERR_ALIGN        8  /* a pointer is not aligned to its element size   */
+#define FVF_ERR_NOT_DEVICE   9  /* a pointer is not device memory of this device  */
+#define FVF_ERR_RANGE       10  /* an array runs past the end of its allocation   */
+#define FVF_ERR_CUDA        11  /* a CUDA call failed (see fvf_last_cuda_error)   */
+
+/* dtype values of diffuse2d_step. */
+#define FVF_FP32 0
+#define FVF_FP64 1
+
+/* Largest number of variables weno_pack and advect_rhs accept. */
+#define FVF_MAX_NV 64
+
+/*
+ * diffuse2d_step -- nsteps explicit 5-point diffusion steps with ping-pong
+ * buffers ([Q] sections 3, 5.1, 5.4).
+ *
+ *   u, v    two nx*ny arrays of float (dtype FVF_FP32) or double (FVF_FP64),
+ *           column-major: cell (i,j), 0 <= i < nx, 0 <= j < ny, at i + nx*j.
+ *           u holds the initial field.  They must not overlap.
+ *   alpha   diffusion number; for FP32 it is rounded once to float.  Any
+ *           finite value is accepted (stability, alpha <= 1/4, is the
+ *           caller's business).
+ *   nsteps  number of steps, >= 0.  Step s (1-based) reads u and writes v
+ *           when s is odd, reads v and writes u when s is even.  Each step
+ *           computes, for 1 <= i <= nx-2 and 1 <= j <= ny-2,
+ *               dst(i,j) = c + alpha*((((W + E) + S) + N) - 4c)
+ *           with c = src(i,j), W = src(i-1,j), E = src(i+1,j),
+ *           S = src(i,j-1), N = src(i,j+1), and writes 0 to every edge cell
+ *           of dst.  Edge cells of src are read as they are.
+ *   Result: in v after an odd nsteps, in u after an even nsteps (u untouched
+ *           for nsteps = 0).  The other buffer holds the previous step.
+ *   Empty grids (nx or ny = 0) and nsteps = 0 return FVF_OK and enqueue
+ *   nothing.
+ *   Pointers must be aligned to the element size.
+ */
+int diffuse2d_step(void *u, void *v, int64_t nx, int64_t ny, double alpha,
+                   int64_t nsteps, int dtype, void *stream);
+
+/*
+ * weno_pack -- the multi-variable WENO input pack of [M] ("Changes",
+ * s_pack_weno_input_arr): out(a,b,c,i) = field_i(...) with the swept axis
+ * first.  FP64 bit copy (NaN payloads and signed zeros preserved).
+ *
+ *   fields   HOST array of nv device pointers; field i is a stored box
+ *            (N1 x N2 x N3 doubles, layout above).  Fields may alias each
+ *            other; none may overlap out.
+ *   nv       number of variables, 0..FVF_MAX_NV (0: nothing to do).
+ *   extents  HOST array {n1, n2, n3} of interior extents, each >= 0 (any
+ *            zero: nothing to do).
+ *   ghost    ghost width g >= 0 on every axis whose interior extent is > 1.
+ *   dir      swept axis: 0 = x (j), 1 = y (k), 2 = z (l).
+ *   out      M1*M2*M3*nv doubles, out(a,b,c,i) at a + M1*(b + M2*(c + M3*i)):
+ *              dir 0: out(a,b,c,i) = field_i(a,    b+g2, c+g3), (M1,M2,M3) = (N1,n2,n3)
+ *              dir 1: out(a,b,c,i) = field_i(b+g1, a,    c+g3), (M1,M2,M3) = (N2,n1,n3)
+ *              dir 2: out(a,b,c,i) = field_i(c+g1, b+g2, a   ), (M1,M2,M3) = (N3,n2,n1)
+ *            with g_a = g where n_a > 1, else 0: the swept axis covers its
+ *            ghost cells, the transverse axes their interior cells.
+ */
+int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int ghost,
+              int dir, double *out, void *stream);
+
+/*
+ * advect_rhs -- the finite-volume flux-difference source of [M]
+ * ("Changes", s_compute_advection_source_term), one direction per call,
+ * assigned (not accumulated):
+ *     dir 0: rhs(j,k,l,i) = inv_d(j) * (F(j-1,k,l,i) - F(j,k,l,i))
+ *     dir 1: rhs(j,k,l,i) = inv_d(k) * (F(j,k-1,l,i) - F(j,k,l,i))
+ *     dir 2: rhs(j,k,l,i) = inv_d(l) * (F(j,k,l-1,i) - F(j,k,l,i))
+ * one subtraction then one multiplication, for 0 <= j < n1, 0 <= k < n2,
+ * 0 <= l < n3, 0 <= i < nv.
+ *
+ *   flux     face fluxes, contiguous doubles with the variable slowest and
+ *            one extra entry along the swept axis: extents (n1+1, n2, n3),
+ *            (n1, n2+1, n3) or (n1, n2, n3+1) per variable; face f
+ *            (-1 <= f <= n-1) is stored at position f+1 on that axis.
+ *   inv_d    inverse cell widths along the swept axis (n_dir doubles).
+ *   nv       0..FVF_MAX_NV (0: nothing to do).
+ *   extents  HOST array {n1, n2, n3} of cell counts, each >= 0.
+ *   dir      0, 1 or 2.
+ *   rhs      n1*n2*n3*nv doubles, rhs(j,k,l,i) at j + n1*(k + n2*(l + n3*i));
+ *            must not overlap flux or inv_d.
+ */
+int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
+               int dir, double *rhs, void *stream);
+
+/* Static, NUL-terminated name of a status code ("unknown status" if none). */
+const char *fvf_status_string(int status);
+
+/* The cudaError_t value behind the calling thread's last FVF_ERR_CUDA
+ * (0 if none). */
+int fvf_last_cuda_error(void);
+
+/* Number of kernels this library has launched since it was loaded (all
+ * threads).  Lets a caller count the library's launches in a region. */
+uint64_t fvf_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FVF_H_ */

@@ -1,0 +1,144 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+libfvf.so must load, export exactly the functions include/fvf.h declares,
+and reject bad arguments with the documented status codes before anything
+reaches the GPU.  No call here launches a kernel.
+"""
+from __future__ import annotations
+
+import ctypes
+import re
+import subprocess
+from pathlib import Path
+
+import numpy as np
+import pytest
+
+from finite_volume_field_gb300 import api, buildlib
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "fvf.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    buildlib.build()
+    return api.load()
+
+
+def _declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^[A-Za-z_][\w \t\*]*?\b([A-Za-z_]\w*)\s*\(", text, flags=re.M))
+
+
+def _status_codes():
+    return {m.group(1): int(m.group(2))
+            for m in re.finditer(r"#define\s+(FVF_\w+)\s+(-?\d+)", HEADER.read_text())}
+
+
+def test_header_declares_the_three_sweeps():
+    decl = _declared_functions()
+    assert {"diffuse2d_step", "weno_pack", "advect_rhs", "fvf_status_string"} <= decl
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", str(api.LIB_PATH)], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    exported = {s for s in exported if not s.startswith("_")}
+    assert exported == _declared_functions()
+
+
+def test_status_strings(lib):
+    codes = _status_codes()
+    seen = set()
+    for name, code in codes.items():
+        if name.startswith("FVF_ERR_") or name == "FVF_OK":
+            s = api.status_string(code)
+            assert s != "unknown status"
+            seen.add(s)
+    assert api.status_string(12345) == "unknown status"
+    assert len(seen) == sum(1 for n in codes if n.startswith("FVF_ERR_") or n == "FVF_OK")
+
+
+C = _status_codes()
+E3 = (ctypes.c_int64 * 3)
+
+
+def test_diffuse_validation(lib):
+    f = lib.diffuse2d_step
+    assert f(None, None, 8, 8, 0.1, 1, 2, None) == C["FVF_ERR_DTYPE"]
+    assert f(None, None, -1, 8, 0.1, 1, 1, None) == C["FVF_ERR_SIZE"]
+    assert f(None, None, 8, 8, 0.1, -1, 1, None) == C["FVF_ERR_SIZE"]
+    assert f(None, None, 1 << 40, 1 << 40, 0.1, 1, 1, None) == C["FVF_ERR_SIZE"]
+    assert f(None, None, 8, 8, float("inf"), 1, 1, None) == C["FVF_ERR_ALPHA"]
+    assert f(None, None, 8, 8, float("nan"), 1, 0, None) == C["FVF_ERR_ALPHA"]
+    assert f(None, None, 8, 8, 1e300, 1, 0, None) == C["FVF_ERR_ALPHA"]   # inf once rounded to FP32
+    assert f(None, None, 8, 8, 0.1, 0, 1, None) == C["FVF_OK"]            # nothing to do
+    assert f(None, None, 0, 8, 0.1, 5, 1, None) == C["FVF_OK"]            # empty grid
+    assert f(None, 4096, 8, 8, 0.1, 1, 1, None) == C["FVF_ERR_NULL"]
+    assert f(4100, 8192, 8, 8, 0.1, 1, 1, None) == C["FVF_ERR_ALIGN"]     # 4100 % 8 != 0
+    # fake addresses: the device-memory check runs before the overlap check
+    assert f(4096, 4096 + 8, 8, 8, 0.1, 1, 1, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_host_memory_rejected(lib):
+    """A host (numpy) buffer is not device memory: rejected before launch."""
+    u = np.zeros(64, dtype=np.float64)
+    v = np.zeros(64, dtype=np.float64)
+    st = lib.diffuse2d_step(u.ctypes.data, v.ctypes.data, 8, 8, 0.1, 1, 1, None)
+    assert st == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_pack_validation(lib):
+    f = lib.weno_pack
+    vp = ctypes.c_void_p
+    table = (vp * 2)(4096, 8192)
+    ext = E3(3, 4, 5)
+    assert f(table, 2, None, 1, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert f(table, 2, ext, 1, 3, 65536, None) == C["FVF_ERR_DIR"]
+    assert f(table, 2, ext, 1, -1, 65536, None) == C["FVF_ERR_DIR"]
+    assert f(table, 65, ext, 1, 0, 65536, None) == C["FVF_ERR_NV"]
+    assert f(table, -1, ext, 1, 0, 65536, None) == C["FVF_ERR_NV"]
+    assert f(table, 2, ext, -1, 0, 65536, None) == C["FVF_ERR_SIZE"]
+    assert f(table, 2, E3(3, -4, 5), 1, 0, 65536, None) == C["FVF_ERR_SIZE"]
+    assert f(table, 0, ext, 1, 0, None, None) == C["FVF_OK"]
+    assert f(table, 2, E3(3, 0, 5), 1, 0, None, None) == C["FVF_OK"]
+    assert f(table, 2, ext, 1, 0, None, None) == C["FVF_ERR_NULL"]
+    assert f(None, 2, ext, 1, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert f((vp * 2)(4096, None), 2, ext, 1, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert f(table, 2, ext, 1, 0, 65540, None) == C["FVF_ERR_ALIGN"]
+    assert f((vp * 2)(4100, 8192), 2, ext, 1, 0, 65536, None) == C["FVF_ERR_ALIGN"]
+    assert f(table, 2, ext, 1, 0, 4096 + 800, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_rhs_validation(lib):
+    f = lib.advect_rhs
+    ext = E3(3, 4, 5)
+    assert f(4096, 8192, 2, None, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert f(4096, 8192, 2, ext, 3, 65536, None) == C["FVF_ERR_DIR"]
+    assert f(4096, 8192, 65, ext, 0, 65536, None) == C["FVF_ERR_NV"]
+    assert f(4096, 8192, 2, E3(-3, 4, 5), 0, 65536, None) == C["FVF_ERR_SIZE"]
+    assert f(4096, 8192, 0, ext, 0, None, None) == C["FVF_OK"]
+    assert f(None, 8192, 2, ext, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert f(4096, None, 2, ext, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert f(4096, 8192, 2, ext, 0, None, None) == C["FVF_ERR_NULL"]
+    assert f(4097, 8192, 2, ext, 0, 65536, None) == C["FVF_ERR_ALIGN"]
+    assert f(4096, 65536, 2, ext, 0, 4096 + 640, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    u = torch.zeros(8, 8, dtype=torch.float64)
+    with pytest.raises(ValueError):
+        api.diffuse2d_step(u, u.clone(), 8, 8, 0.1, 1, stream=0)
+
+
+def test_launch_count_starts_at_zero_without_launches(lib):
+    assert api.launch_count() >= 0

@@ -1,0 +1,177 @@
+"""GPU parity of diffuse2d_step against the CPU oracle, through the C ABI.
+
+The bar is bit-exactness: the kernel and the oracle evaluate
+c + alpha*((((W+E)+S)+N) - 4c) with every operation rounded to nearest even,
+so every cell must match bit for bit (NaN payloads excepted).
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from finite_volume_field_gb300 import api, inputs
+from tests.gpu_util import (assert_bits_equal, canary_intact, guarded, to_dev, to_host,
+                            torch_cuda)
+
+pytestmark = pytest.mark.gpu
+
+DT = {np.float32: api.FVF_FP32, np.float64: api.FVF_FP64}
+
+
+def _run_gpu(torch, u0: np.ndarray, nsteps: int, alpha=0.1, v0=None, stream=None):
+    ny, nx = u0.shape
+    u = to_dev(u0)
+    v = to_dev(np.zeros_like(u0) if v0 is None else v0)
+    api.diffuse2d_step(u, v, nx, ny, alpha, nsteps, DT[u0.dtype.type], stream=stream)
+    torch.cuda.synchronize()
+    return to_host(u), to_host(v)
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float32])
+def test_centre_impulse_64x64_32_steps(dt):
+    """The 64x64 centre-impulse case, 32 steps (result in u)."""
+    torch = torch_cuda()
+    u0 = oracle.centre_impulse(64, 64, dt)
+    gu, gv = _run_gpu(torch, u0, 32)
+    ou, ov, in_v = oracle.diffuse2d(u0, 32, return_both=True)
+    assert not in_v
+    assert_bits_equal(gu, ou, what="u (result)")
+    assert_bits_equal(gv, ov, what="v (previous step)")
+    one_u, one_v = _run_gpu(torch, u0, 1)
+    assert one_v[31, 31] == dt(0.6) and one_v[31, 32] == dt(0.1)
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float32])
+@pytest.mark.parametrize("steps", [7, 8, 31, 32])
+def test_validation_matrix_31x27(dt, steps):
+    """The Qiita page's check matrix (section 10 check scripts): both
+    precisions, steps 7/8/31/32 on 31x27; both buffers bit-exact."""
+    torch = torch_cuda()
+    u0 = oracle.centre_impulse(31, 27, dt)
+    gu, gv = _run_gpu(torch, u0, steps)
+    ou, ov, in_v = oracle.diffuse2d(u0, steps, return_both=True)
+    assert in_v == (steps % 2 == 1)
+    assert_bits_equal(gu, ou, what="u")
+    assert_bits_equal(gv, ov, what="v")
+    res = gv if in_v else gu
+    assert oracle.physical_check(res)["ok"]
+
+
+RAGGED = [(1, 1), (2, 2), (3, 3), (1, 9), (9, 1), (5, 5), (3, 17), (17, 3), (33, 65), (65, 33),
+          (127, 129), (130, 7), (1000, 3), (3, 1000), (257, 255), (513, 67)]
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float32])
+@pytest.mark.parametrize("nx,ny", RAGGED)
+def test_ragged_random_fields(dt, nx, ny):
+    """Sizes that are not multiples of any block or vector width, tiny
+    degenerate grids (no interior) and random values everywhere, edges
+    included (the kernel must read source edges as they are and write zero
+    edges)."""
+    torch = torch_cuda()
+    n = nx * ny
+    vals = (inputs.uniform_f32(7, nx * 1000 + ny, n) if dt == np.float32
+            else inputs.uniform_f64(7, nx * 1000 + ny, n))
+    u0 = vals.reshape(ny, nx)
+    v0 = (inputs.uniform_f32(8, nx, n) if dt == np.float32
+          else inputs.uniform_f64(8, nx, n)).reshape(ny, nx)
+    for steps in (1, 2, 5):
+        gu, gv = _run_gpu(torch, u0, steps, v0=v0)
+        ou, ov, _ = oracle.diffuse2d(u0, steps, v0=v0, return_both=True)
+        assert_bits_equal(gu, ou, what=f"u {nx}x{ny} {steps}")
+        assert_bits_equal(gv, ov, what=f"v {nx}x{ny} {steps}")
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float32])
+def test_special_values(dt):
+    """Huge values (4c overflows: the kernel's two-operation branch), inf,
+    NaN, signed zeros and subnormals, with alpha 0.1 and 0.3; bit-exact up to
+    NaN payloads."""
+    torch = torch_cuda()
+    nx, ny = 37, 23
+    rng_bits = inputs.random_bits(3, 1, nx * ny)
+    if dt == np.float64:
+        u0 = (inputs.uniform_f64(3, 2, nx * ny) - 0.5).reshape(ny, nx)
+        specials = [np.inf, -np.inf, np.nan, -0.0, 5e-324, 2.0 ** 1022, -2.0 ** 1023,
+                    1.7e308, 2.0 ** -1022, 3.0 * 2.0 ** 1021]
+    else:
+        u0 = (inputs.uniform_f32(3, 2, nx * ny) - np.float32(0.5)).reshape(ny, nx)
+        specials = [np.inf, -np.inf, np.nan, -0.0, 1e-45, 2.0 ** 126, -2.0 ** 127, 3.3e38,
+                    2.0 ** -126, 3.0 * 2.0 ** 125]
+    flat = u0.reshape(-1)
+    for s, b in zip(specials, rng_bits[: len(specials)]):
+        flat[int(b % (nx * ny))] = dt(s)
+    for alpha in (0.1, 0.3):
+        for steps in (1, 3):
+            gu, gv = _run_gpu(torch, u0, steps, alpha=alpha)
+            ou, ov, _ = oracle.diffuse2d(u0, steps, alpha=alpha, return_both=True)
+            assert_bits_equal(gu, ou, nan_payloads=False, what=f"u a={alpha} s={steps}")
+            assert_bits_equal(gv, ov, nan_payloads=False, what=f"v a={alpha} s={steps}")
+
+
+def test_guard_band_and_nonzero_stream():
+    """Writes stay inside the nx*ny cells (canaries after both buffers are
+    untouched) and the work runs on the caller's stream."""
+    torch = torch_cuda()
+    nx, ny = 301, 77
+    u0 = inputs.diffusion_field(nx, ny, np.float64, seed=inputs.config_seed(2))
+    uw, u = guarded(torch, nx * ny, torch.float64)
+    vw, v = guarded(torch, nx * ny, torch.float64)
+    u.copy_(torch.from_numpy(u0.reshape(-1)))
+    v.zero_()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        api.diffuse2d_step(u, v, nx, ny, 0.1, 9, api.FVF_FP64, stream=s)
+    s.synchronize()
+    assert canary_intact(torch, uw, nx * ny) and canary_intact(torch, vw, nx * ny)
+    want = oracle.diffuse2d(u0, 9)
+    assert_bits_equal(to_host(v).reshape(ny, nx), want)
+
+
+def test_device_errors_are_status_codes():
+    """A too-small device buffer or a host pointer is refused before launch."""
+    torch = torch_cuda()
+    u = torch.zeros(100, dtype=torch.float64, device="cuda")
+    v = torch.zeros(100, dtype=torch.float64, device="cuda")
+    # 20x20 cells do not fit in 100 elements of a fresh allocation; torch's
+    # caching allocator may hand out a larger block, so use a 1 GiB grid.
+    with pytest.raises(api.FvfError) as e:
+        api.diffuse2d_step(u, v, 1 << 15, 1 << 15, 0.1, 1, api.FVF_FP64)
+    assert e.value.status == 10
+    h = np.zeros(100)
+    with pytest.raises(api.FvfError) as e:
+        api.diffuse2d_step(h.ctypes.data, v, 10, 10, 0.1, 1, api.FVF_FP64)
+    assert e.value.status == 9
+    torch.cuda.synchronize()
+
+
+def test_launch_count():
+    """One kernel launch per step (counted by the library)."""
+    torch = torch_cuda()
+    u = torch.zeros(64 * 64, dtype=torch.float64, device="cuda")
+    v = torch.zeros_like(u)
+    before = api.launch_count()
+    api.diffuse2d_step(u, v, 64, 64, 0.1, 5, api.FVF_FP64)
+    torch.cuda.synchronize()
+    assert api.launch_count() - before >= 1
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_full_size_8192_200_steps(dt):
+    """The 8192 x 8192, 200-step workload (interior uniform [0,1) from the
+    seed, zero edges) in the same launch configuration the benchmark times,
+    compared cell by cell with the multithreaded oracle."""
+    torch = torch_cuda()
+    nx = ny = 8192
+    u0 = inputs.diffusion_field(nx, ny, dt, seed=inputs.config_seed(2),
+                                stream=0 if dt == np.float32 else 1)
+    u = to_dev(u0)
+    v = torch.zeros_like(u)
+    api.diffuse2d_step(u, v, nx, ny, 0.1, 200, DT[dt])
+    torch.cuda.synchronize()
+    got = to_host(u)
+    del u, v
+    want = oracle.diffuse2d(u0, 200, nthreads=oracle.max_threads())
+    assert_bits_equal(got, want, what=f"8192^2 {dt.__name__}")
+    assert oracle.physical_check(got)["min"] >= 0
