@@ -5,6 +5,10 @@
 //     rhs(j,k,l,i) = inv_d(c) * (F(c-1) - F(c))
 // along the swept axis c, one subtraction then one multiplication, each
 // rounded to nearest even (round-to-nearest intrinsics, never contracted).
+// Two FP64 operations per element keep this kernel on GB300's FP64 unit:
+// moving the subtraction to the integer pipes (fp64_emu.cuh) was measured
+// slower here (the integer ALU pipe saturates first), unlike in the
+// diffusion update.
 //
 // Mapping ("Why this is faster" on the same page): one thread per spatial
 // cell; the inverse spacing is loaded once per cell, outside the variable

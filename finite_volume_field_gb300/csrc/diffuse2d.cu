@@ -14,17 +14,48 @@
 // two-operation form instead, so the result is bit-identical for every
 // input.
 //
-// Thread mapping: the contiguous index i runs along the lanes of a warp, so
-// every row access of a warp is one coalesced segment; one thread updates one
-// cell (the spatial loops are the parallel ones, as the MFC pull request
-// #2087 recommends for per-cell sweeps).
+// Kernels
+//   march  (rows 16-byte aligned, nx a multiple of the vector width): one
+//          thread owns one 16-byte vector of cells (4 FP32 or 2 FP64) of a
+//          column strip and walks down the strip, keeping the rows j-1, j,
+//          j+1 in registers and prefetching row j+2, so every element is
+//          read from HBM once per step (plus one row per strip boundary).
+//          The W/E neighbours across vectors come from the adjacent lanes by
+//          warp shuffle; the two warp-edge lanes load their outside
+//          neighbour together with the row.  The grid is one wave: as many
+//          blocks as fit on the SMs at once, each taking an equal band of
+//          rows.
+//   scalar (any size or alignment): one thread per cell.
+#include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
+
+// How the FP64 update splits its additions between the FP64 unit and the
+// integer pipes (fp64_emu.cuh).  Every split gives bit-identical results; the
+// best one balances the two kinds of pipe.
+//   FVF_FP64_EMU_SUMS: how many of the three neighbour sums (W+E, +S, +N, in
+//                      that order) run on the integer pipes (0..3);
+//   FVF_FP64_EMU_T:    1 to also compute s - 4c on the integer pipes.
+#ifndef FVF_FP64_EMU_SUMS
+#define FVF_FP64_EMU_SUMS 2
+#endif
+#ifndef FVF_FP64_EMU_T
+#define FVF_FP64_EMU_T 0
+#endif
 
 namespace fvf {
 namespace {
 
 template <typename T>
 struct Rn;
+
+// s - fl(4c) with two roundings, for the cells where 4c overflows.  Kept out
+// of line so that the compiler does not evaluate it for every cell.
+static __device__ __noinline__ double sub4_two_ops(double s, double c) {
+    return __dsub_rn(s, __dmul_rn(4.0, c));
+}
+static __device__ __noinline__ float sub4_two_ops(float s, float c) {
+    return __fsub_rn(s, __fmul_rn(4.0f, c));
+}
 
 template <>
 struct Rn<double> {
@@ -33,7 +64,7 @@ struct Rn<double> {
     // s - 4c rounded once.
     static __device__ __forceinline__ double sub4(double s, double c) {
         if ((__double2hiint(c) & 0x7ff00000) >= 0x7fd00000)  // |c| >= 2^1022, NaN, Inf
-            return __dsub_rn(s, __dmul_rn(4.0, c));
+            return sub4_two_ops(s, c);
         return __fma_rn(-4.0, c, s);
     }
 };
@@ -44,7 +75,7 @@ struct Rn<float> {
     static __device__ __forceinline__ float mul(float a, float b) { return __fmul_rn(a, b); }
     static __device__ __forceinline__ float sub4(float s, float c) {
         if ((__float_as_uint(c) & 0x7f800000u) >= 0x7e800000u)  // |c| >= 2^126, NaN, Inf
-            return __fsub_rn(s, __fmul_rn(4.0f, c));
+            return sub4_two_ops(s, c);
         return __fmaf_rn(-4.0f, c, s);
     }
 };
@@ -55,6 +86,34 @@ __device__ __forceinline__ T update(T c, T w, T e, T s, T n, T alpha) {
     const T sum = R::add(R::add(R::add(w, e), s), n);
     return R::add(c, R::mul(alpha, R::sub4(sum, c)));
 }
+
+// FP64 update with part of the additions on the integer pipes; the same
+// operations in the same order, each correctly rounded, so the same bits.
+template <>
+__device__ __forceinline__ double update<double>(double c, double w, double e, double s,
+                                                 double n, double alpha) {
+    double sum = FVF_FP64_EMU_SUMS >= 1 ? emu::add_same_sign(w, e) : __dadd_rn(w, e);
+    sum = FVF_FP64_EMU_SUMS >= 2 ? emu::add_same_sign(sum, s) : __dadd_rn(sum, s);
+    sum = FVF_FP64_EMU_SUMS >= 3 ? emu::add_same_sign(sum, n) : __dadd_rn(sum, n);
+    double t;
+#if FVF_FP64_EMU_T
+    // -4c is c with the exponent raised by two and the sign flipped, exactly,
+    // when c is normal and 4c stays normal (biased exponent 1..2044).
+    const uint64_t cb = emu::bits(c);
+    const uint32_t ec = (uint32_t)(cb >> 52) & 0x7FFu;
+    if (ec - 1u < 2044u)
+        t = emu::add(sum, emu::from_bits((cb + (2ull << 52)) ^ emu::kSign));
+    else
+        t = Rn<double>::sub4(sum, c);
+#else
+    t = Rn<double>::sub4(sum, c);
+#endif
+    return __dadd_rn(c, __dmul_rn(alpha, t));
+}
+
+// ---------------------------------------------------------------------------
+// Scalar kernel (any size, any element alignment)
+// ---------------------------------------------------------------------------
 
 constexpr int kBx = 64;  // threads along i
 constexpr int kBy = 4;   // threads along j
@@ -76,16 +135,159 @@ diffuse_step_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Row-marching vector kernel
+// ---------------------------------------------------------------------------
+
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+    static constexpr int n = 4;
+    float v[4];
+};
+template <>
+struct Vec16<double> {
+    static constexpr int n = 2;
+    double v[2];
+};
+
+template <typename T>
+__device__ __forceinline__ Vec16<T> load16(const T *p) {
+    Vec16<T> r;
+    if constexpr (sizeof(T) == 4) {
+        const float4 q = __ldg(reinterpret_cast<const float4 *>(p));
+        r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[3] = q.w;
+    } else {
+        const double2 q = __ldg(reinterpret_cast<const double2 *>(p));
+        r.v[0] = q.x; r.v[1] = q.y;
+    }
+    return r;
+}
+
+template <typename T>
+__device__ __forceinline__ void store16(T *p, const Vec16<T> &r) {
+    if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4 *>(p) = make_float4(r.v[0], r.v[1], r.v[2], r.v[3]);
+    } else {
+        *reinterpret_cast<double2 *>(p) = make_double2(r.v[0], r.v[1]);
+    }
+}
+
+constexpr int kMarchThreads = 128;
+
+// One row of a thread's strip: the vector plus the two scalar neighbours
+// that lanes 0 and 31 fetch for the warp (unused in other lanes).
+template <typename T>
+struct MarchRow {
+    Vec16<T> c;
+    T w_out, e_out;
+};
+
+template <typename T>
+__device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int64_t nx,
+                                                  int64_t ny, int64_t j, int64_t col, int lane,
+                                                  bool active) {
+    constexpr int V = Vec16<T>::n;
+    MarchRow<T> r;
+#pragma unroll
+    for (int k = 0; k < V; ++k) r.c.v[k] = T(0);
+    r.w_out = T(0);
+    r.e_out = T(0);
+    if (active && j >= 0 && j < ny) {
+        const T *row = src + nx * j;
+        r.c = load16<T>(row + col);
+        if (lane == 0 && col > 0) r.w_out = __ldg(row + col - 1);
+        if (lane == 31 && col + V < nx) r.e_out = __ldg(row + col + V);
+    }
+    return r;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMarchThreads)
+diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
+                     int64_t rows_per_block, T alpha) {
+    constexpr int V = Vec16<T>::n;
+    const int lane = threadIdx.x & 31;
+    const int64_t col = ((int64_t)blockIdx.x * kMarchThreads + threadIdx.x) * V;
+    const bool active = col < nx;
+    const int64_t j0 = (int64_t)blockIdx.y * rows_per_block;
+    const int64_t j1 = min(j0 + rows_per_block, ny);
+
+    MarchRow<T> rs = march_load<T>(src, nx, ny, j0 - 1, col, lane, active);
+    MarchRow<T> rc = march_load<T>(src, nx, ny, j0, col, lane, active);
+    MarchRow<T> rn = march_load<T>(src, nx, ny, j0 + 1, col, lane, active);
+    for (int64_t j = j0; j < j1; ++j) {
+        const MarchRow<T> rnn = march_load<T>(src, nx, ny, j + 2, col, lane, active);
+        // W neighbour of element 0 and E neighbour of element V-1.
+        T w_in = __shfl_up_sync(0xffffffffu, rc.c.v[V - 1], 1);
+        T e_in = __shfl_down_sync(0xffffffffu, rc.c.v[0], 1);
+        if (lane == 0) w_in = rc.w_out;
+        if (lane == 31) e_in = rc.e_out;
+        Vec16<T> out;
+        const bool edge_row = (j == 0) || (j == ny - 1);
+#pragma unroll
+        for (int k = 0; k < V; ++k) {
+            const T w = k > 0 ? rc.c.v[k - 1] : w_in;
+            const T e = k < V - 1 ? rc.c.v[k + 1] : e_in;
+            const int64_t i = col + k;
+            const bool edge = edge_row || i == 0 || i == nx - 1;
+            out.v[k] = edge ? T(0) : update<T>(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha);
+        }
+        if (active) store16<T>(dst + nx * j + col, out);
+        rs = rc;
+        rc = rn;
+        rn = rnn;
+    }
+}
+
+template <typename T>
+int march_blocks_per_sm() {
+    static int cached = 0;
+    if (cached == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, diffuse_march_kernel<T>,
+                                                          kMarchThreads, 0) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            n = 8;
+        }
+        cached = n;
+    }
+    return cached;
+}
+
 template <typename T>
 cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
                 cudaStream_t stream, uint64_t *launches) {
-    const dim3 block(kBx, kBy);
-    const int64_t gy = (ny + kBy - 1) / kBy;
-    const dim3 grid((unsigned)((nx + kBx - 1) / kBx), (unsigned)(gy < 65535 ? gy : 65535));
+    constexpr int V = Vec16<T>::n;
+    const bool vec_ok = (nx % V == 0) && ((uintptr_t)u % 16 == 0) && ((uintptr_t)v % 16 == 0) &&
+                        nx >= 2 * V;
+    dim3 grid, block;
+    int64_t rows = 0;
+    if (vec_ok) {
+        const int64_t bx = (nx / V + kMarchThreads - 1) / kMarchThreads;
+        const int64_t resident = (int64_t)march_blocks_per_sm<T>() * sm_count();
+        int64_t by = resident / bx;
+        if (by < 1) by = 1;
+        if (by > ny) by = ny;
+        rows = (ny + by - 1) / by;
+        by = (ny + rows - 1) / rows;
+        if (bx > 0x7fffffff || by > 65535) return cudaErrorInvalidValue;
+        grid = dim3((unsigned)bx, (unsigned)by);
+        block = dim3(kMarchThreads);
+    } else {
+        const int64_t gy = (ny + kBy - 1) / kBy;
+        grid = dim3((unsigned)((nx + kBx - 1) / kBx), (unsigned)(gy < 65535 ? gy : 65535));
+        block = dim3(kBx, kBy);
+    }
     for (int64_t s = 1; s <= nsteps; ++s) {
         const T *src = (s & 1) ? u : v;
         T *dst = (s & 1) ? v : u;
-        diffuse_step_kernel<T><<<grid, block, 0, stream>>>(src, dst, nx, ny, alpha);
+        if (vec_ok)
+            diffuse_march_kernel<T><<<grid, block, 0, stream>>>(src, dst, nx, ny, rows, alpha);
+        else
+            diffuse_step_kernel<T><<<grid, block, 0, stream>>>(src, dst, nx, ny, alpha);
         ++*launches;
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -1,0 +1,225 @@
+// fp64_emu.cuh -- IEEE 754 binary64 addition on the integer pipes.
+//
+// GB300 issues FP64 adds, multiplies and FMAs at about 1/70 of its FP32 and
+// integer rate, so a sweep doing a few FP64 operations per element is bound
+// by the FP64 pipe well below the HBM roof.  The functions here compute the
+// correctly rounded (round-to-nearest-even) binary64 sum with 32/64-bit
+// integer instructions, which run on the full-rate pipes in parallel with the
+// FP64 unit, and contain no FP64 instruction at all.  The result is
+// bit-identical to a hardware add for every input except that every NaN
+// result is the one quiet NaN 0x7FFFFFFFFFFFFFFF.
+//
+// Method: the textbook binary floating-point addition (J.-M. Muller et al.,
+// "Handbook of Floating-Point Arithmetic", 2nd ed., chapter 7; D. Goldberg,
+// "What every computer scientist should know about floating-point
+// arithmetic", 1991):
+//   1. order the operands by magnitude, so |x| >= |y|;
+//   2. place both significands (53 bits, implicit one included) in a 64-bit
+//      frame with 10 guard bits below them: X = mx << 10 in [2^62, 2^63);
+//   3. shift Y right by the exponent difference d;
+//   4. add (same signs) or subtract (opposite signs) the frames;
+//   5. normalise so the leading one is bit 63;
+//   6. round to nearest, ties to even, at bit 11, and pack sign, exponent
+//      and significand (a carry out of the significand on rounding moves
+//      into the exponent field by the addition itself).
+// Fast path and slow path.  The fast path handles normal operands with
+// d < 32 whose result is normal, and drops the bits that step 3 shifts out of
+// the frame (only when d > 10).  Dropped bits are less than one unit of the
+// frame, i.e. less than 2^-10 of the result's last place, so they can only
+// change the rounding when the round field is exactly one half.  That case,
+// exact cancellation or a cancellation of 31 bits or more, d >= 32, and all
+// non-normal operands and results go to the slow path: the complete
+// algorithm with a sticky bit (every bit shifted out OR-ed into bit 0 of the
+// frame), subnormals and the IEEE special values, still in integer
+// arithmetic.  No hardware FP64 instruction appears anywhere, and the slow
+// path is inline code on the bit patterns (a call taking or returning
+// doubles was measured to add FP64-pipe instructions to every element).
+// The functions are __host__ __device__ so the same code can be checked on
+// the CPU against the host's IEEE addition.
+#pragma once
+
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define FVF_HD __host__ __device__ __forceinline__
+#else
+#define FVF_HD inline
+#endif
+
+namespace fvf {
+namespace emu {
+
+constexpr uint64_t kSign = 0x8000000000000000ull;
+constexpr uint64_t kFrac = 0x000FFFFFFFFFFFFFull;
+constexpr uint64_t kHidden = 0x0010000000000000ull;
+
+FVF_HD uint64_t bits(double x) {
+#if defined(__CUDA_ARCH__)
+    return (uint64_t)__double_as_longlong(x);
+#else
+    uint64_t u;
+    __builtin_memcpy(&u, &x, 8);
+    return u;
+#endif
+}
+
+FVF_HD double from_bits(uint64_t u) {
+#if defined(__CUDA_ARCH__)
+    return __longlong_as_double((long long)u);
+#else
+    double x;
+    __builtin_memcpy(&x, &u, 8);
+    return x;
+#endif
+}
+
+FVF_HD int clz64(uint64_t x) {
+#if defined(__CUDA_ARCH__)
+    return __clzll((long long)x);
+#else
+    return x ? __builtin_clzll(x) : 64;
+#endif
+}
+
+FVF_HD int clz32(uint32_t x) {
+#if defined(__CUDA_ARCH__)
+    return __clz((int)x);
+#else
+    return x ? __builtin_clz(x) : 32;
+#endif
+}
+
+constexpr uint64_t kInf = 0x7FF0000000000000ull;
+// The NaN every NaN-valued sum returns (any NaN is a correct IEEE result;
+// this is the quiet NaN the GPU's own FP64 unit produces).
+constexpr uint64_t kQuietNaN = 0x7FFFFFFFFFFFFFFFull;
+
+// Complete binary64 addition in integer arithmetic, every input: NaNs and
+// infinities by the IEEE rules, signed zeros, subnormal operands (biased
+// exponent 0 read as 1 without the implicit one), any exponent difference
+// (a sticky bit stands for the bits shifted out of the frame), gradual
+// underflow (a result below the normal range is shifted right into the
+// subnormal encoding, sticky kept, before rounding) and overflow to
+// infinity.
+FVF_HD uint64_t add_full_int(uint64_t A, uint64_t B) {
+    const uint64_t mA = A & ~kSign, mB = B & ~kSign;
+    if (mA > kInf || mB > kInf) return kQuietNaN;
+    if (mA == kInf || mB == kInf) {
+        if (mA == kInf && mB == kInf && ((A ^ B) & kSign)) return kQuietNaN;  // inf - inf
+        return mA == kInf ? A : B;
+    }
+    const bool swap = mA < mB;
+    const uint64_t X = swap ? B : A;             // larger magnitude (its sign wins)
+    const uint64_t mx = swap ? mB : mA, my = swap ? mA : mB;
+    if (my == 0) return mx == 0 ? (A & B & kSign) : X;   // +0 unless both are -0
+    uint32_t ex = (uint32_t)(mx >> 52), ey = (uint32_t)(my >> 52);
+    uint64_t fx = mx & kFrac, fy = my & kFrac;
+    if (ex) fx |= kHidden; else ex = 1;
+    if (ey) fy |= kHidden; else ey = 1;
+    fx <<= 10;                                   // <= 2^63
+    fy <<= 10;
+    const uint32_t d = ex - ey;
+    uint64_t al;
+    if (d < 64) {
+        al = fy >> d;
+        al |= (uint64_t)((al << d) != fy);       // sticky
+    } else {
+        al = 1;
+    }
+    const bool sub = ((A ^ B) & kSign) != 0;
+    uint64_t s = sub ? fx - al : fx + al;
+    if (s == 0) return 0;                        // exact cancellation: +0
+    const int lz = clz64(s);
+    s <<= lz;                                    // leading one at bit 63
+    int e = (int)ex + 1 - lz;                    // biased exponent of the result
+    if (e < 1) {                                 // below the normal range
+        const int sh = 1 - e;
+        uint64_t t = sh < 64 ? (s >> sh) : 0;
+        t |= (uint64_t)(sh < 64 ? ((t << sh) != s) : (s != 0));
+        s = t;
+        e = 1;
+    }
+    uint64_t mant = s >> 11;
+    const uint32_t rb = (uint32_t)s & 0x7FFu;    // round bits, sticky jammed in
+    mant += (rb + (uint32_t)(mant & 1) + 0x3FFu) >> 11;
+    if (e >= 0x7FF) return (X & kSign) | kInf;
+    // a carry out of the significand moves into the exponent field (also from
+    // the largest subnormal to the smallest normal, and to infinity)
+    return (X & kSign) | (((uint64_t)(e - 1) << 52) + mant);
+}
+
+// Fast path of a + b (any signs).  Returns false when the slow path is
+// needed.
+FVF_HD bool add_fast_int(uint64_t A, uint64_t B, uint64_t *out) {
+    const uint64_t mA = A & ~kSign, mB = B & ~kSign;
+    const bool swap = mA < mB;
+    const uint64_t X = swap ? B : A;
+    const uint64_t mx = swap ? mB : mA, my = swap ? mA : mB;
+    const uint32_t ex = (uint32_t)(mx >> 52), ey = (uint32_t)(my >> 52);
+    const uint32_t d = ex - ey;
+    const uint64_t fx = ((mx & kFrac) | kHidden) << 10;
+    const uint64_t fy = ((my & kFrac) | kHidden) << 10;
+    const uint64_t al = fy >> (d & 31);
+    const bool sub = ((A ^ B) & kSign) != 0;
+    uint64_t s = sub ? fx - al : fx + al;
+    // Leading zeros counted in the high word only: a zero high word means a
+    // cancellation of 31 or more bits, which the slow path handles.
+    const int lz = clz32((uint32_t)(s >> 32));
+    s <<= (lz & 31);
+    const int e = (int)ex + 1 - lz;
+    uint64_t mant = s >> 11;
+    const uint32_t rb = (uint32_t)s & 0x7FFu;
+    mant += (rb + (uint32_t)(mant & 1) + 0x3FFu) >> 11;
+    const bool ok = (ey != 0) & (ex != 0x7FF) & (d < 32) & (lz < 32) & (e > 0) & (e < 0x7FF) &
+                    !((d > 10) & (rb == 0x400u));
+    *out = (X & kSign) | (((uint64_t)(e - 1) << 52) + mant);
+    return ok;
+}
+
+// Fast path of a + b for operands of the same sign (no cancellation: the
+// leading one ends in bit 62 or 63, so normalisation is a one-bit choice).
+FVF_HD bool add_same_sign_fast_int(uint64_t A, uint64_t B, uint64_t *out) {
+    const bool swap = A < B;                     // same sign: raw order = magnitude order
+    const uint64_t mx = (swap ? B : A) & ~kSign, my = (swap ? A : B) & ~kSign;
+    const uint32_t ex = (uint32_t)(mx >> 52), ey = (uint32_t)(my >> 52);
+    const uint32_t d = ex - ey;
+    const uint64_t fx = ((mx & kFrac) | kHidden) << 10;
+    const uint64_t fy = ((my & kFrac) | kHidden) << 10;
+    uint64_t s = fx + (fy >> (d & 31));          // [2^62, 2^64)
+    const uint32_t carry = (uint32_t)(s >> 63);
+    s <<= (carry ^ 1u);                          // leading one at bit 63
+    const int e = (int)ex + (int)carry;
+    uint64_t mant = s >> 11;
+    const uint32_t rb = (uint32_t)s & 0x7FFu;
+    mant += (rb + (uint32_t)(mant & 1) + 0x3FFu) >> 11;
+    const bool ok = (((A ^ B) & kSign) == 0) & (ey != 0) & (ex != 0x7FF) & (d < 32) &
+                    (e < 0x7FF) & !((d > 10) & (rb == 0x400u));
+    *out = (A & kSign) | (((uint64_t)(e - 1) << 52) + mant);
+    return ok;
+}
+
+// Correctly rounded a + b on the integer pipes (bits in, bits out).  The
+// slow path is inline and works on the bit patterns only: no call and no
+// FP64 value crosses a branch, which on this GPU would cost FP64-pipe
+// instructions for every element.
+FVF_HD uint64_t add_bits(uint64_t A, uint64_t B) {
+    uint64_t r;
+    if (!add_fast_int(A, B, &r)) r = add_full_int(A, B);
+    return r;
+}
+
+FVF_HD uint64_t add_same_sign_bits(uint64_t A, uint64_t B) {
+    uint64_t r;
+    if (!add_same_sign_fast_int(A, B, &r)) r = add_full_int(A, B);
+    return r;
+}
+
+FVF_HD double add(double a, double b) { return from_bits(add_bits(bits(a), bits(b))); }
+
+// Fastest when a and b have the same sign; correct for any operands.
+FVF_HD double add_same_sign(double a, double b) {
+    return from_bits(add_same_sign_bits(bits(a), bits(b)));
+}
+
+}  // namespace emu
+}  // namespace fvf

@@ -49,12 +49,16 @@ pack_x_kernel(FieldTable t, int nv, int64_t N1, int64_t N2, int64_t n2, int64_t 
 //   z: a = l (0..N3-1), jj = j (interior), q = k (interior); M = (N3, n2, n1)
 //      src = (jj+g1) + N1*((q+g2) + N2*a),  dst = a + N3*(q + n2*jj)
 // src = (jj + g1) + sa*a + sq*(q + gq); dst = a + da*jj + dq*q.
+// The tile is double-buffered across variables: the loads of variable i+1
+// are in flight while variable i is stored, with one barrier per variable.
+constexpr int kPer = kTile / kRows;
+
 __global__ void __launch_bounds__(kTile * kRows)
 pack_transpose_kernel(FieldTable t, int nv, int64_t na, int64_t nj, int64_t nq, int64_t g1,
                       int64_t gq, int64_t sa, int64_t sq, int64_t da, int64_t dq,
                       int64_t plane, int64_t tiles_a, int64_t tiles_j,
                       double *__restrict__ out) {
-    __shared__ double tile[kTile][kTile + 1];
+    __shared__ double tile[2][kTile][kTile + 1];
     int64_t blk = blockIdx.x;
     const int64_t ta = blk % tiles_a;
     blk /= tiles_a;
@@ -62,22 +66,44 @@ pack_transpose_kernel(FieldTable t, int nv, int64_t na, int64_t nj, int64_t nq, 
     const int64_t q = blk / tiles_j;
     const int64_t a0 = ta * kTile, j0 = tj * kTile;
     const int tx = threadIdx.x, ty = threadIdx.y;
+    // load side: lanes along j (contiguous in the field), rows along a
+    const int64_t jl = j0 + tx;
+    const int64_t src0 = (jl + g1) + sa * (a0 + ty) + sq * (q + gq);
+    bool lok[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) lok[r] = jl < nj && a0 + ty + r * kRows < na;
+    // store side: lanes along a (contiguous in the output), rows along j
+    const int64_t as = a0 + tx;
+    const int64_t dst0 = as + da * (j0 + ty) + dq * q;
+    bool sok[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) sok[r] = as < na && j0 + ty + r * kRows < nj;
+
+    double v[kPer];
+    {
+        const double *f = t.p[0];
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + sa * (r * kRows)) : 0.0;
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) tile[0][ty + r * kRows][tx] = v[r];
+    }
+    __syncthreads();
     for (int i = 0; i < nv; ++i) {
-        const double *f = t.p[i];
-        // load: lanes along j (contiguous in the field)
-        const int64_t jj = j0 + tx;
+        const int buf = i & 1;
+        const bool more = i + 1 < nv;
+        if (more) {
+            const double *f = t.p[i + 1];
 #pragma unroll
-        for (int r = ty; r < kTile; r += kRows) {
-            const int64_t a = a0 + r;
-            if (jj < nj && a < na) tile[r][tx] = __ldg(f + (jj + g1) + sa * a + sq * (q + gq));
+            for (int r = 0; r < kPer; ++r)
+                v[r] = lok[r] ? __ldg(f + src0 + sa * (r * kRows)) : 0.0;
         }
-        __syncthreads();
-        // store: lanes along a (contiguous in the output)
-        const int64_t a = a0 + tx;
+        double *o = out + (int64_t)i * plane + dst0;
 #pragma unroll
-        for (int r = ty; r < kTile; r += kRows) {
-            const int64_t j = j0 + r;
-            if (a < na && j < nj) out[(int64_t)i * plane + a + da * j + dq * q] = tile[tx][r];
+        for (int r = 0; r < kPer; ++r)
+            if (sok[r]) o[da * (r * kRows)] = tile[buf][tx][ty + r * kRows];
+        if (more) {
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) tile[buf ^ 1][ty + r * kRows][tx] = v[r];
         }
         __syncthreads();
     }

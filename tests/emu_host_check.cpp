@@ -1,0 +1,132 @@
+// Host check of the integer-pipe binary64 addition (fp64_emu.cuh): every sum
+// must be bit-identical to the host CPU's IEEE 754 addition (round to nearest
+// even).  Built with -O2 -ffp-contract=off; prints "mismatches N cases M".
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "../finite_volume_field_gb300/csrc/fp64_emu.cuh"
+
+using namespace fvf::emu;
+
+static uint64_t sm_state = 0x243F6A8885A308D3ull;
+static uint64_t next_u64() {  // SplitMix64 (Steele, Lea, Flood 2014)
+    uint64_t z = (sm_state += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+static double native_add(double a, double b) {
+    volatile double x = a, y = b;
+    volatile double r = x + y;
+    return r;
+}
+
+static uint64_t mismatches = 0, cases = 0;
+
+static void check(uint64_t A, uint64_t B) {
+    const double a = from_bits(A), b = from_bits(B);
+    const uint64_t want = bits(native_add(a, b));
+    const uint64_t got = bits(add(a, b));
+    const bool nan = ((want >> 52) & 0x7FF) == 0x7FF && (want & kFrac);
+    ++cases;
+    if (got != want && !(nan && ((got >> 52) & 0x7FF) == 0x7FF && (got & kFrac))) {
+        if (mismatches < 10)
+            std::printf("add mismatch: %016llx + %016llx -> got %016llx want %016llx\n",
+                        (unsigned long long)A, (unsigned long long)B, (unsigned long long)got,
+                        (unsigned long long)want);
+        ++mismatches;
+    }
+    if (((A ^ B) >> 63) == 0) {
+        const uint64_t got2 = bits(add_same_sign(a, b));
+        if (got2 != want && !nan) {
+            if (mismatches < 10)
+                std::printf("same-sign mismatch: %016llx + %016llx -> got %016llx want %016llx\n",
+                            (unsigned long long)A, (unsigned long long)B,
+                            (unsigned long long)got2, (unsigned long long)want);
+            ++mismatches;
+        }
+    }
+    // the complete integer algorithm on its own (the slow path)
+    const uint64_t full = add_full_int(A, B);
+    if (full != want && !(nan && ((full >> 52) & 0x7FF) == 0x7FF && (full & kFrac))) {
+        if (mismatches < 10)
+            std::printf("full mismatch: %016llx + %016llx -> got %016llx want %016llx\n",
+                        (unsigned long long)A, (unsigned long long)B, (unsigned long long)full,
+                        (unsigned long long)want);
+        ++mismatches;
+    }
+    // the other operand order must give the same bits (NaNs: any NaN)
+    const uint64_t swapped = bits(add(b, a));
+    if (swapped != got && !nan) {
+        if (mismatches < 10)
+            std::printf("order mismatch: %016llx + %016llx -> %016llx vs %016llx\n",
+                        (unsigned long long)A, (unsigned long long)B, (unsigned long long)got,
+                        (unsigned long long)swapped);
+        ++mismatches;
+    }
+}
+
+static uint64_t make(uint64_t sign, uint64_t exp, uint64_t frac) {
+    return (sign << 63) | ((exp & 0x7FF) << 52) | (frac & kFrac);
+}
+
+int main(int argc, char **argv) {
+    const long n = argc > 1 ? std::atol(argv[1]) : 1000000;
+    // 1. uniformly random bit patterns
+    for (long i = 0; i < n; ++i) check(next_u64(), next_u64());
+    // 2. exponents within 70 of each other, random signs and fractions
+    for (long i = 0; i < 4 * n; ++i) {
+        const uint64_t e = 1 + next_u64() % 2046;
+        const int64_t de = (int64_t)(next_u64() % 141) - 70;
+        int64_t e2 = (int64_t)e + de;
+        if (e2 < 0) e2 = 0;
+        if (e2 > 2047) e2 = 2047;
+        check(make(next_u64() & 1, e, next_u64()), make(next_u64() & 1, (uint64_t)e2, next_u64()));
+    }
+    // 3. cancellation: opposite signs, nearly equal magnitudes
+    for (long i = 0; i < n; ++i) {
+        const uint64_t A = make(0, 1 + next_u64() % 2046, next_u64());
+        const int64_t k = (int64_t)(next_u64() % 2049) - 1024;
+        uint64_t B = (A + (uint64_t)k) | kSign;
+        if (((B >> 52) & 0x7FF) == 0x7FF) B = A | kSign;
+        check(A, B);
+        check(A, (A ^ kSign) + (next_u64() % 4));
+    }
+    // 4. ties and near-ties: y is a power of two around half an ulp of x
+    for (long i = 0; i < n; ++i) {
+        const uint64_t ex = 60 + next_u64() % 1900;
+        const uint64_t A = make(next_u64() & 1, ex, next_u64() & ((next_u64() & 1) ? ~0ull : ~7ull));
+        const uint64_t ey = ex - 52 - (next_u64() % 4);
+        const uint64_t B = make(next_u64() & 1, ey, (next_u64() & 1) ? 0 : next_u64() % 3);
+        check(A, B);
+    }
+    // 5. the ends of the exponent range: subnormal results, overflow
+    for (long i = 0; i < n / 4; ++i) {
+        check(make(next_u64() & 1, next_u64() % 4, next_u64()), make(next_u64() & 1, next_u64() % 4, next_u64()));
+        check(make(next_u64() & 1, 2043 + next_u64() % 5, next_u64()),
+              make(next_u64() & 1, 2040 + next_u64() % 8, next_u64()));
+    }
+    // 6. gradual underflow: subnormal sums and differences of small normals
+    for (long i = 0; i < n; ++i) {
+        const uint64_t ea = next_u64() % 60, eb = ea + (next_u64() % 5) - 2;
+        check(make(next_u64() & 1, ea, next_u64()), make(next_u64() & 1, eb & 0x7FF, next_u64()));
+        const uint64_t A = make(0, 1 + next_u64() % 54, next_u64());
+        check(A, (A + (next_u64() % 4096) - 2048) | kSign);
+    }
+    // 7. special values against everything
+    const uint64_t specials[] = {0, kSign, 1, kSign | 1, kHidden, kHidden - 1, 0x7FEFFFFFFFFFFFFFull,
+                                 0xFFEFFFFFFFFFFFFFull, 0x7FF0000000000000ull, 0xFFF0000000000000ull,
+                                 0x7FF8000000000000ull, 0x7FF4000000000001ull, 0x3FF0000000000000ull,
+                                 0xBFF0000000000000ull, 0x3CA0000000000000ull, 0x3CB0000000000000ull};
+    const int ns = sizeof(specials) / sizeof(specials[0]);
+    for (int i = 0; i < ns; ++i)
+        for (int j = 0; j < ns; ++j) check(specials[i], specials[j]);
+    for (long i = 0; i < n / 10; ++i)
+        for (int j = 0; j < ns; ++j) check(specials[j], next_u64());
+    std::printf("mismatches %llu cases %llu\n", (unsigned long long)mismatches,
+                (unsigned long long)cases);
+    return mismatches != 0;
+}
