@@ -324,7 +324,7 @@ def source_hash():
 # CPU oracle baseline (bounded sample of the same workload)
 # ---------------------------------------------------------------------------
 
-def oracle_sample(host, diffusion_steps=40, passes=3):
+def oracle_sample(host, diffusion_steps=160, passes=10):
     """Time the CPU oracle, as it stands, on a bounded sample of the step:
     ``diffusion_steps`` of each precision on the full 8192^2 grid (OpenMP over
     rows, all host threads), then ``passes`` passes of pack x/y/z and flux
@@ -358,8 +358,8 @@ def oracle_sample(host, diffusion_steps=40, passes=3):
     return tot_b, tot_cv, tot_s, threads
 
 
-ORACLE_SAMPLE_DESC = ("40 diffusion steps per precision on 8192^2 (OpenMP over rows, all host "
-                      "threads) + 3 passes of pack x/y/z (8x207^3) and flux x/y/z (8x201^3) and 3 "
+ORACLE_SAMPLE_DESC = ("160 diffusion steps per precision on 8192^2 (OpenMP over rows, all host "
+                      "threads) + 10 passes of pack x/y/z (8x207^3) and flux x/y/z (8x201^3) and 10 "
                       "repetitions of the 4800x1200 sequence (single-threaded loops); "
                       "GB/s = compulsory bytes / wall time")
 
@@ -577,6 +577,49 @@ def run_gpu(args):
     return 0
 
 
+def run_ncu_case():
+    """Each sweep kernel at its benchmark size, one buffer set on the device
+    at a time (at most about 1.1 GB), for Nsight Compute captures:
+    diffusion 8192^2 FP64 then FP32 (2 steps each), pack x/y/z on 8 fields of
+    207^3, flux difference x/y/z on 8 x 201^3.  Device-generated values (the
+    kernels' timing does not depend on them)."""
+    import torch
+    from finite_volume_field_gb300 import api, buildlib
+    if not api.LIB_PATH.exists():
+        buildlib.build()
+    api.load()
+
+    def free():
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    for dt, code in ((torch.float64, api.FVF_FP64), (torch.float32, api.FVF_FP32)):
+        u = torch.rand(DIFF_N * DIFF_N, dtype=dt, device="cuda")
+        v = torch.zeros_like(u)
+        api.diffuse2d_step(u, v, DIFF_N, DIFF_N, 0.1, 2, code)
+        del u, v
+        free()
+    N = _prod(inputs.stored_extents(PACK_EXT, PACK_G))
+    fields = [torch.randn(N, dtype=torch.float64, device="cuda") for _ in range(PACK_NV)]
+    out = torch.empty(_prod(pack_extents(PACK_EXT, PACK_G, 0)) * PACK_NV, dtype=torch.float64,
+                      device="cuda")
+    for d in range(3):
+        api.weno_pack(fields, PACK_NV, PACK_EXT, PACK_G, d, out)
+    del fields, out
+    free()
+    for d in range(3):
+        fe = list(RHS_EXT)
+        fe[d] += 1
+        F = torch.randn(_prod(fe) * RHS_NV, dtype=torch.float64, device="cuda")
+        w = torch.rand(RHS_EXT[d], dtype=torch.float64, device="cuda") + 0.5
+        r = torch.empty(_prod(RHS_EXT) * RHS_NV, dtype=torch.float64, device="cuda")
+        api.advect_rhs(F, w, RHS_NV, RHS_EXT, d, r)
+        del F, w, r
+        free()
+    print("ncu case done", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -585,7 +628,11 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (it is only taken at N=1 anyway)")
+    ap.add_argument("--ncu-case", action="store_true",
+                    help="launch each sweep kernel once at benchmark size (for ncu), no timing")
     args = ap.parse_args(argv)
+    if args.ncu_case:
+        return run_ncu_case()
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
