@@ -7,12 +7,12 @@
 // and dst = 0 on the four edges, with the field column-major (i contiguous,
 // section 4).  Every operation is rounded to nearest even on its own, in the
 // order written: the round-to-nearest intrinsics below are never contracted
-// into fused multiply-adds.  The single fused operation used, fma(-4, c, s),
-// rounds the exact value s - 4c once, which is what s - fl(4c) gives whenever
-// 4c is representable (4c is a power-of-two scaling, exact unless it
-// overflows); cells with |c| >= 2^126 (FP32) or 2^1022 (FP64) take the
-// two-operation form instead, so the result is bit-identical for every
-// input.
+// into fused multiply-adds.  In FP64 the single fused operation used,
+// fma(-4, c, s), rounds the exact value s - 4c once, which is what s - fl(4c)
+// gives whenever 4c is representable (4c is a power-of-two scaling, exact
+// unless it overflows); cells with |c| >= 2^1022 take the two-operation form
+// instead, so the result is bit-identical for every input.  (The fused form
+// saves one FP64 operation; FP32 uses the two operations as written.)
 //
 // Kernels
 //   march  (rows 16-byte aligned, nx a multiple of the vector width): one
@@ -53,9 +53,6 @@ struct Rn;
 static __device__ __noinline__ double sub4_two_ops(double s, double c) {
     return __dsub_rn(s, __dmul_rn(4.0, c));
 }
-static __device__ __noinline__ float sub4_two_ops(float s, float c) {
-    return __fsub_rn(s, __fmul_rn(4.0f, c));
-}
 
 template <>
 struct Rn<double> {
@@ -73,10 +70,10 @@ template <>
 struct Rn<float> {
     static __device__ __forceinline__ float add(float a, float b) { return __fadd_rn(a, b); }
     static __device__ __forceinline__ float mul(float a, float b) { return __fmul_rn(a, b); }
+    // FP32 arithmetic is cheap: the two rounded operations as written, no
+    // fused form and no range check.
     static __device__ __forceinline__ float sub4(float s, float c) {
-        if ((__float_as_uint(c) & 0x7f800000u) >= 0x7e800000u)  // |c| >= 2^126, NaN, Inf
-            return sub4_two_ops(s, c);
-        return __fmaf_rn(-4.0f, c, s);
+        return __fsub_rn(s, __fmul_rn(4.0f, c));
     }
 };
 
@@ -257,40 +254,272 @@ int march_blocks_per_sm() {
     return cached;
 }
 
+// ---------------------------------------------------------------------------
+// Temporally blocked kernel: up to kTbSteps steps per launch in shared memory
+// ---------------------------------------------------------------------------
+//
+// A block owns a kTbX x kTbY tile of the output and stages the tile plus a
+// halo of kTbSteps cells on every side (a kTbW x kTbH region) in shared
+// memory.  Step s (1-based) is valid on the rows and columns at distance >= s
+// from the region's border; after `steps` steps the tile is valid and is
+// written out.  Every cell receives exactly the update() of the global
+// stepping, same operands, same order, so the result is bit-identical; the
+// halo is recomputed by the neighbouring tiles.
+//
+// Work mapping: warp w owns the band of kTbRows rows starting at w*kTbRows
+// across the whole region width, each lane four consecutive columns.  A lane
+// walks down its band with the rows above and at the current cell in
+// registers: per row it loads the row below as one 16-byte shared access (two
+// for FP64), takes the W/E neighbours inside its four columns from registers
+// and the two outside ones from the adjacent lanes by shuffle, and stores the
+// four results with one access.  Rows outside the valid range of a step are
+// skipped (the bound is uniform in the warp); all columns are computed: a
+// column outside the valid range computes values that are never read by a
+// valid cell (influence travels one cell per step).  Global edge cells are
+// set to zero at every step; cells outside the grid are never read by an
+// interior cell.
+constexpr int kTbSteps = 8;
+constexpr int kTbX = 112, kTbY = 64;
+constexpr int kTbW = kTbX + 2 * kTbSteps;   // 128 = 4 columns per lane
+constexpr int kTbH = kTbY + 2 * kTbSteps;   // 80
+constexpr int kTbThreads = 256;             // 8 warps
+constexpr int kTbRows = kTbH / 8;           // rows per warp band
+constexpr int kTbCx = kTbW / 32;
+static_assert(kTbW == 128 && kTbH % 8 == 0, "tile shape: one warp spans a row, 4 columns per lane");
+
+// Four consecutive elements of a shared-memory row (16-byte aligned).
 template <typename T>
-cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
-                cudaStream_t stream, uint64_t *launches) {
-    constexpr int V = Vec16<T>::n;
-    const bool vec_ok = (nx % V == 0) && ((uintptr_t)u % 16 == 0) && ((uintptr_t)v % 16 == 0) &&
-                        nx >= 2 * V;
+struct Quad {
+    T v[4];
+};
+
+template <typename T>
+__device__ __forceinline__ Quad<T> ld_quad(const T *p) {
+    Quad<T> q;
+    if constexpr (sizeof(T) == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(p);
+        q.v[0] = x.x; q.v[1] = x.y; q.v[2] = x.z; q.v[3] = x.w;
+    } else {
+        const double2 x = reinterpret_cast<const double2 *>(p)[0];
+        const double2 y = reinterpret_cast<const double2 *>(p)[1];
+        q.v[0] = x.x; q.v[1] = x.y; q.v[2] = y.x; q.v[3] = y.y;
+    }
+    return q;
+}
+
+template <typename T>
+__device__ __forceinline__ void st_quad(T *p, const Quad<T> &q) {
+    if constexpr (sizeof(T) == 4) {
+        *reinterpret_cast<float4 *>(p) = make_float4(q.v[0], q.v[1], q.v[2], q.v[3]);
+    } else {
+        reinterpret_cast<double2 *>(p)[0] = make_double2(q.v[0], q.v[1]);
+        reinterpret_cast<double2 *>(p)[1] = make_double2(q.v[2], q.v[3]);
+    }
+}
+
+// Two blocks per SM is what the shared memory allows in FP32 (80 KB each).
+template <typename T>
+__global__ void __launch_bounds__(kTbThreads, 2)
+diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
+                      int steps, T alpha) {
+    extern __shared__ unsigned char smem_raw[];
+    T *buf0 = reinterpret_cast<T *>(smem_raw);
+    T *buf1 = buf0 + kTbW * kTbH;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t gi0 = (int64_t)blockIdx.x * kTbX - kTbSteps;
+    const int64_t gj0 = (int64_t)blockIdx.y * kTbY - kTbSteps;
+
+    // stage the region (rows strided over the warps: coalesced 32-wide rows)
+#pragma unroll
+    for (int b = 0; b < kTbH / 8; ++b) {
+        const int lj = warp + 8 * b;
+        const int64_t gj = gj0 + lj;
+#pragma unroll
+        for (int a = 0; a < kTbCx; ++a) {
+            const int li = lane + 32 * a;
+            const int64_t gi = gi0 + li;
+            T val = T(0);
+            if (gi >= 0 && gi < nx && gj >= 0 && gj < ny) val = __ldg(src + gi + nx * gj);
+            buf0[lj * kTbW + li] = val;
+        }
+    }
+    // The second buffer starts as zeros: the columns computed outside the
+    // valid range then stay finite (left-over shared memory could hold bit
+    // patterns that send every such cell down the rare-value path).
+    for (int idx = threadIdx.x; idx < kTbW * kTbH / 4; idx += kTbThreads) {
+        Quad<T> z;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) z.v[k] = T(0);
+        st_quad<T>(buf1 + 4 * idx, z);
+    }
+    const int li0 = 4 * lane;                    // this lane's four columns
+    bool col_edge[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int64_t gi = gi0 + li0 + k;
+        col_edge[k] = gi == 0 || gi == nx - 1;
+    }
+    __syncthreads();
+
+    const int band0 = warp * kTbRows;
+    for (int s = 1; s <= steps; ++s) {
+        const T *in = (s & 1) ? buf0 : buf1;
+        T *out = (s & 1) ? buf1 : buf0;
+        const int r0 = max(band0, s), r1 = min(band0 + kTbRows, kTbH - s);
+        if (r0 < r1) {          // uniform in the warp
+            Quad<T> up = ld_quad<T>(in + (r0 - 1) * kTbW + li0);
+            Quad<T> cur = ld_quad<T>(in + r0 * kTbW + li0);
+            const int gjb = (int)gj0;            // row r is global row gjb + r
+            // one row: results into out, returns the row below
+            auto row = [&](int r, const Quad<T> &above, const Quad<T> &mid) -> Quad<T> {
+                const Quad<T> below = ld_quad<T>(in + (r + 1) * kTbW + li0);
+                const T w_in = __shfl_up_sync(0xffffffffu, mid.v[3], 1);
+                const T e_in = __shfl_down_sync(0xffffffffu, mid.v[0], 1);
+                const int gj = gjb + r;
+                const bool row_edge = gj == 0 || gj == (int)ny - 1;
+                Quad<T> res;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const T w = k > 0 ? mid.v[k - 1] : w_in;
+                    const T e = k < 3 ? mid.v[k + 1] : e_in;
+                    const T val = update<T>(mid.v[k], w, e, above.v[k], below.v[k], alpha);
+                    res.v[k] = (row_edge || col_edge[k]) ? T(0) : val;
+                }
+                st_quad<T>(out + r * kTbW + li0, res);
+                return below;
+            };
+            int r = r0;
+            for (; r + 1 < r1; r += 2) {          // two rows per trip: no copies
+                const Quad<T> b1 = row(r, up, cur);
+                const Quad<T> b2 = row(r + 1, cur, b1);
+                up = b1;
+                cur = b2;
+            }
+            if (r < r1) row(r, up, cur);
+        }
+        __syncthreads();
+    }
+
+    const T *fin = (steps & 1) ? buf1 : buf0;
+#pragma unroll
+    for (int b = 0; b < kTbH / 8; ++b) {
+        const int lj = warp + 8 * b;
+        const int64_t gj = gj0 + lj;
+        if (lj < kTbSteps || lj >= kTbSteps + kTbY || gj < 0 || gj >= ny) continue;
+#pragma unroll
+        for (int a = 0; a < kTbCx; ++a) {
+            const int li = lane + 32 * a;
+            const int64_t gi = gi0 + li;
+            if (li >= kTbSteps && li < kTbSteps + kTbX && gi >= 0 && gi < nx)
+                dst[gi + nx * gj] = fin[lj * kTbW + li];
+        }
+    }
+}
+
+constexpr size_t tblock_smem_bytes(size_t elem) { return 2 * (size_t)kTbW * kTbH * elem; }
+
+// Whether to run blocks of steps in shared memory: FP32 is HBM-bound, so
+// blocking cuts its traffic about sixfold; FP64 is arithmetic-bound on large
+// grids (the halo's recomputation would only cost), so it is blocked only on
+// grids small enough that launches, not arithmetic, dominate.
+template <typename T>
+bool use_tblock(int64_t nx, int64_t ny, int64_t nsteps) {
+    if (nsteps < 3) return false;
+    const int64_t tiles_y = (ny + kTbY - 1) / kTbY;
+    if (tiles_y > 65535 || (nx + kTbX - 1) / kTbX > 0x7fffffff) return false;
+    if (sizeof(T) == 4) return true;
+    return nx * ny <= (int64_t)1024 * 1024;
+}
+
+template <typename T>
+cudaError_t tblock_prepare() {
+    static cudaError_t status = cudaErrorNotReady;
+    if (status == cudaErrorNotReady) {
+        status = cudaFuncSetAttribute(diffuse_tblock_kernel<T>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)tblock_smem_bytes(sizeof(T)));
+        if (status != cudaSuccess) cudaGetLastError();
+    }
+    return status;
+}
+
+// One-step launches (march or scalar kernel), configured once per call.
+template <typename T>
+struct SingleStep {
+    bool vec_ok = false;
     dim3 grid, block;
     int64_t rows = 0;
-    if (vec_ok) {
-        const int64_t bx = (nx / V + kMarchThreads - 1) / kMarchThreads;
-        const int64_t resident = (int64_t)march_blocks_per_sm<T>() * sm_count();
-        int64_t by = resident / bx;
-        if (by < 1) by = 1;
-        if (by > ny) by = ny;
-        rows = (ny + by - 1) / by;
-        by = (ny + rows - 1) / rows;
-        if (bx > 0x7fffffff || by > 65535) return cudaErrorInvalidValue;
-        grid = dim3((unsigned)bx, (unsigned)by);
-        block = dim3(kMarchThreads);
-    } else {
-        const int64_t gy = (ny + kBy - 1) / kBy;
-        grid = dim3((unsigned)((nx + kBx - 1) / kBx), (unsigned)(gy < 65535 ? gy : 65535));
-        block = dim3(kBx, kBy);
+
+    cudaError_t setup(const T *u, const T *v, int64_t nx, int64_t ny) {
+        constexpr int V = Vec16<T>::n;
+        vec_ok = (nx % V == 0) && ((uintptr_t)u % 16 == 0) && ((uintptr_t)v % 16 == 0) &&
+                 nx >= 2 * V;
+        if (vec_ok) {
+            const int64_t bx = (nx / V + kMarchThreads - 1) / kMarchThreads;
+            const int64_t resident = (int64_t)march_blocks_per_sm<T>() * sm_count();
+            int64_t by = resident / bx;
+            if (by < 1) by = 1;
+            if (by > ny) by = ny;
+            rows = (ny + by - 1) / by;
+            by = (ny + rows - 1) / rows;
+            if (bx > 0x7fffffff || by > 65535) return cudaErrorInvalidValue;
+            grid = dim3((unsigned)bx, (unsigned)by);
+            block = dim3(kMarchThreads);
+        } else {
+            const int64_t gy = (ny + kBy - 1) / kBy;
+            grid = dim3((unsigned)((nx + kBx - 1) / kBx), (unsigned)(gy < 65535 ? gy : 65535));
+            block = dim3(kBx, kBy);
+        }
+        return cudaSuccess;
     }
-    for (int64_t s = 1; s <= nsteps; ++s) {
-        const T *src = (s & 1) ? u : v;
-        T *dst = (s & 1) ? v : u;
+
+    void launch(const T *src, T *dst, int64_t nx, int64_t ny, T alpha, cudaStream_t stream) {
         if (vec_ok)
             diffuse_march_kernel<T><<<grid, block, 0, stream>>>(src, dst, nx, ny, rows, alpha);
         else
             diffuse_step_kernel<T><<<grid, block, 0, stream>>>(src, dst, nx, ny, alpha);
+    }
+};
+
+template <typename T>
+cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
+                cudaStream_t stream, uint64_t *launches) {
+    SingleStep<T> one;
+    cudaError_t e = one.setup(u, v, nx, ny);
+    if (e != cudaSuccess) return e;
+    if (use_tblock<T>(nx, ny, nsteps) && tblock_prepare<T>() == cudaSuccess) {
+        // Steps 1..n-1 in B blocked launches, step n as one single-step
+        // launch, so the other buffer ends holding step n-1.  Launch k reads
+        // u (k even) or v (k odd); step n-1 must end in u when n is odd (the
+        // last step writes v) and in v when n is even, i.e. B must have the
+        // parity of n+1.  B = n-1 (one step per launch) always has it, so
+        // raising B by one when needed keeps B <= n-1.
+        const int64_t n1 = nsteps - 1;
+        int64_t nb = (n1 + kTbSteps - 1) / kTbSteps;
+        if ((nb & 1) != ((nsteps + 1) & 1)) ++nb;
+        const dim3 grid((unsigned)((nx + kTbX - 1) / kTbX), (unsigned)((ny + kTbY - 1) / kTbY));
+        const size_t smem = tblock_smem_bytes(sizeof(T));
+        for (int64_t k = 0; k < nb; ++k) {
+            const int steps = (int)(n1 / nb + (k < n1 % nb ? 1 : 0));
+            const T *src = (k & 1) ? v : u;
+            T *dst = (k & 1) ? u : v;
+            diffuse_tblock_kernel<T><<<grid, kTbThreads, smem, stream>>>(src, dst, nx, ny, steps,
+                                                                          alpha);
+            ++*launches;
+            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        }
+        const T *src = (nsteps & 1) ? u : v;
+        T *dst = (nsteps & 1) ? v : u;
+        one.launch(src, dst, nx, ny, alpha, stream);
         ++*launches;
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        const T *src = (s & 1) ? u : v;
+        T *dst = (s & 1) ? v : u;
+        one.launch(src, dst, nx, ny, alpha, stream);
+        ++*launches;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

@@ -175,3 +175,21 @@ def test_full_size_8192_200_steps(dt):
     want = oracle.diffuse2d(u0, 200, nthreads=oracle.max_threads())
     assert_bits_equal(got, want, what=f"8192^2 {dt.__name__}")
     assert oracle.physical_check(got)["min"] >= 0
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+@pytest.mark.parametrize("nx,ny", [(300, 250), (113, 65), (224, 128), (1000, 7), (9, 600)])
+@pytest.mark.parametrize("steps", [3, 4, 9, 16, 17, 24])
+def test_blocked_steps_multi_tile(dt, nx, ny, steps):
+    """Step counts that take the shared-memory blocked path (up to 8 steps
+    per launch, the last step on its own): several tiles, ragged tile edges,
+    random values everywhere including the edges; both buffers bit-exact
+    (the other buffer must hold step n-1)."""
+    torch = torch_cuda()
+    n = nx * ny
+    u0 = (inputs.uniform_f32(11, nx + ny, n) if dt == np.float32
+          else inputs.uniform_f64(11, nx + ny, n)).reshape(ny, nx)
+    gu, gv = _run_gpu(torch, u0, steps)
+    ou, ov, _ = oracle.diffuse2d(u0, steps, return_both=True)
+    assert_bits_equal(gu, ou, what=f"u {nx}x{ny} {steps}")
+    assert_bits_equal(gv, ov, what=f"v {nx}x{ny} {steps}")
