@@ -229,14 +229,17 @@ class Sweeps:
             ("seq2d", pick(keys_in, "seq_"), pick(keys_out, "seq_"), seq),
         ]
 
-    def step(self, ev=None):
+    def step(self, ev=None, hook=None):
         """Enqueue one step on self.stream; ev maps row name -> (start, end)
-        CUDA events recorded around that row."""
+        CUDA events recorded around that row; hook(name, 0/1) is called at
+        the same points."""
         s = self.stream
 
         def mark(name, which):
             if ev is not None:
                 ev[name][which].record(s)
+            if hook is not None:
+                hook(name, which)
 
         for _, _, _, enqueue in self.stages():
             enqueue(s, mark)
@@ -514,10 +517,25 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize(device)
 
+    # Warm-up; the first step also counts the kernel launches of each row
+    # (the library's own launch counter; blocked diffusion runs up to 8 steps
+    # per launch).
+    row_launches = {}
+
+    def count(name, which):
+        if which == 0:
+            row_launches[name] = -api.launch_count()
+        else:
+            row_launches[name] += api.launch_count()
+
     with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            sw.step()
+        for w in range(max(1, args.warmup)):
+            sw.step(None, count if w == 0 else None)
     barrier()
+    for name, n in row_launches.items():
+        R[name]["per_launch_bytes"] = R[name]["bytes"] / n
+        R[name]["per_launch_cells"] = R[name]["cellvars"] / n
+        R[name]["launches"] = n
 
     # One set of row events per timed step, read after the loop (no host
     # synchronisation inside the timed region).
@@ -647,8 +665,8 @@ def run_ncu_case():
     """Each sweep kernel at its benchmark size, one buffer set on the device
     at a time (at most about 1.1 GB), for Nsight Compute captures:
     diffusion 8192^2 FP64 then FP32, pack x/y/z on 8 fields of
-    207^3, flux difference x/y/z on 8 x 201^3.  FP64 runs 2 single steps, FP32 9 steps (one
-    8-step shared-memory launch, then one single step).  Device-generated values (the
+    207^3, flux difference x/y/z on 8 x 201^3.  FP64 runs 2 single steps, FP32 17 steps (two
+    8-step shared-memory launches, then one single step).  Device-generated values (the
     kernels' timing does not depend on them)."""
     import torch
     from finite_volume_field_gb300 import api, buildlib
@@ -660,7 +678,7 @@ def run_ncu_case():
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
-    for dt, code, steps in ((torch.float64, api.FVF_FP64, 2), (torch.float32, api.FVF_FP32, 9)):
+    for dt, code, steps in ((torch.float64, api.FVF_FP64, 2), (torch.float32, api.FVF_FP32, 17)):
         u = torch.rand(DIFF_N * DIFF_N, dtype=dt, device="cuda")
         v = torch.zeros_like(u)
         api.diffuse2d_step(u, v, DIFF_N, DIFF_N, 0.1, steps, code)
