@@ -69,6 +69,10 @@ def _load():
     lib.oracle_weno_pack.restype = cint
     lib.oracle_advect_rhs.argtypes = [vp, vp, cint, i64, i64, i64, cint, vp]
     lib.oracle_advect_rhs.restype = cint
+    lib.oracle_advect_rhs_add.argtypes = [vp, vp, cint, i64, i64, i64, cint, vp]
+    lib.oracle_advect_rhs_add.restype = cint
+    lib.oracle_flux_unpack.argtypes = [vp, cint, i64, i64, i64, cint, vp]
+    lib.oracle_flux_unpack.restype = cint
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = cint
     _lib = lib
@@ -191,6 +195,46 @@ def advect_rhs(flux: np.ndarray, inv_d: np.ndarray, nv: int, extents, direction:
     if rc != 0:
         raise ValueError("bad direction")
     return rhs
+
+
+def advect_rhs_add(flux: np.ndarray, inv_d: np.ndarray, nv: int, extents, direction: int,
+                   rhs: np.ndarray) -> np.ndarray:
+    """rhs + the flux-difference term of ``direction`` (returns a new array):
+    the accumulating form that builds the finite-volume right-hand side over
+    the directions."""
+    n1, n2, n3 = (int(x) for x in extents)
+    fl = np.ascontiguousarray(flux, dtype=np.float64).reshape(-1)
+    w = np.ascontiguousarray(inv_d, dtype=np.float64).reshape(-1)
+    out = np.array(rhs, dtype=np.float64, copy=True).reshape(-1)
+    if fl.size != int(np.prod(flux_extents(extents, direction))) * nv or out.size != n1 * n2 * n3 * nv:
+        raise ValueError("size mismatch")
+    rc = _load().oracle_advect_rhs_add(_ptr(fl), _ptr(w), int(nv), n1, n2, n3, int(direction),
+                                       _ptr(out))
+    if rc != 0:
+        raise ValueError("bad direction")
+    return out
+
+
+def sweep_flux_extents(extents, direction):
+    """Extents of a sweep-frame face array (swept axis first, n+1 faces)."""
+    n1, n2, n3 = (int(x) for x in extents)
+    return [(n1 + 1, n2, n3), (n2 + 1, n1, n3), (n3 + 1, n2, n1)][direction]
+
+
+def flux_unpack(sweep_flux: np.ndarray, nv: int, extents, direction: int) -> np.ndarray:
+    """Directional flux copy from the sweep frame to the physical frame
+    (MFC pull request #2087, "Changes", s_finalize_riemann_solver); layout
+    as in ``fvf_oracle.c``."""
+    n1, n2, n3 = (int(x) for x in extents)
+    src = np.ascontiguousarray(sweep_flux, dtype=np.float64).reshape(-1)
+    size = int(np.prod(flux_extents(extents, direction))) * nv
+    if src.size != size:
+        raise ValueError("size mismatch")
+    out = np.empty(size, dtype=np.float64)
+    rc = _load().oracle_flux_unpack(_ptr(src), int(nv), n1, n2, n3, int(direction), _ptr(out))
+    if rc != 0:
+        raise ValueError("bad direction")
+    return out
 
 
 def multivar_sweep_2d(fields, fluxes_x, fluxes_y, inv_dx, inv_dy, nv, extents, ghost):

@@ -20,7 +20,7 @@
  *       per-variable GPU kernels": "Changes" (the WENO input pack
  *       v_rs_weno(j,k,l,i) = v_vf(i)%sf(j,k,l) and the x/y/z flux
  *       differences in s_compute_advection_source_term, inverse spacing taken
- *       once per cell).
+ *       once per cell; s_finalize_riemann_solver, the directional flux copies).
  *
  * Conventions (0-based C indices; the pages use 1-based Fortran):
  *  - 2D field u(i,j), 0 <= i < nx, 0 <= j < ny, stored at u[i + nx*j].
@@ -231,6 +231,84 @@ int oracle_advect_rhs(const double *flux, const double *inv_d, int nv, int64_t n
                     const double lo = flux[jl + F1 * (kl + F2 * (ll + F3 * (int64_t)i))];
                     const double hi = flux[jh + F1 * (kh + F2 * (lh + F3 * (int64_t)i))];
                     rhs[j + n1 * (k + n2 * (l + n3 * (int64_t)i))] = w * (lo - hi);
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Accumulating form of the flux difference: rhs(j,k,l,i) = rhs(j,k,l,i) +
+ * inv_d(c) * (F(c-1) - F(c)), so that successive directions build the
+ * finite-volume right-hand side (the x/y/z flux differences of
+ * s_compute_advection_source_term in [M] "Changes" are terms of one sum).
+ * The term is formed exactly as in oracle_advect_rhs, then added once.
+ */
+int oracle_advect_rhs_add(const double *flux, const double *inv_d, int nv, int64_t n1,
+                          int64_t n2, int64_t n3, int dir, double *rhs)
+{
+    int64_t F1 = n1, F2 = n2, F3 = n3;
+    if (dir == 0)
+        F1 = n1 + 1;
+    else if (dir == 1)
+        F2 = n2 + 1;
+    else if (dir == 2)
+        F3 = n3 + 1;
+    else
+        return -1;
+    for (int i = 0; i < nv; ++i) {
+        for (int64_t l = 0; l < n3; ++l) {
+            for (int64_t k = 0; k < n2; ++k) {
+                for (int64_t j = 0; j < n1; ++j) {
+                    const int64_t c = dir == 0 ? j : (dir == 1 ? k : l);
+                    const int64_t sj = dir == 0 ? 1 : 0, sk = dir == 1 ? 1 : 0, sl = dir == 2 ? 1 : 0;
+                    const double lo = flux[j + F1 * (k + F2 * (l + F3 * (int64_t)i))];
+                    const double hi = flux[(j + sj) + F1 * ((k + sk) + F2 * ((l + sl) + F3 * (int64_t)i))];
+                    const double term = inv_d[c] * (lo - hi);
+                    double *r = &rhs[j + n1 * (k + n2 * (l + n3 * (int64_t)i))];
+                    *r = *r + term;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * Directional flux copy back to the physical frame (s_finalize_riemann_solver
+ * in [M] "Changes"): the inverse of the pack's permutation for face arrays.
+ * A sweep-frame face array has the swept axis first, with its n+1 faces:
+ *   dir 0: in(f, k, l, i), extents (n1+1, n2, n3)  ->  out(f, k, l, i)   (same layout)
+ *   dir 1: in(f, j, l, i), extents (n2+1, n1, n3)  ->  out(j, f, l, i), extents (n1, n2+1, n3)
+ *   dir 2: in(f, k, j, i), extents (n3+1, n2, n1)  ->  out(j, k, f, i), extents (n1, n2, n3+1)
+ * Arrays are contiguous with the first index fastest and the variable slowest.
+ * A plain element copy.  Returns 0, or -1 for an unknown direction.
+ */
+int oracle_flux_unpack(const double *in, int nv, int64_t n1, int64_t n2, int64_t n3, int dir,
+                       double *out)
+{
+    int64_t F1 = n1, F2 = n2, F3 = n3;   /* physical face-array extents */
+    if (dir == 0)
+        F1 = n1 + 1;
+    else if (dir == 1)
+        F2 = n2 + 1;
+    else if (dir == 2)
+        F3 = n3 + 1;
+    else
+        return -1;
+    for (int i = 0; i < nv; ++i) {
+        for (int64_t l = 0; l < F3; ++l) {
+            for (int64_t k = 0; k < F2; ++k) {
+                for (int64_t j = 0; j < F1; ++j) {
+                    int64_t src;
+                    if (dir == 0)
+                        src = j + F1 * (k + F2 * (l + F3 * (int64_t)i));
+                    else if (dir == 1)   /* in(f=k, j, l): extents (F2, F1, F3) */
+                        src = k + F2 * (j + F1 * (l + F3 * (int64_t)i));
+                    else                 /* in(f=l, k, j): extents (F3, F2, F1) */
+                        src = l + F3 * (k + F2 * (j + F1 * (int64_t)i));
+                    out[j + F1 * (k + F2 * (l + F3 * (int64_t)i))] = in[src];
                 }
             }
         }

@@ -39,7 +39,8 @@ def _mutant(tmp_path, old: str, new: str, count: int = 1):
     real = oracle._load()
     lib = ctypes.CDLL(str(so))
     for name in ("oracle_diffuse2d_f64", "oracle_diffuse2d_f32", "oracle_weno_pack",
-                 "oracle_advect_rhs", "oracle_max_threads"):
+                 "oracle_advect_rhs", "oracle_advect_rhs_add", "oracle_flux_unpack",
+                 "oracle_max_threads"):
         getattr(lib, name).argtypes = getattr(real, name).argtypes
         getattr(lib, name).restype = getattr(real, name).restype
     oracle._lib = lib
@@ -90,6 +91,13 @@ MUTANTS = [
     ("flux-z-spacing-index",
      "ll = l; lh = l + 1; w = inv_d[l];", "ll = l; lh = l + 1; w = inv_d[0];",
      1, lambda: P.test_rhs_linear_flux_gives_minus_inv_d(2)),
+    ("rhs-add-faces-swapped",
+     "const double term = inv_d[c] * (lo - hi);", "const double term = inv_d[c] * (hi - lo);",
+     1, lambda: P.test_rhs_add_builds_two_direction_sum()),
+    ("unpack-y-as-x",
+     "src = k + F2 * (j + F1 * (l + F3 * (int64_t)i));",
+     "src = j + F1 * (k + F2 * (l + F3 * (int64_t)i));",
+     1, lambda: P.test_flux_unpack_coordinate_tags(1)),
 ]
 
 

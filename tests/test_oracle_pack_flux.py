@@ -218,3 +218,111 @@ def test_multivar_sequence_shapes():
     assert rx.size == ry.size == 12 * 8 * 7
     assert np.all(fields[5] >= 0) and np.all(fields[5] < 1)
     assert np.all(fields[0] > 0)
+
+
+# ---------------------------------------------------------------------------
+# Accumulating flux difference and the directional flux copy (unpack)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("extents", [(3, 4, 5), (5, 4, 1), (7, 1, 3)])
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_rhs_add_matches_numpy_formulation(extents, direction):
+    """rhs_new = rhs_old + inv_d*(F(c-1) - F(c)), each operation rounded once
+    (numpy float64, no contraction)."""
+    nv = 3
+    seed = inputs.config_seed(0)
+    flux = inputs.face_fluxes(seed, nv, extents, direction)
+    inv_d = inputs.inverse_spacing(seed, extents[direction], stream=210 + direction)
+    old = inputs.normal_f64(seed, 300 + direction, int(np.prod(extents)) * nv)
+    got = oracle.advect_rhs_add(flux, inv_d, nv, extents, direction, old)
+    want = old + _numpy_rhs(flux, inv_d, nv, extents, direction)
+    assert np.array_equal(got.view(np.uint64), want.view(np.uint64))
+
+
+def test_rhs_add_into_zero_is_assignment():
+    """Accumulating into +0 gives the assigned term, except that a -0 term
+    becomes +0 (+0 + -0 = +0 under round to nearest)."""
+    extents, nv = (6, 5, 4), 2
+    for direction in range(3):
+        flux = inputs.face_fluxes(3, nv, extents, direction)
+        flux[::9] = 1.5                     # some equal faces: zero differences
+        inv_d = inputs.inverse_spacing(3, extents[direction])
+        zero = np.zeros(int(np.prod(extents)) * nv)
+        acc = oracle.advect_rhs_add(flux, inv_d, nv, extents, direction, zero)
+        asg = oracle.advect_rhs(flux, inv_d, nv, extents, direction)
+        assert np.array_equal(acc, asg)
+        assert np.array_equal(acc.view(np.uint64), np.where(asg == 0, 0.0, asg).view(np.uint64))
+
+
+def test_rhs_add_builds_two_direction_sum():
+    """Linear fluxes along x and along y, accumulated into zero: each cell
+    holds (-inv_dx) + (-inv_dy), rounded once."""
+    extents, nv = (4, 5, 1), 2
+    wx = inputs.inverse_spacing(8, 4)
+    wy = inputs.inverse_spacing(9, 5, stream=201)
+    rhs = np.zeros(4 * 5 * nv)
+    for direction, w in ((0, wx), (1, wy)):
+        F1, F2, F3 = oracle.flux_extents(extents, direction)
+        l, k, j = np.meshgrid(np.arange(F3), np.arange(F2), np.arange(F1), indexing="ij")
+        F = np.tile(((j, k, l)[direction] - 1.0).reshape(-1), nv)
+        rhs = oracle.advect_rhs_add(F, w, nv, extents, direction, rhs)
+    R = rhs.reshape(nv, 1, 5, 4)
+    want = (-wx)[None, None, None, :] + (-wy)[None, None, :, None]
+    assert np.array_equal(R, np.broadcast_to(want, R.shape))
+
+
+def _numpy_unpack(src, nv, extents, direction):
+    """Sweep frame -> physical frame with numpy transposes of [i, c, b, a]
+    arrays (a = swept axis)."""
+    S = oracle.sweep_flux_extents(extents, direction)
+    A = np.asarray(src).reshape(nv, S[2], S[1], S[0])      # [i, c, b, a]
+    if direction == 0:
+        P = A                                               # out[i, l, k, f] = in[i, l, k, f]
+    elif direction == 1:
+        P = A.transpose(0, 1, 3, 2)                         # out[i, l, f, j] = in[i, l, j, f]
+    else:
+        P = A.transpose(0, 3, 2, 1)                         # out[i, f, k, j] = in[i, j, k, f]
+    return np.ascontiguousarray(P).reshape(-1)
+
+
+@pytest.mark.parametrize("extents", [(3, 4, 5), (5, 4, 1), (1, 6, 2), (7, 1, 3)])
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_flux_unpack_matches_numpy_formulation(extents, direction):
+    nv = 3
+    src = inputs.normal_f64(4, direction, int(np.prod(oracle.sweep_flux_extents(extents, direction))) * nv)
+    got = oracle.flux_unpack(src, nv, extents, direction)
+    assert np.array_equal(got.view(np.uint64), _numpy_unpack(src, nv, extents, direction).view(np.uint64))
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_flux_unpack_coordinate_tags(direction):
+    """Each sweep-frame element carries (i, a, b, c); the physical element
+    (j, k, l, i) must hold the tag of the face it is: a = the swept-axis face
+    index, b and c the transverse cells in the sweep frame's order."""
+    extents, nv = (4, 5, 6), 2
+    S = oracle.sweep_flux_extents(extents, direction)
+    c, b, a = np.meshgrid(np.arange(S[2]), np.arange(S[1]), np.arange(S[0]), indexing="ij")
+    src = np.concatenate([(i * 1e9 + a * 1e6 + b * 1e3 + c).astype(np.float64).reshape(-1)
+                          for i in range(nv)])
+    out = oracle.flux_unpack(src, nv, extents, direction)
+    F1, F2, F3 = oracle.flux_extents(extents, direction)
+    for i, l, k, j in itertools.product(range(nv), range(F3), range(F2), range(F1)):
+        val = int(out[j + F1 * (k + F2 * (l + F3 * i))])
+        ti, r = divmod(val, 10**9)
+        ta, r = divmod(r, 10**6)
+        tb, tc = divmod(r, 10**3)
+        want = [(j, k, l), (k, j, l), (l, k, j)][direction]
+        assert (ti, ta, tb, tc) == (i, *want)
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_flux_unpack_inverts_the_pack_permutation(direction):
+    """A physical face array packed along its direction (ghost width 0, the
+    face-extended extents as the box) and unpacked again is unchanged."""
+    extents, nv = (5, 6, 7), 3
+    fe = oracle.flux_extents(extents, direction)
+    phys = inputs.normal_f64(12, direction, int(np.prod(fe)) * nv)
+    fields = [phys[i * int(np.prod(fe)):(i + 1) * int(np.prod(fe))] for i in range(nv)]
+    sweep = oracle.weno_pack(fields, fe, 0, direction)
+    back = oracle.flux_unpack(sweep, nv, extents, direction)
+    assert np.array_equal(back.view(np.uint64), phys.view(np.uint64))
