@@ -485,6 +485,50 @@ def run_reference(args):
     return 0
 
 
+def time_extra_sweeps(torch, sw, stream, reps=5):
+    """Rows beyond the benchmark step (the accumulating flux difference and
+    the directional flux copy back to the physical frame), each timed on
+    its own with CUDA events on the launching stream: median of ``reps``
+    calls after one warm-up call, on the 8 x 201^3 flux workload's buffers."""
+    from finite_volume_field_gb300 import api
+    peaks, _ = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    cells = _prod(RHS_EXT) * RHS_NV
+    out = {}
+    scratch = torch.empty_like(sw.rhs_flux[1])
+    for k in (1, 2):
+        ax = "xyz"[k]
+        faces = sw.rhs_flux[k].numel()
+        jobs = {
+            f"rhs_add_{ax}": (lambda k=k: api.advect_rhs_add(sw.rhs_flux[k], sw.rhs_invd[k], RHS_NV,
+                                                             RHS_EXT, k, sw.rhs_out[k], stream),
+                              8 * (faces + 2 * cells + RHS_EXT[k]), cells, 3),
+            f"unpack_{ax}": (lambda k=k: api.flux_unpack(sw.rhs_flux[k], RHS_NV, RHS_EXT, k, scratch,
+                                                         stream),
+                             16 * faces, faces, 0),
+        }
+        for name, (fn, nbytes, units, flops) in jobs.items():
+            fn()
+            times = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            t = statistics.median(times)
+            rec = {"ms": round(t, 4), "gbs": round(nbytes / (t * 1e-3) / 1e9, 1),
+                   "gcell_var_per_s": round(units / (t * 1e-3) / 1e9, 2),
+                   "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / hbm, 4)}
+            if flops:
+                tf = flops * units / (t * 1e-3) / 1e12
+                rec.update(fp64_tflops=round(tf, 4), frac_fp64=round(tf / FP64_NOMINAL_TFLOPS, 4))
+            out[name] = rec
+    del scratch
+    return out
+
+
 def aggregate(per_rank, world):
     """Combine per-rank measurements: device time is the max over ranks,
     throughput counts the work of every rank."""
@@ -577,6 +621,8 @@ def run_gpu(args):
     barrier()
     del sw2
 
+    extras = time_extra_sweeps(torch, sw, stream)
+
     mine = {"ms_per_step": ms_per_step, "e2e_ms_per_step": e2e_ms, "launches": launches}
     if world > 1:
         import torch.distributed as dist
@@ -645,6 +691,7 @@ def run_gpu(args):
                     "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps},
             "gpu_launches": launches,
             "clocks": clocks,
+            "extra_sweeps": extras,
         }
         if world == 1 and not args.no_cpu_baseline:
             b, cv, sec, threads = oracle_sample(host)

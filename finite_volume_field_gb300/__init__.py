@@ -1,14 +1,17 @@
 """GB300-native per-cell field sweeps: 2D 5-point diffusion with ping-pong
 buffers, the multi-variable WENO input pack and the finite-volume
-flux-difference source, as sm_103a CUDA kernels behind a C ABI
+flux-difference source (assigned or accumulated) and the directional flux
+copy back to the physical frame, as sm_103a CUDA kernels behind a C ABI
 (include/fvf.h, libfvf.so).
 
 The public calls are re-exported from ``api``; they load libfvf.so on first
 use and raise if it is missing.  ``inputs`` holds the seeded synthetic input
 generators.
 """
-from .api import (FVF_FP32, FVF_FP64, MAX_NV, FvfError, advect_rhs, diffuse2d_step,
-                  last_cuda_error, launch_count, load, status_string, weno_pack)
+from .api import (FVF_FP32, FVF_FP64, MAX_NV, FvfError, advect_rhs, advect_rhs_add,
+                  diffuse2d_step, flux_unpack, last_cuda_error, launch_count, load,
+                  status_string, weno_pack)
 
-__all__ = ["FVF_FP32", "FVF_FP64", "MAX_NV", "FvfError", "advect_rhs", "diffuse2d_step",
-           "last_cuda_error", "launch_count", "load", "status_string", "weno_pack"]
+__all__ = ["FVF_FP32", "FVF_FP64", "MAX_NV", "FvfError", "advect_rhs", "advect_rhs_add",
+           "diffuse2d_step", "flux_unpack", "last_cuda_error", "launch_count", "load",
+           "status_string", "weno_pack"]

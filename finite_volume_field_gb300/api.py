@@ -49,6 +49,10 @@ def load() -> ctypes.CDLL:
     lib.weno_pack.restype = cint
     lib.advect_rhs.argtypes = [vp, vp, cint, ctypes.POINTER(i64), cint, vp, vp]
     lib.advect_rhs.restype = cint
+    lib.advect_rhs_add.argtypes = [vp, vp, cint, ctypes.POINTER(i64), cint, vp, vp]
+    lib.advect_rhs_add.restype = cint
+    lib.flux_unpack.argtypes = [vp, cint, ctypes.POINTER(i64), cint, vp, vp]
+    lib.flux_unpack.restype = cint
     lib.fvf_status_string.argtypes = [cint]
     lib.fvf_status_string.restype = ctypes.c_char_p
     lib.fvf_last_cuda_error.argtypes = []
@@ -151,3 +155,22 @@ def advect_rhs(flux, inv_d, nv: int, extents, dir: int, rhs, stream=None) -> Non
                            int(nv), _extents(extents), int(dir), _addr(rhs, torch.float64, "rhs"),
                            _stream(stream))
     _check("advect_rhs", st)
+
+
+def advect_rhs_add(flux, inv_d, nv: int, extents, dir: int, rhs, stream=None) -> None:
+    """Enqueue rhs += the flux-difference term along ``dir``."""
+    import torch
+    st = load().advect_rhs_add(_addr(flux, torch.float64, "flux"),
+                               _addr(inv_d, torch.float64, "inv_d"), int(nv), _extents(extents),
+                               int(dir), _addr(rhs, torch.float64, "rhs"), _stream(stream))
+    _check("advect_rhs_add", st)
+
+
+def flux_unpack(sweep_flux, nv: int, extents, dir: int, out, stream=None) -> None:
+    """Enqueue the directional flux copy from the sweep frame to the physical
+    frame."""
+    import torch
+    st = load().flux_unpack(_addr(sweep_flux, torch.float64, "sweep_flux"), int(nv),
+                            _extents(extents), int(dir), _addr(out, torch.float64, "out"),
+                            _stream(stream))
+    _check("flux_unpack", st)

@@ -1,4 +1,5 @@
-// advect_rhs.cu -- finite-volume flux-difference source for sm_103a.
+// advect_rhs.cu -- finite-volume flux-difference source for sm_103a,
+// assigned or accumulated into an existing rhs.
 //
 // Operation (MFlowCode/MFC pull request #2087, "Changes",
 // s_compute_advection_source_term, x/y/z flux differences):
@@ -22,7 +23,7 @@ namespace {
 
 // F extents per variable (F1, F2, F3); the high face of a cell is `step`
 // elements after its low face (1, F1 or F1*F2).
-template <int DIR>
+template <int DIR, bool ACC>
 __global__ void __launch_bounds__(256)
 advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ inv_d, int nv,
                   int64_t n1, int64_t n2, int64_t n3, double *__restrict__ rhs) {
@@ -45,7 +46,9 @@ advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ in
         for (int i = 0; i < nv; ++i) {
             const double a = __ldg(f + (int64_t)i * fplane);
             const double b = __ldg(f + (int64_t)i * fplane + step);
-            r[(int64_t)i * rplane] = __dmul_rn(w, __dsub_rn(a, b));
+            const double term = __dmul_rn(w, __dsub_rn(a, b));
+            // accumulate form: the term added once to the existing rhs
+            r[(int64_t)i * rplane] = ACC ? __dadd_rn(r[(int64_t)i * rplane], term) : term;
         }
     }
 }
@@ -53,19 +56,23 @@ advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ in
 }  // namespace
 
 cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
-                              const int64_t n[3], int dir, double *rhs, cudaStream_t stream,
-                              uint64_t *launches) {
+                              const int64_t n[3], int dir, bool accumulate, double *rhs,
+                              cudaStream_t stream, uint64_t *launches) {
     const dim3 block(64, 4);
     const int64_t gx = (n[0] + 63) / 64;
     const int64_t gy = (n[1] * n[2] + 3) / 4;
     if (gx > 0x7fffffff) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
-    if (dir == 0)
-        advect_rhs_kernel<0><<<grid, block, 0, stream>>>(flux, inv_d, nv, n[0], n[1], n[2], rhs);
-    else if (dir == 1)
-        advect_rhs_kernel<1><<<grid, block, 0, stream>>>(flux, inv_d, nv, n[0], n[1], n[2], rhs);
-    else
-        advect_rhs_kernel<2><<<grid, block, 0, stream>>>(flux, inv_d, nv, n[0], n[1], n[2], rhs);
+#define FVF_RHS_LAUNCH(D, A) \
+    advect_rhs_kernel<D, A><<<grid, block, 0, stream>>>(flux, inv_d, nv, n[0], n[1], n[2], rhs)
+    if (dir == 0) {
+        if (accumulate) FVF_RHS_LAUNCH(0, true); else FVF_RHS_LAUNCH(0, false);
+    } else if (dir == 1) {
+        if (accumulate) FVF_RHS_LAUNCH(1, true); else FVF_RHS_LAUNCH(1, false);
+    } else {
+        if (accumulate) FVF_RHS_LAUNCH(2, true); else FVF_RHS_LAUNCH(2, false);
+    }
+#undef FVF_RHS_LAUNCH
     ++*launches;
     return cudaGetLastError();
 }

@@ -174,8 +174,9 @@ FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents
     return cuda_status(e);
 }
 
-FVF_API int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
-                       int dir, double *rhs, void *stream) {
+static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
+                           const int64_t extents[3], int dir, bool accumulate, double *rhs,
+                           void *stream) {
     if (!extents) return FVF_ERR_NULL;
     if (dir < 0 || dir > 2) return FVF_ERR_DIR;
     if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
@@ -202,8 +203,58 @@ FVF_API int advect_rhs(const double *flux, const double *inv_d, int nv, const in
     if (overlaps(rhs, rbytes, flux, fbytes) || overlaps(rhs, rbytes, inv_d, wbytes))
         return FVF_ERR_ALIAS;
     uint64_t launched = 0;
-    const cudaError_t e = launch_advect_rhs(flux, inv_d, nv, n, dir, rhs, (cudaStream_t)stream,
-                                            &launched);
+    const cudaError_t e = launch_advect_rhs(flux, inv_d, nv, n, dir, accumulate, rhs,
+                                            (cudaStream_t)stream, &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
+FVF_API int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
+                       int dir, double *rhs, void *stream) {
+    return advect_rhs_impl(flux, inv_d, nv, extents, dir, false, rhs, stream);
+}
+
+FVF_API int advect_rhs_add(const double *flux, const double *inv_d, int nv,
+                           const int64_t extents[3], int dir, double *rhs, void *stream) {
+    return advect_rhs_impl(flux, inv_d, nv, extents, dir, true, rhs, stream);
+}
+
+// The inverse of the pack's axis exchange is the same exchange, so the copy
+// back to the physical frame is the pack of the sweep-frame face box (its
+// extents as the interior, ghost width 0), with the variables' planes of the
+// one input array as the field table.
+FVF_API int flux_unpack(const double *sweep_flux, int nv, const int64_t extents[3], int dir,
+                        double *out, void *stream) {
+    if (!extents) return FVF_ERR_NULL;
+    if (dir < 0 || dir > 2) return FVF_ERR_DIR;
+    if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
+    for (int a = 0; a < 3; ++a)
+        if (extents[a] < 0) return FVF_ERR_SIZE;
+    const int64_t n1 = extents[0], n2 = extents[1], n3 = extents[2];
+    const int64_t S[3][3] = {{n1 + 1, n2, n3}, {n2 + 1, n1, n3}, {n3 + 1, n2, n1}};
+    Box box;
+    for (int a = 0; a < 3; ++a) {
+        box.n[a] = S[dir][a];
+        box.N[a] = S[dir][a];
+        box.g[a] = 0;
+    }
+    int64_t t = 0, plane = 0, elems = 0;
+    if (!mul_ok(box.n[0], box.n[1], &t) || !mul_ok(t, box.n[2], &plane) ||
+        !mul_ok(plane, nv, &elems))
+        return FVF_ERR_SIZE;
+    if (n1 == 0 || n2 == 0 || n3 == 0 || elems == 0) return FVF_OK;
+    if (!sweep_flux || !out) return FVF_ERR_NULL;
+    if ((uintptr_t)sweep_flux % 8 || (uintptr_t)out % 8) return FVF_ERR_ALIGN;
+    const uint64_t bytes = (uint64_t)elems * 8;
+    int st = check_device_array(sweep_flux, bytes);
+    if (st == FVF_OK) st = check_device_array(out, bytes);
+    if (st != FVF_OK) return st;
+    if (overlaps(sweep_flux, bytes, out, bytes)) return FVF_ERR_ALIAS;
+    FieldTable table;
+    std::memset(&table, 0, sizeof(table));
+    for (int i = 0; i < nv; ++i) table.p[i] = sweep_flux + (int64_t)i * plane;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_weno_pack(table, nv, box, dir, out, (cudaStream_t)stream, &launched);
     g_launches += launched;
     return cuda_status(e);
 }

@@ -37,7 +37,7 @@ cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, i
                              double *out, cudaStream_t stream, uint64_t *launches);
 
 cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
-                              const int64_t n[3], int dir, double *rhs,
+                              const int64_t n[3], int dir, bool accumulate, double *rhs,
                               cudaStream_t stream, uint64_t *launches);
 
 }  // namespace fvf

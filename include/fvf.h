@@ -1,8 +1,9 @@
 /*
  * fvf.h -- C ABI of libfvf.so, the GB300 (sm_103a) library of per-cell field
  * sweeps: the explicit 2D 5-point diffusion step with ping-pong buffers, the
- * multi-variable WENO input pack and the finite-volume flux-difference
- * source.
+ * multi-variable WENO input pack, the finite-volume flux-difference source
+ * (assigned or accumulated) and the directional flux copy back to the
+ * physical frame.
  *
  * Sources of the operations (pages, by title and section):
  *   [Q] Qiita, "Fortran 2018でGPUを高速化する Part 3" ("Fortran 2018 GPU
@@ -12,8 +13,9 @@
  *       (alpha = 0.1_real32 in FP32).
  *   [M] MFlowCode/MFC pull request #2087, "Collapse only spatial loops in
  *       per-variable GPU kernels": "Changes" (s_pack_weno_input_arr,
- *       s_compute_advection_source_term) and "Why this is faster" (one thread
- *       per spatial cell, variables looped inside the thread).
+ *       s_compute_advection_source_term, s_finalize_riemann_solver) and "Why
+ *       this is faster" (one thread per spatial cell, variables looped inside
+ *       the thread).
  *
  * Conventions common to every entry point
  *   - All array pointers are DEVICE pointers owned by the caller (for
@@ -139,6 +141,37 @@ int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int
  */
 int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
                int dir, double *rhs, void *stream);
+
+/*
+ * advect_rhs_add -- the accumulating form of advect_rhs: the same term,
+ * added once to the existing rhs,
+ *     rhs(j,k,l,i) = rhs(j,k,l,i) + inv_d(c) * (F(c-1) - F(c)),
+ * so that the x, y and z calls build the finite-volume right-hand side (the
+ * x/y/z flux differences of [M] "Changes", s_compute_advection_source_term,
+ * are the terms of one sum).  Arguments, layouts and validation as for
+ * advect_rhs; rhs is read and written.
+ */
+int advect_rhs_add(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
+                   int dir, double *rhs, void *stream);
+
+/*
+ * flux_unpack -- the directional flux copy from the sweep frame back to the
+ * physical frame ([M] "Changes", s_finalize_riemann_solver): the inverse of
+ * the pack's axis exchange, for face arrays.  A bit copy.
+ *
+ *   sweep_flux  contiguous doubles, swept axis first with its n+1 faces,
+ *               variable slowest:
+ *                 dir 0: in(f,k,l,i), extents (n1+1, n2, n3)
+ *                 dir 1: in(f,j,l,i), extents (n2+1, n1, n3)
+ *                 dir 2: in(f,k,j,i), extents (n3+1, n2, n1)
+ *   nv          0..FVF_MAX_NV (0: nothing to do).
+ *   extents     HOST array {n1, n2, n3} of cell counts, each >= 0.
+ *   out         the face array in the physical frame (the layout advect_rhs
+ *               reads): extents (n1+1,n2,n3), (n1,n2+1,n3) or (n1,n2,n3+1),
+ *               j fastest, variable slowest; must not overlap sweep_flux.
+ */
+int flux_unpack(const double *sweep_flux, int nv, const int64_t extents[3], int dir,
+                double *out, void *stream);
 
 /* Static, NUL-terminated name of a status code ("unknown status" if none). */
 const char *fvf_status_string(int status);

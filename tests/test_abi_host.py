@@ -133,6 +133,24 @@ def test_rhs_validation(lib):
     assert f(4096, 65536, 2, ext, 0, 4096 + 640, None) == C["FVF_ERR_NOT_DEVICE"]
 
 
+def test_unpack_and_rhs_add_validation(lib):
+    u, a = lib.flux_unpack, lib.advect_rhs_add
+    ext = E3(3, 4, 5)
+    assert u(4096, 2, None, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert u(4096, 2, ext, 3, 65536, None) == C["FVF_ERR_DIR"]
+    assert u(4096, 65, ext, 0, 65536, None) == C["FVF_ERR_NV"]
+    assert u(4096, 2, E3(3, -1, 5), 0, 65536, None) == C["FVF_ERR_SIZE"]
+    assert u(None, 0, ext, 0, None, None) == C["FVF_OK"]
+    assert u(None, 2, E3(3, 0, 5), 1, None, None) == C["FVF_OK"]
+    assert u(None, 2, ext, 0, 65536, None) == C["FVF_ERR_NULL"]
+    assert u(4100, 2, ext, 0, 65536, None) == C["FVF_ERR_ALIGN"]
+    assert u(4096, 2, ext, 0, 65536, None) == C["FVF_ERR_NOT_DEVICE"]
+    assert a(4096, 8192, 2, ext, 3, 65536, None) == C["FVF_ERR_DIR"]
+    assert a(4096, 8192, 0, ext, 0, None, None) == C["FVF_OK"]
+    assert a(4096, 8192, 2, ext, 0, None, None) == C["FVF_ERR_NULL"]
+    assert a(4096, 8192, 2, ext, 0, 65536, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
 def test_binding_rejects_cpu_tensors(lib):
     torch = pytest.importorskip("torch")
     u = torch.zeros(8, 8, dtype=torch.float64)
