@@ -487,9 +487,10 @@ def run_reference(args):
 
 def time_extra_sweeps(torch, sw, stream, reps=5):
     """Rows beyond the benchmark step (the accumulating flux difference and
-    the directional flux copy back to the physical frame), each timed on
-    its own with CUDA events on the launching stream: median of ``reps``
-    calls after one warm-up call, on the 8 x 201^3 flux workload's buffers."""
+    the directional flux copy back to the physical frame, on the 8 x 201^3
+    flux workload's buffers) and the latency of the 64 x 64 FP64 diffusion
+    case, each timed on its own with CUDA events on the launching stream:
+    median of several calls after one warm-up call."""
     from finite_volume_field_gb300 import api
     peaks, _ = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -526,6 +527,24 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
                 rec.update(fp64_tflops=round(tf, 4), frac_fp64=round(tf / FP64_NOMINAL_TFLOPS, 4))
             out[name] = rec
     del scratch
+    # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
+    # (both states live in shared memory), reported per call and per step
+    u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)
+    u[31 + 64 * 31] = 1.0
+    v = torch.zeros_like(u)
+    call = lambda: api.diffuse2d_step(u, v, 64, 64, 0.1, 32, api.FVF_FP64, stream)  # noqa: E731
+    call()
+    times = []
+    for _ in range(20):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    t = statistics.median(times)
+    out["diffuse_64x64_fp64_32steps"] = {"us_per_call": round(1e3 * t, 2),
+                                         "us_per_step": round(1e3 * t / 32, 3)}
     return out
 
 

@@ -26,8 +26,15 @@
 //          blocks as fit on the SMs at once, each taking an equal band of
 //          rows.
 //   scalar (any size or alignment): one thread per cell.
+//   cluster (small grids, nsteps >= 2): all steps in one launch, the grid in
+//          the shared memory of an 8-block thread-block cluster.  The
+//          cluster, blocked and march kernels are described below.
+#include <cooperative_groups.h>
+
 #include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 // How the FP64 update splits its additions between the FP64 unit and the
 // integer pipes (fp64_emu.cuh).  Every split gives bit-identical results; the
@@ -416,6 +423,90 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
     }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster kernel: a small grid in the shared memory of one thread-block
+// cluster, every step in one launch
+// ---------------------------------------------------------------------------
+//
+// For grids of up to a few tens of thousands of cells the time goes to
+// launch latency and, for FP64, to arithmetic that one SM would do alone.  A
+// cluster of kClusterSize blocks (one per SM) splits the rows into bands:
+// each block keeps both ping-pong states of its band in its own shared
+// memory, reads the row just above and just below its band from the
+// neighbouring blocks' shared memory (distributed shared memory), and the
+// blocks separate steps with the cluster barrier (a hardware barrier: every
+// block of a cluster is resident at once).  Each cell gets the same update()
+// as in the other kernels, so the same bits.  At the end every block writes
+// its band of the last state to the result array and of the state before it
+// to the other array.
+constexpr int kClusterSize = 8;
+constexpr int kClusterThreads = 512;
+constexpr int64_t kClusterMaxBytes = 200 * 1024;   // per block: both states of a band
+
+template <typename T>
+__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kClusterThreads)
+diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restrict__ v, int nx,
+                       int ny, int band, int64_t nsteps, T alpha) {
+    extern __shared__ unsigned char smem_raw[];
+    T *const st0 = reinterpret_cast<T *>(smem_raw);
+    T *const st1 = st0 + band * nx;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    const int r0 = rank * band;
+    const int rows = max(0, min(band, ny - r0));
+    const int cells = rows * nx;
+    for (int c = threadIdx.x; c < cells; c += kClusterThreads) st0[c] = u0[(int64_t)r0 * nx + c];
+    cluster.sync();
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        T *in = (s & 1) ? st0 : st1;
+        T *out = (s & 1) ? st1 : st0;
+        // the neighbours' copies of the same state (rows r0-1 and r0+rows)
+        const T *above = rank > 0 ? cluster.map_shared_rank(in, rank - 1) : nullptr;
+        const T *below = rank + 1 < kClusterSize ? cluster.map_shared_rank(in, rank + 1) : nullptr;
+        for (int c = threadIdx.x; c < cells; c += kClusterThreads) {
+            const int lr = c / nx, i = c - lr * nx;
+            const int j = r0 + lr;
+            if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1) {
+                out[c] = T(0);
+            } else {
+                const T sv = lr > 0 ? in[c - nx] : above[(band - 1) * nx + i];
+                const T nv = lr + 1 < rows ? in[c + nx] : below[i];
+                out[c] = update<T>(in[c], in[c - 1], in[c + 1], sv, nv, alpha);
+            }
+        }
+        cluster.sync();
+    }
+    // state n is in st[n & 1]; it belongs in v for odd n and in u for even n
+    const T *last = (nsteps & 1) ? st1 : st0, *prev = (nsteps & 1) ? st0 : st1;
+    T *res = (nsteps & 1) ? v : u, *oth = (nsteps & 1) ? u : v;
+    for (int c = threadIdx.x; c < cells; c += kClusterThreads) {
+        res[(int64_t)r0 * nx + c] = last[c];
+        oth[(int64_t)r0 * nx + c] = prev[c];
+    }
+}
+
+// Band height and whether the cluster kernel applies (nsteps >= 2: step n-1
+// must exist for the other buffer).
+template <typename T>
+int cluster_band(int64_t nx, int64_t ny, int64_t nsteps) {
+    if (nsteps < 2 || nx > 65536 || ny > 65536) return 0;
+    const int64_t band = (ny + kClusterSize - 1) / kClusterSize;
+    if (band * nx * 2 * (int64_t)sizeof(T) > kClusterMaxBytes) return 0;
+    return (int)band;
+}
+
+template <typename T>
+cudaError_t cluster_prepare() {
+    static cudaError_t status = cudaErrorNotReady;
+    if (status == cudaErrorNotReady) {
+        status = cudaFuncSetAttribute(diffuse_cluster_kernel<T>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kClusterMaxBytes);
+        if (status != cudaSuccess) cudaGetLastError();
+    }
+    return status;
+}
+
 constexpr size_t tblock_smem_bytes(size_t elem) { return 2 * (size_t)kTbW * kTbH * elem; }
 
 // Whether to run blocks of steps in shared memory: FP32 is HBM-bound, so
@@ -484,8 +575,20 @@ struct SingleStep {
 template <typename T>
 cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
                 cudaStream_t stream, uint64_t *launches) {
+    cudaError_t e;
+    if (const int band = cluster_band<T>(nx, ny, nsteps)) {
+        if (cluster_prepare<T>() == cudaSuccess) {
+            // u is both the input and an output: every block reads its band
+            // before the first cluster barrier and writes after the last.
+            const size_t smem = (size_t)(2 * band * nx) * sizeof(T);
+            diffuse_cluster_kernel<T><<<kClusterSize, kClusterThreads, smem, stream>>>(
+                u, u, v, (int)nx, (int)ny, band, nsteps, alpha);
+            ++*launches;
+            return cudaGetLastError();
+        }
+    }
     SingleStep<T> one;
-    cudaError_t e = one.setup(u, v, nx, ny);
+    e = one.setup(u, v, nx, ny);
     if (e != cudaSuccess) return e;
     if (use_tblock<T>(nx, ny, nsteps) && tblock_prepare<T>() == cudaSuccess) {
         // Steps 1..n-1 in B blocked launches, step n as one single-step
