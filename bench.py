@@ -486,47 +486,72 @@ def run_reference(args):
 
 
 def time_extra_sweeps(torch, sw, stream, reps=5):
-    """Rows beyond the benchmark step (the accumulating flux difference and
-    the directional flux copy back to the physical frame, on the 8 x 201^3
-    flux workload's buffers) and the latency of the 64 x 64 FP64 diffusion
-    case, each timed on its own with CUDA events on the launching stream:
-    median of several calls after one warm-up call."""
+    """Rows beyond the benchmark step, each timed on its own with CUDA events
+    on the launching stream (median of several calls after one warm-up call):
+    the accumulating flux difference and the directional flux copy back to
+    the physical frame on the 8 x 201^3 flux workload's buffers, the
+    conservative-variable copy alone and fused with the pack on the 8 x 207^3
+    pack workload's fields, and the latency of the 64 x 64 FP64 diffusion
+    case."""
     from finite_volume_field_gb300 import api
     peaks, _ = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
     cells = _prod(RHS_EXT) * RHS_NV
     out = {}
+
+    def timed(fn):
+        fn()
+        times = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
+
+    def record(name, fn, nbytes, units, flops=0):
+        t = timed(fn)
+        rec = {"ms": round(t, 4), "gbs": round(nbytes / (t * 1e-3) / 1e9, 1),
+               "gcell_var_per_s": round(units / (t * 1e-3) / 1e9, 2),
+               "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / hbm, 4)}
+        if flops:
+            tf = flops * units / (t * 1e-3) / 1e12
+            rec.update(fp64_tflops=round(tf, 4), frac_fp64=round(tf / FP64_NOMINAL_TFLOPS, 4))
+        out[name] = rec
+
     scratch = torch.empty_like(sw.rhs_flux[1])
     for k in (1, 2):
         ax = "xyz"[k]
         faces = sw.rhs_flux[k].numel()
-        jobs = {
-            f"rhs_add_{ax}": (lambda k=k: api.advect_rhs_add(sw.rhs_flux[k], sw.rhs_invd[k], RHS_NV,
-                                                             RHS_EXT, k, sw.rhs_out[k], stream),
-                              8 * (faces + 2 * cells + RHS_EXT[k]), cells, 3),
-            f"unpack_{ax}": (lambda k=k: api.flux_unpack(sw.rhs_flux[k], RHS_NV, RHS_EXT, k, scratch,
-                                                         stream),
-                             16 * faces, faces, 0),
-        }
-        for name, (fn, nbytes, units, flops) in jobs.items():
-            fn()
-            times = []
-            for _ in range(reps):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                e1.synchronize()
-                times.append(e0.elapsed_time(e1))
-            t = statistics.median(times)
-            rec = {"ms": round(t, 4), "gbs": round(nbytes / (t * 1e-3) / 1e9, 1),
-                   "gcell_var_per_s": round(units / (t * 1e-3) / 1e9, 2),
-                   "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / hbm, 4)}
-            if flops:
-                tf = flops * units / (t * 1e-3) / 1e12
-                rec.update(fp64_tflops=round(tf, 4), frac_fp64=round(tf / FP64_NOMINAL_TFLOPS, 4))
-            out[name] = rec
+        record(f"rhs_add_{ax}",
+               lambda k=k: api.advect_rhs_add(sw.rhs_flux[k], sw.rhs_invd[k], RHS_NV, RHS_EXT, k,
+                                              sw.rhs_out[k], stream),
+               8 * (faces + 2 * cells + RHS_EXT[k]), cells, 3)
+        record(f"unpack_{ax}",
+               lambda k=k: api.flux_unpack(sw.rhs_flux[k], RHS_NV, RHS_EXT, k, scratch, stream),
+               16 * faces, faces)
     del scratch
+    # conservative-variable copy: alone, fused with the pack, and the unfused
+    # pair (pack then copy) for comparison
+    copies = [torch.empty_like(f) for f in sw.pack_fields]
+    nst = sw.pack_fields[0].numel() * PACK_NV
+    record("fields_copy",
+           lambda: api.fields_copy(sw.pack_fields, PACK_NV, PACK_EXT, PACK_G, copies, stream),
+           16 * nst, nst)
+    for k, ax in enumerate("xyz"):
+        npk = _prod(pack_extents(PACK_EXT, PACK_G, k)) * PACK_NV
+        record(f"pack_copy_{ax}",
+               lambda k=k: api.weno_pack_copy(sw.pack_fields, PACK_NV, PACK_EXT, PACK_G, k,
+                                              sw.pack_out[k], copies, stream),
+               8 * (2 * nst + npk), nst)
+
+        def unfused(k=k):
+            api.weno_pack(sw.pack_fields, PACK_NV, PACK_EXT, PACK_G, k, sw.pack_out[k], stream)
+            api.fields_copy(sw.pack_fields, PACK_NV, PACK_EXT, PACK_G, copies, stream)
+        record(f"pack_then_copy_{ax}", unfused, 8 * (2 * nst + npk), nst)
+    del copies
     # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
     # (both states live in shared memory), reported per call and per step
     u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)
@@ -731,7 +756,9 @@ def run_ncu_case():
     """Each sweep kernel at its benchmark size, one buffer set on the device
     at a time (at most about 1.1 GB), for Nsight Compute captures:
     diffusion 8192^2 FP64 then FP32, pack x/y/z on 8 fields of
-    207^3, flux difference x/y/z on 8 x 201^3.  FP64 runs 2 single steps, FP32 17 steps (two
+    207^3, the conservative-variable copy alone and fused with the pack x/y/z
+    on the same fields (at most about 1.7 GB), flux difference x/y/z on
+    8 x 201^3.  FP64 runs 2 single steps, FP32 17 steps (two
     8-step shared-memory launches, then one single step).  Device-generated values (the
     kernels' timing does not depend on them)."""
     import torch
@@ -756,7 +783,11 @@ def run_ncu_case():
                       device="cuda")
     for d in range(3):
         api.weno_pack(fields, PACK_NV, PACK_EXT, PACK_G, d, out)
-    del fields, out
+    copies = [torch.empty_like(f) for f in fields]
+    api.fields_copy(fields, PACK_NV, PACK_EXT, PACK_G, copies)
+    for d in range(3):
+        api.weno_pack_copy(fields, PACK_NV, PACK_EXT, PACK_G, d, out, copies)
+    del fields, out, copies
     free()
     for d in range(3):
         fe = list(RHS_EXT)

@@ -1,7 +1,8 @@
 """GB300-native per-cell field sweeps: 2D 5-point diffusion with ping-pong
 buffers, the multi-variable WENO input pack and the finite-volume
-flux-difference source (assigned or accumulated) and the directional flux
-copy back to the physical frame, as sm_103a CUDA kernels behind a C ABI
+flux-difference source (assigned or accumulated), the directional flux
+copy back to the physical frame and the conservative-variable copy (alone or
+fused with the pack), as sm_103a CUDA kernels behind a C ABI
 (include/fvf.h, libfvf.so).
 
 The public calls are re-exported from ``api``; they load libfvf.so on first
@@ -9,9 +10,9 @@ use and raise if it is missing.  ``inputs`` holds the seeded synthetic input
 generators.
 """
 from .api import (FVF_FP32, FVF_FP64, MAX_NV, FvfError, advect_rhs, advect_rhs_add,
-                  diffuse2d_step, flux_unpack, last_cuda_error, launch_count, load,
-                  status_string, weno_pack)
+                  diffuse2d_step, fields_copy, flux_unpack, last_cuda_error, launch_count, load,
+                  status_string, weno_pack, weno_pack_copy)
 
 __all__ = ["FVF_FP32", "FVF_FP64", "MAX_NV", "FvfError", "advect_rhs", "advect_rhs_add",
-           "diffuse2d_step", "flux_unpack", "last_cuda_error", "launch_count", "load",
-           "status_string", "weno_pack"]
+           "diffuse2d_step", "fields_copy", "flux_unpack", "last_cuda_error", "launch_count",
+           "load", "status_string", "weno_pack", "weno_pack_copy"]

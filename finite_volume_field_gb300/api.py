@@ -53,6 +53,12 @@ def load() -> ctypes.CDLL:
     lib.advect_rhs_add.restype = cint
     lib.flux_unpack.argtypes = [vp, cint, ctypes.POINTER(i64), cint, vp, vp]
     lib.flux_unpack.restype = cint
+    lib.fields_copy.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint,
+                                ctypes.POINTER(vp), vp]
+    lib.fields_copy.restype = cint
+    lib.weno_pack_copy.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint, cint, vp,
+                                   ctypes.POINTER(vp), vp]
+    lib.weno_pack_copy.restype = cint
     lib.fvf_status_string.argtypes = [cint]
     lib.fvf_status_string.restype = ctypes.c_char_p
     lib.fvf_last_cuda_error.argtypes = []
@@ -174,3 +180,27 @@ def flux_unpack(sweep_flux, nv: int, extents, dir: int, out, stream=None) -> Non
                             _extents(extents), int(dir), _addr(out, torch.float64, "out"),
                             _stream(stream))
     _check("flux_unpack", st)
+
+
+def _table(arrays, nv: int, name: str):
+    import torch
+    ptrs = [_addr(a, torch.float64, f"{name}[{i}]") for i, a in enumerate(list(arrays)[:nv])]
+    return (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs) if ptrs else None
+
+
+def fields_copy(fields, nv: int, extents, ghost: int, copies, stream=None) -> None:
+    """Enqueue the conservative-variable copy copies[i] = fields[i]."""
+    st = load().fields_copy(_table(fields, nv, "fields"), int(nv), _extents(extents), int(ghost),
+                            _table(copies, nv, "copies"), _stream(stream))
+    _check("fields_copy", st)
+
+
+def weno_pack_copy(fields, nv: int, extents, ghost: int, dir: int, out, copies,
+                   stream=None) -> None:
+    """Enqueue the WENO input pack along ``dir`` fused with the
+    conservative-variable copy of the same fields."""
+    import torch
+    st = load().weno_pack_copy(_table(fields, nv, "fields"), int(nv), _extents(extents),
+                               int(ghost), int(dir), _addr(out, torch.float64, "out"),
+                               _table(copies, nv, "copies"), _stream(stream))
+    _check("weno_pack_copy", st)

@@ -174,6 +174,123 @@ FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents
     return cuda_status(e);
 }
 
+// Pointer tables of the multi-variable calls: each entry non-NULL and 8-byte
+// aligned; fills *table (a FieldTable or CopyTable).
+template <typename Table, typename Ptr>
+static int fill_table(Ptr const *ptrs, int nv, Table *table) {
+    if (!ptrs) return FVF_ERR_NULL;
+    std::memset(table, 0, sizeof(*table));
+    for (int i = 0; i < nv; ++i) {
+        if (!ptrs[i]) return FVF_ERR_NULL;
+        if ((uintptr_t)ptrs[i] % 8) return FVF_ERR_ALIGN;
+        table->p[i] = ptrs[i];
+    }
+    return FVF_OK;
+}
+
+// Every entry of a table is `bytes` of device memory of this device.
+template <typename Ptr>
+static int check_device_table(Ptr const *ptrs, int nv, uint64_t bytes) {
+    for (int i = 0; i < nv; ++i) {
+        const int st = check_device_array(ptrs[i], bytes);
+        if (st != FVF_OK) return st;
+    }
+    return FVF_OK;
+}
+
+// A copy must overlap no field, no other copy and not out (out_bytes == 0:
+// no out).
+static bool copies_overlap(const double *const *fields, double *const *copies, int nv,
+                           uint64_t bytes, const double *out, uint64_t out_bytes) {
+    for (int i = 0; i < nv; ++i) {
+        for (int k = 0; k < nv; ++k) {
+            if (overlaps(copies[i], bytes, fields[k], bytes)) return true;
+            if (k != i && overlaps(copies[i], bytes, copies[k], bytes)) return true;
+        }
+        if (out_bytes && overlaps(copies[i], bytes, out, out_bytes)) return true;
+    }
+    return false;
+}
+
+// Stored box of interior extents with ghost width `ghost`; *stored gets
+// N1*N2*N3.  FVF_OK or the status of the first bad argument.
+static int make_box(const int64_t extents[3], int ghost, Box *box, int64_t *stored) {
+    if (!extents) return FVF_ERR_NULL;
+    if (ghost < 0) return FVF_ERR_SIZE;
+    for (int a = 0; a < 3; ++a) {
+        if (extents[a] < 0) return FVF_ERR_SIZE;
+        box->n[a] = extents[a];
+        box->g[a] = extents[a] > 1 ? ghost : 0;
+        box->N[a] = extents[a] > 1 ? extents[a] + 2 * (int64_t)ghost : extents[a];
+    }
+    int64_t t = 0;
+    if (!mul_ok(box->N[0], box->N[1], &t) || !mul_ok(t, box->N[2], stored)) return FVF_ERR_SIZE;
+    return FVF_OK;
+}
+
+FVF_API int fields_copy(const double *const *fields, int nv, const int64_t extents[3], int ghost,
+                        double *const *copies, void *stream) {
+    if (!extents) return FVF_ERR_NULL;
+    if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
+    Box box;
+    int64_t stored = 0, elems = 0;
+    int st = make_box(extents, ghost, &box, &stored);
+    if (st != FVF_OK) return st;
+    if (!mul_ok(stored, nv, &elems)) return FVF_ERR_SIZE;
+    if (elems == 0) return FVF_OK;
+    const uint64_t bytes = (uint64_t)stored * 8;
+    FieldTable ft;
+    CopyTable ct;
+    st = fill_table(fields, nv, &ft);
+    if (st == FVF_OK) st = fill_table(copies, nv, &ct);
+    if (st == FVF_OK) st = check_device_table(fields, nv, bytes);
+    if (st == FVF_OK) st = check_device_table(copies, nv, bytes);
+    if (st != FVF_OK) return st;
+    if (copies_overlap(fields, copies, nv, bytes, nullptr, 0)) return FVF_ERR_ALIAS;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_fields_copy(ft, nv, stored, ct, (cudaStream_t)stream, &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
+FVF_API int weno_pack_copy(const double *const *fields, int nv, const int64_t extents[3],
+                           int ghost, int dir, double *out, double *const *copies,
+                           void *stream) {
+    if (!extents) return FVF_ERR_NULL;
+    if (dir < 0 || dir > 2) return FVF_ERR_DIR;
+    if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
+    Box box;
+    int64_t stored = 0, t = 0, cells_out = 0, elems_out = 0;
+    int st = make_box(extents, ghost, &box, &stored);
+    if (st != FVF_OK) return st;
+    const int64_t M[3][3] = {{box.N[0], box.n[1], box.n[2]},
+                             {box.N[1], box.n[0], box.n[2]},
+                             {box.N[2], box.n[1], box.n[0]}};
+    if (!mul_ok(M[dir][0], M[dir][1], &t) || !mul_ok(t, M[dir][2], &cells_out) ||
+        !mul_ok(cells_out, nv, &elems_out) || !mul_ok(stored, nv, &t))
+        return FVF_ERR_SIZE;
+    if (elems_out == 0) return FVF_OK;
+    if (!out) return FVF_ERR_NULL;
+    if ((uintptr_t)out % 8) return FVF_ERR_ALIGN;
+    const uint64_t out_bytes = (uint64_t)elems_out * 8, in_bytes = (uint64_t)stored * 8;
+    FieldTable ft;
+    CopyTable ct;
+    st = fill_table(fields, nv, &ft);
+    if (st == FVF_OK) st = fill_table(copies, nv, &ct);
+    if (st == FVF_OK) st = check_device_array(out, out_bytes);
+    if (st == FVF_OK) st = check_device_table(fields, nv, in_bytes);
+    if (st == FVF_OK) st = check_device_table(copies, nv, in_bytes);
+    if (st != FVF_OK) return st;
+    for (int i = 0; i < nv; ++i)
+        if (overlaps(fields[i], in_bytes, out, out_bytes)) return FVF_ERR_ALIAS;
+    if (copies_overlap(fields, copies, nv, in_bytes, out, out_bytes)) return FVF_ERR_ALIAS;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_weno_pack_copy(ft, nv, box, dir, out, ct, (cudaStream_t)stream,
+                                                &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
 static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
                            const int64_t extents[3], int dir, bool accumulate, double *rhs,
                            void *stream) {

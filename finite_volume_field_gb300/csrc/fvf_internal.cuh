@@ -15,6 +15,12 @@ struct FieldTable {
     const double *p[kMaxNv];
 };
 
+// Output pointer table of the conservative-variable copies (one array per
+// variable, each the size of the stored box), passed by value like FieldTable.
+struct CopyTable {
+    double *p[kMaxNv];
+};
+
 // Box geometry of a 3D sweep: interior extents n, stored extents N (n + 2g on
 // axes with n > 1, else 1) and ghost offsets g (g where n > 1, else 0).
 struct Box {
@@ -35,6 +41,18 @@ cudaError_t launch_diffuse2d(void *u, void *v, int64_t nx, int64_t ny, double al
 
 cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
                              double *out, cudaStream_t stream, uint64_t *launches);
+
+// The conservative-variable copy alone: copy_i[e] = field_i[e] for the
+// `stored` elements of every variable.
+cudaError_t launch_fields_copy(const FieldTable &fields, int nv, int64_t stored,
+                               const CopyTable &copies, cudaStream_t stream, uint64_t *launches);
+
+// The pack fused with the conservative-variable copy: one pass reads every
+// stored element once, writes it to its copy and, inside the pack region, to
+// the packed output.
+cudaError_t launch_weno_pack_copy(const FieldTable &fields, int nv, const Box &box, int dir,
+                                  double *out, const CopyTable &copies, cudaStream_t stream,
+                                  uint64_t *launches);
 
 cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
                               const int64_t n[3], int dir, bool accumulate, double *rhs,

@@ -4,7 +4,9 @@
 // s_pack_weno_input_arr): out(a,b,c,i) = field_i(...) with the swept axis
 // first (x: no permutation; y: j and k exchanged; z: j and l exchanged), the
 // swept axis covering its ghost cells and the transverse axes their interior.
-// A pure 64-bit copy.
+// A pure 64-bit copy.  The same file holds the conservative-variable copy
+// (s_compute_rhs on the same page) alone and fused with the pack: the pack
+// reads the fields the copy reads, so the fused pass reads them once.
 //
 // Mapping ("Why this is faster" on the same page): one thread per spatial
 // output cell, the variable loop sequential inside the thread, the index
@@ -41,51 +43,84 @@ pack_x_kernel(FieldTable t, int nv, int64_t N1, int64_t N2, int64_t n2, int64_t 
     }
 }
 
-// Transposing pack (y or z).  The tile spans the swept axis (output-fast,
-// index a) and the j axis (input-fast, index jj); the third axis (index q) is
-// fixed per block.
-//   y: a = k (0..N2-1), jj = j (interior), q = l (interior); M = (N2, n1, n3)
-//      src = (jj+g1) + N1*(a + N2*(q+g3)),  dst = a + N2*(jj + n1*q)
-//   z: a = l (0..N3-1), jj = j (interior), q = k (interior); M = (N3, n2, n1)
-//      src = (jj+g1) + N1*((q+g2) + N2*a),  dst = a + N3*(q + n2*jj)
-// src = (jj + g1) + sa*a + sq*(q + gq); dst = a + da*jj + dq*q.
+// Transposing pack (y or z), optionally fused with the conservative-variable
+// copy.  The tile spans the swept axis (output-fast, index a, 0..na-1) and the
+// j axis (input-fast, index jt, 0..nj-1); the third axis (index q, 0..nq-1)
+// is fixed per block.
+//   source element    (jt + jo) + sa*a + sq*(q + qo)
+//   packed element    a + da*(jt - pj) + dq*(q - pq), written when
+//                     0 <= jt - pj < pnj and 0 <= q - pq < pnq
+// Pack alone: jt and q run over the interior (jo, qo = the ghost offsets,
+// pj = pq = 0).  Pack with copy: jt and q run over the whole stored box
+// (jo = qo = 0, pj, pq = the ghost offsets) and every loaded element is also
+// stored to its copy at the source index, a coalesced store along j.
+//   y: a = k, jt = j, q = l; packed extents (N2, n1, n3)
+//   z: a = l, jt = j, q = k; packed extents (N3, n2, n1)
 // The tile is double-buffered across variables: the loads of variable i+1
 // are in flight while variable i is stored, with one barrier per variable.
 constexpr int kPer = kTile / kRows;
 
+struct TransposeGeom {
+    int64_t na, nj, nq, jo, qo, pj, pq, pnj, pnq, sa, sq, da, dq, plane, tiles_a, tiles_j;
+};
+
+template <bool COPY>
 __global__ void __launch_bounds__(kTile * kRows)
-pack_transpose_kernel(FieldTable t, int nv, int64_t na, int64_t nj, int64_t nq, int64_t g1,
-                      int64_t gq, int64_t sa, int64_t sq, int64_t da, int64_t dq,
-                      int64_t plane, int64_t tiles_a, int64_t tiles_j,
+pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                       double *__restrict__ out) {
     __shared__ double tile[2][kTile][kTile + 1];
     int64_t blk = blockIdx.x;
-    const int64_t ta = blk % tiles_a;
-    blk /= tiles_a;
-    const int64_t tj = blk % tiles_j;
-    const int64_t q = blk / tiles_j;
+    const int64_t ta = blk % G.tiles_a;
+    blk /= G.tiles_a;
+    const int64_t tj = blk % G.tiles_j;
+    const int64_t q = blk / G.tiles_j;
     const int64_t a0 = ta * kTile, j0 = tj * kTile;
     const int tx = threadIdx.x, ty = threadIdx.y;
     // load side: lanes along j (contiguous in the field), rows along a
     const int64_t jl = j0 + tx;
-    const int64_t src0 = (jl + g1) + sa * (a0 + ty) + sq * (q + gq);
+    const int64_t src0 = (jl + G.jo) + G.sa * (a0 + ty) + G.sq * (q + G.qo);
     bool lok[kPer];
 #pragma unroll
-    for (int r = 0; r < kPer; ++r) lok[r] = jl < nj && a0 + ty + r * kRows < na;
+    for (int r = 0; r < kPer; ++r) lok[r] = jl < G.nj && a0 + ty + r * kRows < G.na;
+    const int64_t qp = q - G.pq;
+    if (COPY && (qp < 0 || qp >= G.pnq)) {
+        // a transverse ghost slice: copied, not packed (block-uniform branch)
+        for (int i = 0; i < nv; ++i) {
+            const double *f = t.p[i];
+            double *c = cp.p[i];
+            double v[kPer];
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : 0.0;
+#pragma unroll
+            for (int r = 0; r < kPer; ++r)
+                if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
+        }
+        return;
+    }
     // store side: lanes along a (contiguous in the output), rows along j
     const int64_t as = a0 + tx;
-    const int64_t dst0 = as + da * (j0 + ty) + dq * q;
+    const int64_t jp0 = j0 + ty - G.pj;
+    const int64_t dst0 = as + G.da * jp0 + G.dq * qp;
     bool sok[kPer];
 #pragma unroll
-    for (int r = 0; r < kPer; ++r) sok[r] = as < na && j0 + ty + r * kRows < nj;
+    for (int r = 0; r < kPer; ++r) {
+        const int64_t jp = jp0 + r * kRows;
+        sok[r] = as < G.na && jp >= 0 && jp < G.pnj;
+    }
 
     double v[kPer];
     {
         const double *f = t.p[0];
 #pragma unroll
-        for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + sa * (r * kRows)) : 0.0;
+        for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : 0.0;
 #pragma unroll
         for (int r = 0; r < kPer; ++r) tile[0][ty + r * kRows][tx] = v[r];
+        if (COPY) {
+            double *c = cp.p[0];
+#pragma unroll
+            for (int r = 0; r < kPer; ++r)
+                if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
+        }
     }
     __syncthreads();
     for (int i = 0; i < nv; ++i) {
@@ -95,27 +130,146 @@ pack_transpose_kernel(FieldTable t, int nv, int64_t na, int64_t nj, int64_t nq, 
             const double *f = t.p[i + 1];
 #pragma unroll
             for (int r = 0; r < kPer; ++r)
-                v[r] = lok[r] ? __ldg(f + src0 + sa * (r * kRows)) : 0.0;
+                v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : 0.0;
         }
-        double *o = out + (int64_t)i * plane + dst0;
+        const int64_t obase = (int64_t)i * G.plane + dst0;
 #pragma unroll
         for (int r = 0; r < kPer; ++r)
-            if (sok[r]) o[da * (r * kRows)] = tile[buf][tx][ty + r * kRows];
+            if (sok[r]) out[obase + G.da * (r * kRows)] = tile[buf][tx][ty + r * kRows];
         if (more) {
 #pragma unroll
             for (int r = 0; r < kPer; ++r) tile[buf ^ 1][ty + r * kRows][tx] = v[r];
+            if (COPY) {
+                double *c = cp.p[i + 1];
+#pragma unroll
+                for (int r = 0; r < kPer; ++r)
+                    if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
+            }
         }
         __syncthreads();
     }
 }
 
+// x pack fused with the copy: one thread per element of a stored row
+// (a = j over N1), rows (k, l) over the whole stored box.  Each element is
+// loaded once and stored to its copy, and to the packed output when its row
+// is a transverse-interior row.  Variables go in batches of kBatch: the
+// batch's loads are issued before its stores, so they overlap even though the
+// compiler cannot prove the copies and the fields apart.
+constexpr int kBatch = 8;
+
+__global__ void __launch_bounds__(256, 4)
+pack_copy_x_kernel(FieldTable t, CopyTable cp, int nv, int64_t N1, int64_t N2, int64_t N3,
+                   int64_t n2, int64_t n3, int64_t g2, int64_t g3, double *__restrict__ out) {
+    const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (a >= N1) return;
+    const int64_t plane = N1 * n2 * n3;
+    for (int64_t bc = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; bc < N2 * N3;
+         bc += (int64_t)gridDim.y * blockDim.y) {
+        const int64_t b = bc % N2 - g2, c = bc / N2 - g3;
+        const bool packed = b >= 0 && b < n2 && c >= 0 && c < n3;
+        const int64_t src = a + N1 * bc;
+        const int64_t dst = a + N1 * (b + n2 * c);
+        for (int i0 = 0; i0 < nv; i0 += kBatch) {
+            double x[kBatch];
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r)
+                if (i0 + r < nv) x[r] = __ldg(t.p[i0 + r] + src);
+#pragma unroll
+            for (int r = 0; r < kBatch; ++r) {
+                if (i0 + r < nv) {
+                    cp.p[i0 + r][src] = x[r];
+                    if (packed) out[(int64_t)(i0 + r) * plane + dst] = x[r];
+                }
+            }
+        }
+    }
+}
+
+// The copy alone over the flat stored box: one thread per element (per pair
+// of elements with 16-byte vectors when every pointer allows it), variables in
+// batches as above, grid-stride over one wave of blocks.
+template <bool V2>
+__global__ void __launch_bounds__(256)
+fields_copy_kernel(FieldTable t, CopyTable cp, int nv, int64_t total) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (V2) {
+        const int64_t pairs = total >> 1;
+        for (int64_t e = tid; e < pairs; e += stride) {
+            for (int i0 = 0; i0 < nv; i0 += kBatch) {
+                double2 x[kBatch];
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r)
+                    if (i0 + r < nv) x[r] = __ldg(reinterpret_cast<const double2 *>(t.p[i0 + r]) + e);
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r)
+                    if (i0 + r < nv) reinterpret_cast<double2 *>(cp.p[i0 + r])[e] = x[r];
+            }
+        }
+        if ((total & 1) && tid == 0)
+            for (int i = 0; i < nv; ++i) cp.p[i][total - 1] = __ldg(t.p[i] + total - 1);
+    } else {
+        for (int64_t e = tid; e < total; e += stride) {
+            for (int i0 = 0; i0 < nv; i0 += kBatch) {
+                double x[kBatch];
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r)
+                    if (i0 + r < nv) x[r] = __ldg(t.p[i0 + r] + e);
+#pragma unroll
+                for (int r = 0; r < kBatch; ++r)
+                    if (i0 + r < nv) cp.p[i0 + r][e] = x[r];
+            }
+        }
+    }
+}
+
 }  // namespace
+
+// Launch geometry of the transposing kernel for dir 1 or 2 (see above).
+static TransposeGeom transpose_geom(const Box &box, int dir, bool copy) {
+    const int64_t n1 = box.n[0], n2 = box.n[1], n3 = box.n[2];
+    const int64_t N1 = box.N[0], N2 = box.N[1], N3 = box.N[2];
+    const int64_t g1 = box.g[0];
+    TransposeGeom G;
+    int64_t nq, Nq, gq;
+    if (dir == 1) {
+        G.na = N2; nq = n3; Nq = N3; gq = box.g[2];
+        G.sa = N1; G.sq = N1 * N2; G.da = N2; G.dq = N2 * n1;
+        G.plane = N2 * n1 * n3;
+    } else {
+        G.na = N3; nq = n2; Nq = N2; gq = box.g[1];
+        G.sa = N1 * N2; G.sq = N1; G.da = N3 * n2; G.dq = N3;
+        G.plane = N3 * n2 * n1;
+    }
+    G.pnj = n1;
+    G.pnq = nq;
+    if (copy) {
+        G.nj = N1; G.nq = Nq; G.jo = 0; G.qo = 0; G.pj = g1; G.pq = gq;
+    } else {
+        G.nj = n1; G.nq = nq; G.jo = g1; G.qo = gq; G.pj = 0; G.pq = 0;
+    }
+    G.tiles_a = (G.na + kTile - 1) / kTile;
+    G.tiles_j = (G.nj + kTile - 1) / kTile;
+    return G;
+}
+
+template <bool COPY>
+static cudaError_t launch_transpose(const FieldTable &fields, const CopyTable &copies, int nv,
+                                    const Box &box, int dir, double *out, cudaStream_t stream) {
+    const TransposeGeom G = transpose_geom(box, dir, COPY);
+    const int64_t blocks = G.tiles_a * G.tiles_j * G.nq;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    pack_transpose_kernel<COPY><<<(unsigned)blocks, dim3(kTile, kRows), 0, stream>>>(
+        fields, copies, nv, G, out);
+    return cudaSuccess;
+}
 
 cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
                              double *out, cudaStream_t stream, uint64_t *launches) {
-    const int64_t n1 = box.n[0], n2 = box.n[1], n3 = box.n[2];
-    const int64_t N1 = box.N[0], N2 = box.N[1], N3 = box.N[2];
-    const int64_t g1 = box.g[0], g2 = box.g[1], g3 = box.g[2];
+    const int64_t n2 = box.n[1], n3 = box.n[2];
+    const int64_t N1 = box.N[0], N2 = box.N[1];
+    const int64_t g2 = box.g[1], g3 = box.g[2];
     if (dir == 0) {
         const dim3 block(64, 4);
         const int64_t gx = (N1 + 63) / 64;
@@ -124,21 +278,48 @@ cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, i
         const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
         pack_x_kernel<<<grid, block, 0, stream>>>(fields, nv, N1, N2, n2, n3, g2, g3, out);
     } else {
-        int64_t na, nj, nq, gq, sa, sq, da, dq;
-        if (dir == 1) {
-            na = N2; nj = n1; nq = n3; gq = g3;
-            sa = N1; sq = N1 * N2; da = N2; dq = N2 * n1;
-        } else {
-            na = N3; nj = n1; nq = n2; gq = g2;
-            sa = N1 * N2; sq = N1; da = N3 * n2; dq = N3;
-        }
-        const int64_t tiles_a = (na + kTile - 1) / kTile, tiles_j = (nj + kTile - 1) / kTile;
-        const int64_t blocks = tiles_a * tiles_j * nq;
-        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        const int64_t plane = na * nj * nq;
-        pack_transpose_kernel<<<(unsigned)blocks, dim3(kTile, kRows), 0, stream>>>(
-            fields, nv, na, nj, nq, g1, gq, sa, sq, da, dq, plane, tiles_a, tiles_j, out);
+        CopyTable none;
+        for (int i = 0; i < kMaxNv; ++i) none.p[i] = nullptr;
+        const cudaError_t e = launch_transpose<false>(fields, none, nv, box, dir, out, stream);
+        if (e != cudaSuccess) return e;
     }
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_weno_pack_copy(const FieldTable &fields, int nv, const Box &box, int dir,
+                                  double *out, const CopyTable &copies, cudaStream_t stream,
+                                  uint64_t *launches) {
+    if (dir == 0) {
+        const int64_t N1 = box.N[0], N2 = box.N[1], N3 = box.N[2];
+        const dim3 block(64, 4);
+        const int64_t gx = (N1 + 63) / 64;
+        const int64_t gy = (N2 * N3 + 3) / 4;
+        if (gx > 0x7fffffff) return cudaErrorInvalidValue;
+        const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
+        pack_copy_x_kernel<<<grid, block, 0, stream>>>(fields, copies, nv, N1, N2, N3, box.n[1],
+                                                      box.n[2], box.g[1], box.g[2], out);
+    } else {
+        const cudaError_t e = launch_transpose<true>(fields, copies, nv, box, dir, out, stream);
+        if (e != cudaSuccess) return e;
+    }
+    ++*launches;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_fields_copy(const FieldTable &fields, int nv, int64_t stored,
+                               const CopyTable &copies, cudaStream_t stream, uint64_t *launches) {
+    bool v2 = true;
+    for (int i = 0; i < nv; ++i)
+        v2 = v2 && ((uintptr_t)fields.p[i] % 16 == 0) && ((uintptr_t)copies.p[i] % 16 == 0);
+    const int64_t work = v2 ? (stored >> 1) + 1 : stored;
+    int64_t blocks = (work + 255) / 256;
+    const int64_t wave = (int64_t)sm_count() * 8;
+    if (blocks > wave) blocks = wave;
+    if (v2)
+        fields_copy_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(fields, copies, nv, stored);
+    else
+        fields_copy_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(fields, copies, nv, stored);
     ++*launches;
     return cudaGetLastError();
 }

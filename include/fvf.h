@@ -2,8 +2,8 @@
  * fvf.h -- C ABI of libfvf.so, the GB300 (sm_103a) library of per-cell field
  * sweeps: the explicit 2D 5-point diffusion step with ping-pong buffers, the
  * multi-variable WENO input pack, the finite-volume flux-difference source
- * (assigned or accumulated) and the directional flux copy back to the
- * physical frame.
+ * (assigned or accumulated), the directional flux copy back to the physical
+ * frame and the conservative-variable copy (alone or fused with the pack).
  *
  * Sources of the operations (pages, by title and section):
  *   [Q] Qiita, "Fortran 2018でGPUを高速化する Part 3" ("Fortran 2018 GPU
@@ -13,7 +13,8 @@
  *       (alpha = 0.1_real32 in FP32).
  *   [M] MFlowCode/MFC pull request #2087, "Collapse only spatial loops in
  *       per-variable GPU kernels": "Changes" (s_pack_weno_input_arr,
- *       s_compute_advection_source_term, s_finalize_riemann_solver) and "Why
+ *       s_compute_advection_source_term, s_finalize_riemann_solver,
+ *       s_compute_rhs) and "Why
  *       this is faster" (one thread per spatial cell, variables looped inside
  *       the thread).
  *
@@ -66,7 +67,7 @@ extern "C" {
 #define FVF_FP32 0
 #define FVF_FP64 1
 
-/* Largest number of variables weno_pack and advect_rhs accept. */
+/* Largest number of variables the multi-variable calls accept. */
 #define FVF_MAX_NV 64
 
 /*
@@ -172,6 +173,37 @@ int advect_rhs_add(const double *flux, const double *inv_d, int nv, const int64_
  */
 int flux_unpack(const double *sweep_flux, int nv, const int64_t extents[3], int dir,
                 double *out, void *stream);
+
+/*
+ * fields_copy -- the conservative-variable copy of [M] ("Changes",
+ * s_compute_rhs): copy_i = field_i element by element over the whole stored
+ * box, ghost cells included, for every variable.  A bit copy (NaN payloads and
+ * signed zeros preserved).
+ *
+ *   fields   HOST array of nv device pointers, each a stored box of
+ *            N1*N2*N3 doubles (layout above).  Fields may alias each other.
+ *   nv       0..FVF_MAX_NV (0: nothing to do).
+ *   extents  HOST array {n1, n2, n3} of interior extents, each >= 0.
+ *   ghost    ghost width g >= 0 (it only sets the stored extents N_a).
+ *   copies   HOST array of nv device pointers, each N1*N2*N3 doubles.  A
+ *            copy must not overlap any field or any other copy.
+ */
+int fields_copy(const double *const *fields, int nv, const int64_t extents[3], int ghost,
+                double *const *copies, void *stream);
+
+/*
+ * weno_pack_copy -- weno_pack and fields_copy of the same fields in one pass:
+ * each stored element is read once, written to its copy and, when it lies in
+ * the pack's region, to out.  The results equal those of weno_pack(fields,
+ * nv, extents, ghost, dir, out) and fields_copy(fields, nv, extents, ghost,
+ * copies).  [M] ("Changes") lists both loops, in s_compute_rhs and
+ * s_pack_weno_input_arr, over the same conservative-variable fields.
+ *
+ *   Arguments as for weno_pack, plus copies as for fields_copy.  out must
+ *   not overlap a field or a copy.
+ */
+int weno_pack_copy(const double *const *fields, int nv, const int64_t extents[3], int ghost,
+                   int dir, double *out, double *const *copies, void *stream);
 
 /* Static, NUL-terminated name of a status code ("unknown status" if none). */
 const char *fvf_status_string(int status);

@@ -73,6 +73,9 @@ def _load():
     lib.oracle_advect_rhs_add.restype = cint
     lib.oracle_flux_unpack.argtypes = [vp, cint, i64, i64, i64, cint, vp]
     lib.oracle_flux_unpack.restype = cint
+    lib.oracle_fields_copy.argtypes = [ctypes.POINTER(vp), cint, i64, i64, i64, i64,
+                                       ctypes.POINTER(vp)]
+    lib.oracle_fields_copy.restype = cint
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = cint
     _lib = lib
@@ -235,6 +238,27 @@ def flux_unpack(sweep_flux: np.ndarray, nv: int, extents, direction: int) -> np.
     if rc != 0:
         raise ValueError("bad direction")
     return out
+
+
+def fields_copy(fields, extents, ghost: int):
+    """The conservative-variable copy (MFC pull request #2087, "Changes",
+    s_compute_rhs): a new array per field holding its whole stored box."""
+    n1, n2, n3 = (int(x) for x in extents)
+    nst = int(np.prod(stored_extents(extents, ghost)))
+    src = [np.ascontiguousarray(f, dtype=np.float64).reshape(-1) for f in fields]
+    if any(a.size != nst for a in src):
+        raise ValueError("field size mismatch")
+    dst = [np.empty(nst, dtype=np.float64) for _ in src]
+    st = (ctypes.c_void_p * max(1, len(src)))(*[_ptr(a) for a in src])
+    dt = (ctypes.c_void_p * max(1, len(dst)))(*[_ptr(a) for a in dst])
+    _load().oracle_fields_copy(st, len(src), n1, n2, n3, int(ghost), dt)
+    return dst
+
+
+def weno_pack_copy(fields, extents, ghost: int, direction: int):
+    """The pack fused with the conservative-variable copy: (packed, copies),
+    the two results of one pass over the fields."""
+    return weno_pack(fields, extents, ghost, direction), fields_copy(fields, extents, ghost)
 
 
 def multivar_sweep_2d(fields, fluxes_x, fluxes_y, inv_dx, inv_dy, nv, extents, ghost):

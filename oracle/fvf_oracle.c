@@ -20,7 +20,8 @@
  *       per-variable GPU kernels": "Changes" (the WENO input pack
  *       v_rs_weno(j,k,l,i) = v_vf(i)%sf(j,k,l) and the x/y/z flux
  *       differences in s_compute_advection_source_term, inverse spacing taken
- *       once per cell; s_finalize_riemann_solver, the directional flux copies).
+ *       once per cell; s_finalize_riemann_solver, the directional flux copies;
+ *       s_compute_rhs, the conservative-variable copy).
  *
  * Conventions (0-based C indices; the pages use 1-based Fortran):
  *  - 2D field u(i,j), 0 <= i < nx, 0 <= j < ny, stored at u[i + nx*j].
@@ -313,6 +314,21 @@ int oracle_flux_unpack(const double *in, int nv, int64_t n1, int64_t n2, int64_t
             }
         }
     }
+    return 0;
+}
+
+/*
+ * The conservative-variable copy of [M] "Changes" (s_compute_rhs): field i
+ * copied element by element, the whole stored box (ghost cells included),
+ * into dst_i.  Returns 0.
+ */
+int oracle_fields_copy(const double *const *src, int nv, int64_t n1, int64_t n2, int64_t n3,
+                       int64_t g, double *const *dst)
+{
+    const int64_t total = stored_extent(n1, g) * stored_extent(n2, g) * stored_extent(n3, g);
+    for (int i = 0; i < nv; ++i)
+        for (int64_t e = 0; e < total; ++e)
+            dst[i][e] = src[i][e];
     return 0;
 }
 

@@ -160,3 +160,33 @@ def test_binding_rejects_cpu_tensors(lib):
 
 def test_launch_count_starts_at_zero_without_launches(lib):
     assert api.launch_count() >= 0
+
+
+def test_copy_validation(lib):
+    c, pc = lib.fields_copy, lib.weno_pack_copy
+    vp = ctypes.c_void_p
+    src = (vp * 2)(4096, 8192)
+    dst = (vp * 2)(16384, 32768)
+    ext = E3(3, 4, 5)
+    assert c(src, 2, None, 1, dst, None) == C["FVF_ERR_NULL"]
+    assert c(src, 65, ext, 1, dst, None) == C["FVF_ERR_NV"]
+    assert c(src, 2, ext, -1, dst, None) == C["FVF_ERR_SIZE"]
+    assert c(src, 2, E3(3, -4, 5), 1, dst, None) == C["FVF_ERR_SIZE"]
+    assert c(None, 0, ext, 1, None, None) == C["FVF_OK"]
+    assert c(None, 2, E3(3, 0, 5), 1, None, None) == C["FVF_OK"]
+    assert c(None, 2, ext, 1, dst, None) == C["FVF_ERR_NULL"]
+    assert c(src, 2, ext, 1, None, None) == C["FVF_ERR_NULL"]
+    assert c(src, 2, ext, 1, (vp * 2)(16384, None), None) == C["FVF_ERR_NULL"]
+    assert c(src, 2, ext, 1, (vp * 2)(16384, 32772), None) == C["FVF_ERR_ALIGN"]
+    assert c((vp * 2)(4100, 8192), 2, ext, 1, dst, None) == C["FVF_ERR_ALIGN"]
+    assert c(src, 2, ext, 1, dst, None) == C["FVF_ERR_NOT_DEVICE"]
+    assert pc(src, 2, None, 1, 0, 65536, dst, None) == C["FVF_ERR_NULL"]
+    assert pc(src, 2, ext, 1, 3, 65536, dst, None) == C["FVF_ERR_DIR"]
+    assert pc(src, 65, ext, 1, 0, 65536, dst, None) == C["FVF_ERR_NV"]
+    assert pc(src, 2, ext, -2, 0, 65536, dst, None) == C["FVF_ERR_SIZE"]
+    assert pc(None, 0, ext, 1, 0, None, None, None) == C["FVF_OK"]
+    assert pc(src, 2, ext, 1, 0, None, dst, None) == C["FVF_ERR_NULL"]
+    assert pc(src, 2, ext, 1, 0, 65536, None, None) == C["FVF_ERR_NULL"]
+    assert pc(src, 2, ext, 1, 0, 65540, dst, None) == C["FVF_ERR_ALIGN"]
+    assert pc(src, 2, ext, 1, 1, 65536, (vp * 2)(16385, 32768), None) == C["FVF_ERR_ALIGN"]
+    assert pc(src, 2, ext, 1, 2, 65536, dst, None) == C["FVF_ERR_NOT_DEVICE"]

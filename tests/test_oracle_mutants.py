@@ -3,9 +3,9 @@
 Each case copies the oracle's C source, plants one mistake in the copy
 (a reordered sum, a fused multiply-add, a flipped sign, a wrong neighbour
 index, a missing edge write, a swapped ping-pong, a wrong ghost offset, a
-swapped face), builds it with the oracle's flags, swaps it in for the real
-oracle library and runs the named pin, which must fail.  Everything runs on
-the CPU; nothing here touches the GPU path.
+swapped face, a copy of the wrong variable), builds it with the oracle's
+flags, swaps it in for the real oracle library and runs the named pin, which
+must fail.  Everything runs on the CPU; nothing here touches the GPU path.
 """
 from __future__ import annotations
 
@@ -40,7 +40,7 @@ def _mutant(tmp_path, old: str, new: str, count: int = 1):
     lib = ctypes.CDLL(str(so))
     for name in ("oracle_diffuse2d_f64", "oracle_diffuse2d_f32", "oracle_weno_pack",
                  "oracle_advect_rhs", "oracle_advect_rhs_add", "oracle_flux_unpack",
-                 "oracle_max_threads"):
+                 "oracle_fields_copy", "oracle_max_threads"):
         getattr(lib, name).argtypes = getattr(real, name).argtypes
         getattr(lib, name).restype = getattr(real, name).restype
     oracle._lib = lib
@@ -98,6 +98,13 @@ MUTANTS = [
      "src = k + F2 * (j + F1 * (l + F3 * (int64_t)i));",
      "src = j + F1 * (k + F2 * (l + F3 * (int64_t)i));",
      1, lambda: P.test_flux_unpack_coordinate_tags(1)),
+    ("copy-wrong-variable",
+     "dst[i][e] = src[i][e];", "dst[i][e] = src[0][e];",
+     1, lambda: P.test_fields_copy_is_bitwise_identity()),
+    ("copy-last-element-dropped",
+     "for (int64_t e = 0; e < total; ++e)\n            dst[i][e]",
+     "for (int64_t e = 0; e < total - 1; ++e)\n            dst[i][e]",
+     1, lambda: P.test_fields_copy_is_bitwise_identity()),
 ]
 
 

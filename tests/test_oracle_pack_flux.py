@@ -326,3 +326,30 @@ def test_flux_unpack_inverts_the_pack_permutation(direction):
     sweep = oracle.weno_pack(fields, fe, 0, direction)
     back = oracle.flux_unpack(sweep, nv, extents, direction)
     assert np.array_equal(back.view(np.uint64), phys.view(np.uint64))
+
+
+# ---------------------------------------------------------------------------
+# Conservative-variable copy (and the pack fused with it)
+# ---------------------------------------------------------------------------
+
+def test_fields_copy_is_bitwise_identity():
+    """Every element of every stored box, ghosts included, is copied bit for
+    bit (NaN payloads, signed zeros and subnormals too)."""
+    extents, g, nv = (5, 4, 3), 2, 3
+    n = int(np.prod(inputs.stored_extents(extents, g)))
+    fields = [inputs.random_bits(31, i, n).view(np.float64) for i in range(nv)]
+    fields[0][:4] = np.array([0x7FF4000000000001, 0x8000000000000000, 1, 0x7FF0000000000000],
+                             dtype=np.uint64).view(np.float64)
+    copies = oracle.fields_copy(fields, extents, g)
+    for f, c in zip(fields, copies):
+        assert c.size == n
+        assert np.array_equal(f.view(np.uint64), c.view(np.uint64))
+
+
+def test_pack_copy_is_pack_and_copy():
+    extents, g, nv = (6, 5, 4), 2, 2
+    fields = inputs.normal_fields(5, nv, extents, g)
+    for direction in range(3):
+        packed, copies = oracle.weno_pack_copy(fields, extents, g, direction)
+        assert np.array_equal(packed, _numpy_pack(fields, extents, g, direction))
+        assert all(np.array_equal(a, b) for a, b in zip(copies, fields))
