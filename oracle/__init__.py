@@ -76,6 +76,9 @@ def _load():
     lib.oracle_fields_copy.argtypes = [ctypes.POINTER(vp), cint, i64, i64, i64, i64,
                                        ctypes.POINTER(vp)]
     lib.oracle_fields_copy.restype = cint
+    lib.oracle_rk_axpby.argtypes = [vp, vp, vp, i64, ctypes.c_double, ctypes.c_double,
+                                    ctypes.c_double, vp]
+    lib.oracle_rk_axpby.restype = cint
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = cint
     _lib = lib
@@ -259,6 +262,44 @@ def weno_pack_copy(fields, extents, ghost: int, direction: int):
     """The pack fused with the conservative-variable copy: (packed, copies),
     the two results of one pass over the fields."""
     return weno_pack(fields, extents, ghost, direction), fields_copy(fields, extents, ghost)
+
+
+# Shu-Osher SSPRK3 stage coefficients (a, b) of out = a*u^n + b*(u + dt*rhs).
+SSPRK3_STAGES = ((0.0, 1.0), (0.75, 0.25), (1.0 / 3.0, 2.0 / 3.0))
+
+
+def rk_axpby(u0, u, rhs, a: float, b: float, dt: float):
+    """One SSPRK3 stage update out = a*u0 + b*(u + dt*rhs) (Mallard
+    documentation, "Design: single-GPU performance and parallel scaling",
+    "Baseline (main)": axpby per stage)."""
+    u0 = np.ascontiguousarray(u0, dtype=np.float64).reshape(-1)
+    u = np.ascontiguousarray(u, dtype=np.float64).reshape(-1)
+    rhs = np.ascontiguousarray(rhs, dtype=np.float64).reshape(-1)
+    if not (u0.size == u.size == rhs.size):
+        raise ValueError("size mismatch")
+    out = np.empty_like(u)
+    _load().oracle_rk_axpby(_ptr(u0), _ptr(u), _ptr(rhs), u.size, float(a), float(b), float(dt),
+                            _ptr(out))
+    return out
+
+
+def fv_rhs(fluxes, inv_ds, nv: int, extents):
+    """The finite-volume right-hand side from face fluxes: the x difference
+    assigned, then the y and z differences added in that order (a direction
+    whose flux is None is skipped; x must be given)."""
+    if fluxes[0] is None:
+        raise ValueError("the x flux is required")
+    rhs = advect_rhs(fluxes[0], inv_ds[0], nv, extents, 0)
+    for d in (1, 2):
+        if fluxes[d] is not None:
+            rhs = advect_rhs_add(fluxes[d], inv_ds[d], nv, extents, d, rhs)
+    return rhs
+
+
+def ssprk3_stage(u0, u, fluxes, inv_ds, nv: int, extents, a: float, b: float, dt: float):
+    """The stage update fused with the flux difference: rhs from the face
+    fluxes (fv_rhs), then out = a*u0 + b*(u + dt*rhs)."""
+    return rk_axpby(u0, u, fv_rhs(fluxes, inv_ds, nv, extents), a, b, dt)
 
 
 def multivar_sweep_2d(fields, fluxes_x, fluxes_y, inv_dx, inv_dy, nv, extents, ghost):

@@ -22,6 +22,13 @@
  *       differences in s_compute_advection_source_term, inverse spacing taken
  *       once per cell; s_finalize_riemann_solver, the directional flux copies;
  *       s_compute_rhs, the conservative-variable copy).
+ *  [D]  Mallard documentation, "Design: single-GPU performance and parallel
+ *       scaling": "Hardware and method" (a step is SSPRK3, three stages) and
+ *       "Baseline (main)" (per stage, after the flux sums, the rhs and axpby
+ *       kernels).  The stage coefficients are those of the three-stage,
+ *       third-order strong-stability-preserving Runge-Kutta scheme of Shu and
+ *       Osher (J. Comput. Phys. 77, 1988): u1 = u^n + dt L(u^n),
+ *       u2 = 3/4 u^n + 1/4 (u1 + dt L(u1)), u^{n+1} = 1/3 u^n + 2/3 (u2 + dt L(u2)).
  *
  * Conventions (0-based C indices; the pages use 1-based Fortran):
  *  - 2D field u(i,j), 0 <= i < nx, 0 <= j < ny, stored at u[i + nx*j].
@@ -329,6 +336,27 @@ int oracle_fields_copy(const double *const *src, int nv, int64_t n1, int64_t n2,
     for (int i = 0; i < nv; ++i)
         for (int64_t e = 0; e < total; ++e)
             dst[i][e] = src[i][e];
+    return 0;
+}
+
+/*
+ * One SSPRK3 stage update ([D] "Baseline (main)", axpby per stage) on
+ * `count` cell-variable entries:
+ *     out = a*u0 + b*(u + dt*rhs)
+ * evaluated as t = u + dt*rhs, then a*u0 and b*t, then their sum, every
+ * operation rounded separately.  (a, b) is (0, 1), (3/4, 1/4) or (1/3, 2/3)
+ * for the three stages, with u0 = u^n and u the previous stage.  out may be
+ * u or u0 itself: each entry is read before it is written.  Returns 0.
+ */
+int oracle_rk_axpby(const double *u0, const double *u, const double *rhs, int64_t count,
+                    double a, double b, double dt, double *out)
+{
+    for (int64_t e = 0; e < count; ++e) {
+        const double t = u[e] + dt * rhs[e];
+        const double p = a * u0[e];
+        const double q = b * t;
+        out[e] = p + q;
+    }
     return 0;
 }
 

@@ -3,9 +3,9 @@
 Each case copies the oracle's C source, plants one mistake in the copy
 (a reordered sum, a fused multiply-add, a flipped sign, a wrong neighbour
 index, a missing edge write, a swapped ping-pong, a wrong ghost offset, a
-swapped face, a copy of the wrong variable), builds it with the oracle's
-flags, swaps it in for the real oracle library and runs the named pin, which
-must fail.  Everything runs on the CPU; nothing here touches the GPU path.
+swapped face, a copy of the wrong variable, swapped stage coefficients),
+builds it with the oracle's flags, swaps it in for the real oracle library
+and runs the named pin, which must fail.  Everything runs on the CPU; nothing here touches the GPU path.
 """
 from __future__ import annotations
 
@@ -21,6 +21,7 @@ import pytest
 import oracle
 import tests.test_oracle_diffusion as D
 import tests.test_oracle_pack_flux as P
+import tests.test_oracle_rk as R
 
 SRC = Path(oracle.__file__).parent / "fvf_oracle.c"
 
@@ -40,7 +41,7 @@ def _mutant(tmp_path, old: str, new: str, count: int = 1):
     lib = ctypes.CDLL(str(so))
     for name in ("oracle_diffuse2d_f64", "oracle_diffuse2d_f32", "oracle_weno_pack",
                  "oracle_advect_rhs", "oracle_advect_rhs_add", "oracle_flux_unpack",
-                 "oracle_fields_copy", "oracle_max_threads"):
+                 "oracle_fields_copy", "oracle_rk_axpby", "oracle_max_threads"):
         getattr(lib, name).argtypes = getattr(real, name).argtypes
         getattr(lib, name).restype = getattr(real, name).restype
     oracle._lib = lib
@@ -105,6 +106,16 @@ MUTANTS = [
      "for (int64_t e = 0; e < total; ++e)\n            dst[i][e]",
      "for (int64_t e = 0; e < total - 1; ++e)\n            dst[i][e]",
      1, lambda: P.test_fields_copy_is_bitwise_identity()),
+    ("stage-coefficients-swapped",
+     "const double p = a * u0[e];\n        const double q = b * t;",
+     "const double p = b * u0[e];\n        const double q = a * t;",
+     1, lambda: R.test_ssprk3_closed_form_on_linear_equation(-0.5)),
+    ("stage-from-un-not-u",
+     "const double t = u[e] + dt * rhs[e];", "const double t = u0[e] + dt * rhs[e];",
+     1, lambda: R.test_ssprk3_closed_form_on_linear_equation(-0.5)),
+    ("stage-dt-dropped",
+     "const double t = u[e] + dt * rhs[e];", "const double t = u[e] + rhs[e];",
+     1, lambda: R.test_axpby_worked_values(1.0, 2.0, 4.0, 0.5, 0.75, 0.25, 1.75)),
 ]
 
 
