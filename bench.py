@@ -491,8 +491,11 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     the accumulating flux difference and the directional flux copy back to
     the physical frame on the 8 x 201^3 flux workload's buffers, the
     conservative-variable copy alone and fused with the pack on the 8 x 207^3
-    pack workload's fields, and the latency of the 64 x 64 FP64 diffusion
-    case."""
+    pack workload's fields, the SSPRK3 stage update (fused with the flux
+    difference, alone, and unfused) on the flux workload, and the latency of
+    the 64 x 64 FP64 diffusion case.  Stage rows count the bytes of the fused
+    form (the unfused row's extra rhs traffic is its cost) and 13 FP64
+    operations per element (5 for the update alone)."""
     from finite_volume_field_gb300 import api
     peaks, _ = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
@@ -552,6 +555,30 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
             api.fields_copy(sw.pack_fields, PACK_NV, PACK_EXT, PACK_G, copies, stream)
         record(f"pack_then_copy_{ax}", unfused, 8 * (2 * nst + npk), nst)
     del copies
+    # SSPRK3 stage update on the flux workload (8 x 201^3, x/y/z faces):
+    # fused with the flux difference, alone (axpby on a given rhs), and the
+    # unfused sequence (flux difference x, +y, +z into rhs, then axpby)
+    u0 = torch.randn(cells, dtype=torch.float64, device=sw.dev)
+    u = torch.randn(cells, dtype=torch.float64, device=sw.dev)
+    uo = torch.empty_like(u)
+    rhs = sw.rhs_out[0]
+    fl, w = sw.rhs_flux, sw.rhs_invd
+    face_bytes = 8 * sum(f.numel() for f in fl)
+    a, b, dt = 0.75, 0.25, 1e-4
+    record("ssprk3_stage_xyz",
+           lambda: api.ssprk3_stage(u0, u, fl, w, RHS_NV, RHS_EXT, a, b, dt, uo, stream),
+           face_bytes + 24 * cells, cells, 13)
+    record("ssprk3_axpby",
+           lambda: api.ssprk3_axpby(u0, u, rhs, RHS_NV, RHS_EXT, a, b, dt, uo, stream),
+           32 * cells, cells, 5)
+
+    def stage_unfused():
+        api.advect_rhs(fl[0], w[0], RHS_NV, RHS_EXT, 0, rhs, stream)
+        api.advect_rhs_add(fl[1], w[1], RHS_NV, RHS_EXT, 1, rhs, stream)
+        api.advect_rhs_add(fl[2], w[2], RHS_NV, RHS_EXT, 2, rhs, stream)
+        api.ssprk3_axpby(u0, u, rhs, RHS_NV, RHS_EXT, a, b, dt, uo, stream)
+    record("ssprk3_stage_unfused_xyz", stage_unfused, face_bytes + 24 * cells, cells, 13)
+    del u0, u, uo
     # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
     # (both states live in shared memory), reported per call and per step
     u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)
@@ -758,7 +785,8 @@ def run_ncu_case():
     diffusion 8192^2 FP64 then FP32, pack x/y/z on 8 fields of
     207^3, the conservative-variable copy alone and fused with the pack x/y/z
     on the same fields (at most about 1.7 GB), flux difference x/y/z on
-    8 x 201^3.  FP64 runs 2 single steps, FP32 17 steps (two
+    8 x 201^3, the SSPRK3 stage fused with the x/y/z flux difference on
+    8 x 201^3 (about 3.1 GB).  FP64 runs 2 single steps, FP32 17 steps (two
     8-step shared-memory launches, then one single step).  Device-generated values (the
     kernels' timing does not depend on them)."""
     import torch
@@ -798,6 +826,17 @@ def run_ncu_case():
         api.advect_rhs(F, w, RHS_NV, RHS_EXT, d, r)
         del F, w, r
         free()
+    fl, ws = [], []
+    for d in range(3):
+        fe = list(RHS_EXT)
+        fe[d] += 1
+        fl.append(torch.randn(_prod(fe) * RHS_NV, dtype=torch.float64, device="cuda"))
+        ws.append(torch.rand(RHS_EXT[d], dtype=torch.float64, device="cuda") + 0.5)
+    u0 = torch.randn(_prod(RHS_EXT) * RHS_NV, dtype=torch.float64, device="cuda")
+    u = torch.randn_like(u0)
+    api.ssprk3_stage(u0, u, fl, ws, RHS_NV, RHS_EXT, 0.75, 0.25, 1e-4, u)
+    del fl, ws, u0, u
+    free()
     print("ncu case done", flush=True)
     return 0
 

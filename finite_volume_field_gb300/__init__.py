@@ -1,8 +1,9 @@
 """GB300-native per-cell field sweeps: 2D 5-point diffusion with ping-pong
 buffers, the multi-variable WENO input pack and the finite-volume
 flux-difference source (assigned or accumulated), the directional flux
-copy back to the physical frame and the conservative-variable copy (alone or
-fused with the pack), as sm_103a CUDA kernels behind a C ABI
+copy back to the physical frame, the conservative-variable copy (alone or
+fused with the pack) and the SSPRK3 stage update (alone or fused with the
+flux difference), as sm_103a CUDA kernels behind a C ABI
 (include/fvf.h, libfvf.so).
 
 The public calls are re-exported from ``api``; they load libfvf.so on first
@@ -11,8 +12,9 @@ generators.
 """
 from .api import (FVF_FP32, FVF_FP64, MAX_NV, FvfError, advect_rhs, advect_rhs_add,
                   diffuse2d_step, fields_copy, flux_unpack, last_cuda_error, launch_count, load,
-                  status_string, weno_pack, weno_pack_copy)
+                  ssprk3_axpby, ssprk3_stage, status_string, weno_pack, weno_pack_copy)
 
 __all__ = ["FVF_FP32", "FVF_FP64", "MAX_NV", "FvfError", "advect_rhs", "advect_rhs_add",
            "diffuse2d_step", "fields_copy", "flux_unpack", "last_cuda_error", "launch_count",
-           "load", "status_string", "weno_pack", "weno_pack_copy"]
+           "load", "ssprk3_axpby", "ssprk3_stage", "status_string", "weno_pack",
+           "weno_pack_copy"]

@@ -59,6 +59,12 @@ def load() -> ctypes.CDLL:
     lib.weno_pack_copy.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint, cint, vp,
                                    ctypes.POINTER(vp), vp]
     lib.weno_pack_copy.restype = cint
+    dbl = ctypes.c_double
+    lib.ssprk3_axpby.argtypes = [vp, vp, vp, cint, ctypes.POINTER(i64), dbl, dbl, dbl, vp, vp]
+    lib.ssprk3_axpby.restype = cint
+    lib.ssprk3_stage.argtypes = [vp, vp, ctypes.POINTER(vp), ctypes.POINTER(vp), cint,
+                                 ctypes.POINTER(i64), dbl, dbl, dbl, vp, vp]
+    lib.ssprk3_stage.restype = cint
     lib.fvf_status_string.argtypes = [cint]
     lib.fvf_status_string.restype = ctypes.c_char_p
     lib.fvf_last_cuda_error.argtypes = []
@@ -204,3 +210,32 @@ def weno_pack_copy(fields, nv: int, extents, ghost: int, dir: int, out, copies,
                                int(ghost), int(dir), _addr(out, torch.float64, "out"),
                                _table(copies, nv, "copies"), _stream(stream))
     _check("weno_pack_copy", st)
+
+
+def ssprk3_axpby(u0, u, rhs, nv: int, extents, a: float, b: float, dt: float, out,
+                 stream=None) -> None:
+    """Enqueue one SSPRK3 stage update out = a*u0 + b*(u + dt*rhs)."""
+    import torch
+    f64 = torch.float64
+    st = load().ssprk3_axpby(_addr(u0, f64, "u0"), _addr(u, f64, "u"), _addr(rhs, f64, "rhs"),
+                             int(nv), _extents(extents), float(a), float(b), float(dt),
+                             _addr(out, f64, "out"), _stream(stream))
+    _check("ssprk3_axpby", st)
+
+
+def ssprk3_stage(u0, u, fluxes, inv_ds, nv: int, extents, a: float, b: float, dt: float, out,
+                 stream=None) -> None:
+    """Enqueue the SSPRK3 stage update fused with the flux difference;
+    ``fluxes`` and ``inv_ds`` are three entries each (x, y, z), y and z may be
+    None."""
+    import torch
+    f64 = torch.float64
+    fl = [_addr(f, f64, f"fluxes[{d}]") for d, f in enumerate(list(fluxes)[:3])]
+    w = [_addr(x, f64, f"inv_ds[{d}]") if x is not None else None
+         for d, x in enumerate(list(inv_ds)[:3])]
+    fl += [None] * (3 - len(fl))
+    w += [None] * (3 - len(w))
+    st = load().ssprk3_stage(_addr(u0, f64, "u0"), _addr(u, f64, "u"), (ctypes.c_void_p * 3)(*fl),
+                             (ctypes.c_void_p * 3)(*w), int(nv), _extents(extents), float(a),
+                             float(b), float(dt), _addr(out, f64, "out"), _stream(stream))
+    _check("ssprk3_stage", st)

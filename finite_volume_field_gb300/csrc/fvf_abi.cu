@@ -291,6 +291,97 @@ FVF_API int weno_pack_copy(const double *const *fields, int nv, const int64_t ex
     return cuda_status(e);
 }
 
+// out of a stage update may be u or u0 itself (same start; each element is
+// read before it is written) but must not overlap them otherwise.
+static bool bad_inplace(const double *out, const double *in, uint64_t bytes) {
+    return out != in && overlaps(out, bytes, in, bytes);
+}
+
+// Shared validation and launch of ssprk3_axpby (rhs given, fused false) and
+// ssprk3_stage (fluxes given, fused true).
+static int rk_stage_impl(const double *u0, const double *u, const double *rhs,
+                         const double *const *flux, const double *const *inv_d, int nv,
+                         const int64_t extents[3], double a, double b, double dt, double *out,
+                         bool fused, void *stream) {
+    if (!extents) return FVF_ERR_NULL;
+    if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
+    RkStageArgs A;
+    std::memset(&A, 0, sizeof(A));
+    int64_t t = 0, cells = 0, elems = 0, felems[3] = {0, 0, 0};
+    for (int d = 0; d < 3; ++d) {
+        if (extents[d] < 0) return FVF_ERR_SIZE;
+        A.n[d] = extents[d];
+    }
+    if (!mul_ok(A.n[0], A.n[1], &t) || !mul_ok(t, A.n[2], &cells) || !mul_ok(cells, nv, &elems))
+        return FVF_ERR_SIZE;
+    for (int d = 0; d < 3; ++d) {
+        int64_t F[3] = {A.n[0], A.n[1], A.n[2]}, faces = 0;
+        F[d] += 1;
+        if (!mul_ok(F[0], F[1], &t) || !mul_ok(t, F[2], &faces) || !mul_ok(faces, nv, &felems[d]))
+            return FVF_ERR_SIZE;
+    }
+    if (!std::isfinite(a) || !std::isfinite(b) || !std::isfinite(dt)) return FVF_ERR_ALPHA;
+    if (elems == 0) return FVF_OK;
+    if (!u0 || !u || !out) return FVF_ERR_NULL;
+    if (fused) {
+        if (!flux || !inv_d || !flux[0] || !inv_d[0]) return FVF_ERR_NULL;
+        for (int d = 0; d < 3; ++d) {
+            if (flux[d] && !inv_d[d]) return FVF_ERR_NULL;
+            A.f[d] = flux[d];
+            A.w[d] = flux[d] ? inv_d[d] : nullptr;
+        }
+    } else {
+        if (!rhs) return FVF_ERR_NULL;
+        A.f[0] = rhs;
+    }
+    const double *ptrs[8] = {u0, u, out, A.f[0], A.f[1], A.f[2], A.w[0], A.w[1]};
+    for (const double *p : ptrs)
+        if ((uintptr_t)p % 8) return FVF_ERR_ALIGN;
+    if ((uintptr_t)A.w[2] % 8) return FVF_ERR_ALIGN;
+    const uint64_t cbytes = (uint64_t)elems * 8;
+    uint64_t fbytes[3], wbytes[3];
+    for (int d = 0; d < 3; ++d) {
+        fbytes[d] = fused ? (uint64_t)felems[d] * 8 : (d == 0 ? cbytes : 0);
+        wbytes[d] = (uint64_t)A.n[d] * 8;
+    }
+    int st = check_device_array(u0, cbytes);
+    if (st == FVF_OK) st = check_device_array(u, cbytes);
+    if (st == FVF_OK) st = check_device_array(out, cbytes);
+    for (int d = 0; d < 3 && st == FVF_OK; ++d) {
+        if (A.f[d]) st = check_device_array(A.f[d], fbytes[d]);
+        if (st == FVF_OK && A.w[d]) st = check_device_array(A.w[d], wbytes[d]);
+    }
+    if (st != FVF_OK) return st;
+    if (bad_inplace(out, u, cbytes) || bad_inplace(out, u0, cbytes)) return FVF_ERR_ALIAS;
+    for (int d = 0; d < 3; ++d) {
+        if (A.f[d] && overlaps(out, cbytes, A.f[d], fbytes[d])) return FVF_ERR_ALIAS;
+        if (A.w[d] && overlaps(out, cbytes, A.w[d], wbytes[d])) return FVF_ERR_ALIAS;
+    }
+    A.u0 = u0;
+    A.u = u;
+    A.out = out;
+    A.nv = nv;
+    A.a = a;
+    A.b = b;
+    A.dt = dt;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_rk_stage(A, fused, (cudaStream_t)stream, &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
+FVF_API int ssprk3_axpby(const double *u0, const double *u, const double *rhs, int nv,
+                         const int64_t extents[3], double a, double b, double dt, double *out,
+                         void *stream) {
+    return rk_stage_impl(u0, u, rhs, nullptr, nullptr, nv, extents, a, b, dt, out, false, stream);
+}
+
+FVF_API int ssprk3_stage(const double *u0, const double *u, const double *const flux[3],
+                         const double *const inv_d[3], int nv, const int64_t extents[3], double a,
+                         double b, double dt, double *out, void *stream) {
+    return rk_stage_impl(u0, u, nullptr, flux, inv_d, nv, extents, a, b, dt, out, true, stream);
+}
+
 static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
                            const int64_t extents[3], int dir, bool accumulate, double *rhs,
                            void *stream) {
@@ -385,7 +476,7 @@ FVF_API const char *fvf_status_string(int status) {
         case FVF_ERR_DIR: return "invalid direction";
         case FVF_ERR_NV: return "invalid number of variables";
         case FVF_ERR_ALIAS: return "output overlaps an input";
-        case FVF_ERR_ALPHA: return "alpha is not finite";
+        case FVF_ERR_ALPHA: return "alpha or a stage coefficient is not finite";
         case FVF_ERR_ALIGN: return "misaligned pointer";
         case FVF_ERR_NOT_DEVICE: return "pointer is not device memory of the current device";
         case FVF_ERR_RANGE: return "array runs past the end of its allocation";

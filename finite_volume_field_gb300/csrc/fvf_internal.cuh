@@ -29,6 +29,21 @@ struct Box {
     int64_t g[3];
 };
 
+// Arguments of the SSPRK3 stage update, alone (f[0] = rhs) or fused with the
+// flux difference (f[0..2] = x/y/z face fluxes, y and z possibly NULL;
+// w[0..2] = inverse spacings of the present directions).  Cell arrays have
+// n[0]*n[1]*n[2] cells per variable, j fastest, the variable slowest.
+struct RkStageArgs {
+    const double *u0;
+    const double *u;
+    const double *f[3];
+    const double *w[3];
+    double *out;
+    int nv;
+    int64_t n[3];
+    double a, b, dt;
+};
+
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
@@ -53,6 +68,9 @@ cudaError_t launch_fields_copy(const FieldTable &fields, int nv, int64_t stored,
 cudaError_t launch_weno_pack_copy(const FieldTable &fields, int nv, const Box &box, int dir,
                                   double *out, const CopyTable &copies, cudaStream_t stream,
                                   uint64_t *launches);
+
+cudaError_t launch_rk_stage(const RkStageArgs &args, bool fused, cudaStream_t stream,
+                            uint64_t *launches);
 
 cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
                               const int64_t n[3], int dir, bool accumulate, double *rhs,

@@ -1,0 +1,163 @@
+// rk_stage.cu -- SSPRK3 stage update for sm_103a, alone (given rhs) and
+// fused with the finite-volume flux difference.
+//
+// Operation (Mallard documentation, "Design: single-GPU performance and
+// parallel scaling": "Hardware and method", a step is three SSPRK3 stages;
+// "Baseline (main)", the per-stage rhs and axpby kernels), per cell c and
+// variable i:
+//     rhs = inv_x(j)*(Fx(j-1) - Fx(j)) [+ inv_y(k)*(Fy(k-1) - Fy(k))]
+//                                      [+ inv_z(l)*(Fz(l-1) - Fz(l))]
+//     t   = u + dt*rhs
+//     out = a*u0 + b*t
+// every operation rounded to nearest even in this order (the flux terms as
+// in the x/y/z flux differences of MFlowCode/MFC pull request #2087,
+// "Changes", s_compute_advection_source_term).  The fused kernel keeps rhs
+// in registers: per element it reads u0, u and the faces and writes out, in
+// place of the flux difference writing rhs and the update reading it back.
+//
+// Mapping: one thread per cell (j, k) of a plane l, the (j, k) pairs
+// flattened so that every lane of every warp has a cell (the rows of 201
+// cells would leave a fifth of the lanes of a row-per-block mapping idle, and
+// the kernel is bound by the FP64 unit, which charges idle lanes).  The
+// variables are processed in chunks of kChunk inside the thread: the chunk's
+// loads are all issued before its stores, since out may be u or u0 itself
+// and the compiler must not assume that it is not.
+//
+// FP64 throughput.  The fused 3D update is 13 FP64 operations per element
+// against 48 bytes of HBM traffic, far above GB300's FP64-to-bandwidth
+// ratio, so the FP64 unit bounds it; this kernel issues FP64 operations at
+// the unit's measured rate.  FVF_RK_EMU selects additions that run as exact
+// integer-pipe binary64 additions (fp64_emu.cuh) instead, in parallel with
+// the FP64 unit: bit 1 the y term, 2 the z term, 4 u + dt*rhs, 8 the final
+// sum, 16/32/64 the x/y/z face differences.  Every choice measured slower
+// than none (the added latency of the integer chains in front of the
+// dependent FP64 operations costs more than the FP64 issue slots it frees),
+// so the default is 0.  FVF_RK_CHUNK is the number of variables per load
+// batch (2 measured best of 2, 4 and 8).
+#include "fp64_emu.cuh"
+#include "fvf_internal.cuh"
+
+#ifndef FVF_RK_EMU
+#define FVF_RK_EMU 0
+#endif
+#ifndef FVF_RK_CHUNK
+#define FVF_RK_CHUNK 2
+#endif
+
+namespace fvf {
+namespace {
+
+constexpr int kChunk = FVF_RK_CHUNK;
+constexpr int kThreads = 256;
+
+template <int BIT>
+__device__ __forceinline__ double add_rn(double x, double y) {
+    if (FVF_RK_EMU & BIT) return emu::add(x, y);
+    return __dadd_rn(x, y);
+}
+
+template <int BIT>
+__device__ __forceinline__ double sub_rn(double x, double y) {
+    if (FVF_RK_EMU & BIT) return emu::add(x, emu::from_bits(emu::bits(y) ^ emu::kSign));
+    return __dsub_rn(x, y);
+}
+
+template <bool FUSED, bool FY, bool FZ, typename Idx>
+__global__ void __launch_bounds__(kThreads)
+rk_stage_kernel(RkStageArgs A) {
+    const Idx n1 = (Idx)A.n[0], n2 = (Idx)A.n[1];
+    const Idx plane_jk = n1 * n2;
+    const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
+    if (jk >= plane_jk) return;
+    const Idx k = jk / n1, j = jk - k * n1;
+    const int64_t n3 = A.n[2];
+    const int64_t cplane = (int64_t)plane_jk * n3;  // cells per variable
+    const int64_t fxp = (int64_t)(n1 + 1) * n2 * n3, fyp = (int64_t)n1 * (n2 + 1) * n3,
+                  fzp = (int64_t)plane_jk * (n3 + 1);
+    const double wx = FUSED ? __ldg(A.w[0] + j) : 0.0;
+    const double wy = FY ? __ldg(A.w[1] + k) : 0.0;
+    for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
+        const double wz = FZ ? __ldg(A.w[2] + l) : 0.0;
+        const int64_t c = (int64_t)jk + (int64_t)plane_jk * l;
+        const int64_t xlo = (int64_t)j + (int64_t)(n1 + 1) * ((int64_t)k + (int64_t)n2 * l);
+        const int64_t ylo = (int64_t)j + (int64_t)n1 * ((int64_t)k + (int64_t)(n2 + 1) * l);
+        const int64_t zlo = c;
+        for (int i0 = 0; i0 < A.nv; i0 += kChunk) {
+            double u0v[kChunk], uv[kChunk], r[kChunk];
+            double xl[kChunk], xh[kChunk], yl[kChunk], yh[kChunk], zl[kChunk], zh[kChunk];
+#pragma unroll
+            for (int q = 0; q < kChunk; ++q) {
+                if (i0 + q < A.nv) {
+                    const int64_t iv = i0 + q;
+                    u0v[q] = A.u0[c + iv * cplane];
+                    uv[q] = A.u[c + iv * cplane];
+                    if (FUSED) {
+                        xl[q] = __ldg(A.f[0] + xlo + iv * fxp);
+                        xh[q] = __ldg(A.f[0] + xlo + iv * fxp + 1);
+                    } else {
+                        r[q] = __ldg(A.f[0] + c + iv * cplane);
+                    }
+                    if (FY) {
+                        yl[q] = __ldg(A.f[1] + ylo + iv * fyp);
+                        yh[q] = __ldg(A.f[1] + ylo + iv * fyp + n1);
+                    }
+                    if (FZ) {
+                        zl[q] = __ldg(A.f[2] + zlo + iv * fzp);
+                        zh[q] = __ldg(A.f[2] + zlo + iv * fzp + plane_jk);
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < kChunk; ++q) {
+                if (i0 + q < A.nv) {
+                    double rr;
+                    if (FUSED) {
+                        rr = __dmul_rn(wx, sub_rn<16>(xl[q], xh[q]));
+                        if (FY) rr = add_rn<1>(rr, __dmul_rn(wy, sub_rn<32>(yl[q], yh[q])));
+                        if (FZ) rr = add_rn<2>(rr, __dmul_rn(wz, sub_rn<64>(zl[q], zh[q])));
+                    } else {
+                        rr = r[q];
+                    }
+                    const double t = add_rn<4>(uv[q], __dmul_rn(A.dt, rr));
+                    A.out[c + (int64_t)(i0 + q) * cplane] =
+                        add_rn<8>(__dmul_rn(A.a, u0v[q]), __dmul_rn(A.b, t));
+                }
+            }
+        }
+    }
+}
+
+template <bool FUSED, bool FY, bool FZ>
+cudaError_t launch_typed(const RkStageArgs &A, cudaStream_t stream) {
+    const int64_t plane = A.n[0] * A.n[1];
+    const int64_t gx = (plane + kThreads - 1) / kThreads;
+    if (gx > 0x7fffffff) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)gx, (unsigned)(A.n[2] < 65535 ? A.n[2] : 65535));
+    // 32-bit (j, k) arithmetic while the plane index and n1 + 1 fit
+    if (plane + A.n[0] + kThreads < ((int64_t)1 << 31))
+        rk_stage_kernel<FUSED, FY, FZ, uint32_t><<<grid, kThreads, 0, stream>>>(A);
+    else
+        rk_stage_kernel<FUSED, FY, FZ, int64_t><<<grid, kThreads, 0, stream>>>(A);
+    return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t launch_rk_stage(const RkStageArgs &A, bool fused, cudaStream_t stream,
+                            uint64_t *launches) {
+    cudaError_t e;
+    if (!fused) {
+        e = launch_typed<false, false, false>(A, stream);
+    } else {
+        const bool fy = A.f[1] != nullptr, fz = A.f[2] != nullptr;
+        if (fy && fz) e = launch_typed<true, true, true>(A, stream);
+        else if (fy) e = launch_typed<true, true, false>(A, stream);
+        else if (fz) e = launch_typed<true, false, true>(A, stream);
+        else e = launch_typed<true, false, false>(A, stream);
+    }
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    return cudaGetLastError();
+}
+
+}  // namespace fvf

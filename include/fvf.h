@@ -3,7 +3,8 @@
  * sweeps: the explicit 2D 5-point diffusion step with ping-pong buffers, the
  * multi-variable WENO input pack, the finite-volume flux-difference source
  * (assigned or accumulated), the directional flux copy back to the physical
- * frame and the conservative-variable copy (alone or fused with the pack).
+ * frame, the conservative-variable copy (alone or fused with the pack) and
+ * the SSPRK3 stage update (alone or fused with the flux difference).
  *
  * Sources of the operations (pages, by title and section):
  *   [Q] Qiita, "Fortran 2018でGPUを高速化する Part 3" ("Fortran 2018 GPU
@@ -17,6 +18,10 @@
  *       s_compute_rhs) and "Why
  *       this is faster" (one thread per spatial cell, variables looped inside
  *       the thread).
+ *   [D] Mallard documentation, "Design: single-GPU performance and parallel
+ *       scaling": "Hardware and method" (a time step is three SSPRK3 stages)
+ *       and "Baseline (main)" (per stage, the rhs and axpby kernels).  The
+ *       stage coefficients are Shu and Osher's (J. Comput. Phys. 77, 1988).
  *
  * Conventions common to every entry point
  *   - All array pointers are DEVICE pointers owned by the caller (for
@@ -57,7 +62,7 @@ extern "C" {
 #define FVF_ERR_DIR          4  /* dir is not 0, 1 or 2                           */
 #define FVF_ERR_NV           5  /* nv outside 0..FVF_MAX_NV                       */
 #define FVF_ERR_ALIAS        6  /* an output overlaps an input or the other buffer */
-#define FVF_ERR_ALPHA        7  /* alpha is not finite                            */
+#define FVF_ERR_ALPHA        7  /* alpha or a stage coefficient is not finite     */
 #define FVF_ERR_ALIGN        8  /* a pointer is not aligned to its element size   */
 #define FVF_ERR_NOT_DEVICE   9  /* a pointer is not device memory of this device  */
 #define FVF_ERR_RANGE       10  /* an array runs past the end of its allocation   */
@@ -204,6 +209,50 @@ int fields_copy(const double *const *fields, int nv, const int64_t extents[3], i
  */
 int weno_pack_copy(const double *const *fields, int nv, const int64_t extents[3], int ghost,
                    int dir, double *out, double *const *copies, void *stream);
+
+/*
+ * ssprk3_axpby -- one SSPRK3 stage update ([D], axpby per stage):
+ *     out(c,i) = a*u0(c,i) + b*(u(c,i) + dt*rhs(c,i))
+ * evaluated as t = u + dt*rhs, then a*u0 and b*t, then their sum, each
+ * operation rounded to nearest even.  The three stages of a step use
+ * (a, b) = (0, 1), (3/4, 1/4), (1/3, 2/3) with u0 = u^n and u the previous
+ * stage (u^n itself in stage 1); 1/3 and 2/3 are the doubles nearest them.
+ * The formula is applied as written for any finite a, b, dt (0*u0 is still
+ * computed when a = 0).
+ *
+ *   u0, u, rhs, out  n1*n2*n3*nv doubles each, cell (j,k,l) of variable i at
+ *                    j + n1*(k + n2*(l + n3*i)) (the rhs layout of
+ *                    advect_rhs).  u0 and u may be the same array.  out may
+ *                    be u or u0 itself (same start address: an in-place
+ *                    stage) but must not overlap them otherwise, nor rhs.
+ *   nv               0..FVF_MAX_NV (0: nothing to do).
+ *   extents          HOST array {n1, n2, n3} of cell counts, each >= 0.
+ *   a, b, dt         finite (else FVF_ERR_ALPHA).
+ */
+int ssprk3_axpby(const double *u0, const double *u, const double *rhs, int nv,
+                 const int64_t extents[3], double a, double b, double dt, double *out,
+                 void *stream);
+
+/*
+ * ssprk3_stage -- the stage update fused with the flux difference: rhs is
+ * formed in registers from the face fluxes, exactly as advect_rhs for x
+ * followed by advect_rhs_add for y and then z would form it,
+ *     rhs = inv_x(j)*(Fx(j-1) - Fx(j))
+ *           [+ inv_y(k)*(Fy(k-1) - Fy(k))] [+ inv_z(l)*(Fz(l-1) - Fz(l))],
+ * then out = a*u0 + b*(u + dt*rhs) as in ssprk3_axpby.  No rhs array is
+ * read or written.
+ *
+ *   flux    HOST array of 3 device pointers: the x, y and z face fluxes in
+ *           the layouts of advect_rhs.  flux[0] is required; flux[1] or
+ *           flux[2] NULL leaves that direction out (a 2D or 1D problem).
+ *   inv_d   HOST array of 3 device pointers: inverse cell widths along x
+ *           (n1 doubles), y (n2) and z (n3); needed where the flux is given.
+ *   Other arguments as for ssprk3_axpby; out must not overlap a flux or an
+ *   inverse-width array.
+ */
+int ssprk3_stage(const double *u0, const double *u, const double *const flux[3],
+                 const double *const inv_d[3], int nv, const int64_t extents[3], double a,
+                 double b, double dt, double *out, void *stream);
 
 /* Static, NUL-terminated name of a status code ("unknown status" if none). */
 const char *fvf_status_string(int status);

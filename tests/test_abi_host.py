@@ -190,3 +190,35 @@ def test_copy_validation(lib):
     assert pc(src, 2, ext, 1, 0, 65540, dst, None) == C["FVF_ERR_ALIGN"]
     assert pc(src, 2, ext, 1, 1, 65536, (vp * 2)(16385, 32768), None) == C["FVF_ERR_ALIGN"]
     assert pc(src, 2, ext, 1, 2, 65536, dst, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_stage_validation(lib):
+    ax, st = lib.ssprk3_axpby, lib.ssprk3_stage
+    vp = ctypes.c_void_p
+    ext = E3(3, 4, 5)
+    fl = (vp * 3)(4096, 8192, None)
+    w = (vp * 3)(16384, 16448, None)
+    assert ax(4096, 4096, 8192, 2, None, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NULL"]
+    assert ax(4096, 4096, 8192, 65, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NV"]
+    assert ax(4096, 4096, 8192, 2, E3(3, -4, 5), 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_SIZE"]
+    assert ax(4096, 4096, 8192, 2, ext, float("nan"), 0.25, 0.1, 65536, None) == C["FVF_ERR_ALPHA"]
+    assert ax(4096, 4096, 8192, 2, ext, 0.75, float("inf"), 0.1, 65536, None) == C["FVF_ERR_ALPHA"]
+    assert ax(4096, 4096, 8192, 2, ext, 0.75, 0.25, float("-inf"), 65536, None) == C["FVF_ERR_ALPHA"]
+    assert ax(None, None, None, 0, ext, 0.75, 0.25, 0.1, None, None) == C["FVF_OK"]
+    assert ax(None, None, None, 2, E3(3, 0, 5), 0.75, 0.25, 0.1, None, None) == C["FVF_OK"]
+    assert ax(None, 4096, 8192, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NULL"]
+    assert ax(4096, 4096, None, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NULL"]
+    assert ax(4096, 4096, 8192, 2, ext, 0.75, 0.25, 0.1, None, None) == C["FVF_ERR_NULL"]
+    assert ax(4096, 4100, 8192, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_ALIGN"]
+    assert ax(4096, 4096, 8192, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NOT_DEVICE"]
+    assert st(4096, 4096, fl, w, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NOT_DEVICE"]
+    assert st(4096, 4096, None, w, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NULL"]
+    assert st(4096, 4096, fl, None, 2, ext, 0.75, 0.25, 0.1, 65536, None) == C["FVF_ERR_NULL"]
+    assert st(4096, 4096, (vp * 3)(None, 8192, None), w, 2, ext, 0.75, 0.25, 0.1, 65536,
+              None) == C["FVF_ERR_NULL"]
+    assert st(4096, 4096, (vp * 3)(4096, 8192, 12288), w, 2, ext, 0.75, 0.25, 0.1, 65536,
+              None) == C["FVF_ERR_NULL"]   # z flux given without its inverse widths
+    assert st(4096, 4096, fl, (vp * 3)(16384, 16452, None), 2, ext, 0.75, 0.25, 0.1, 65536,
+              None) == C["FVF_ERR_ALIGN"]
+    assert st(4096, 4096, fl, w, 2, ext, 0.75, 0.25, float("nan"), 65536, None) == \
+        C["FVF_ERR_ALPHA"]
