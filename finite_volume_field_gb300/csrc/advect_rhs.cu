@@ -16,41 +16,93 @@
 // loop, and the face offsets are computed once and reused for every variable.
 // The contiguous index j is on the lanes, so every load and store of a warp
 // is coalesced in all three directions.
+#include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
+
+#ifndef FVF_RHS_EMU
+#define FVF_RHS_EMU 0
+#endif
 
 namespace fvf {
 namespace {
 
+constexpr int kThreads = 256;
+constexpr int kGroup = 4;  // variables per load batch
+
+// Face difference F(c-1) - F(c) of variable slot q of a batch: on the FP64
+// unit, or as an exact integer-pipe addition of -F(c) when bit q of
+// FVF_RHS_EMU is set.
+template <int Q>
+__device__ __forceinline__ double face_diff(double lo, double hi) {
+    if ((FVF_RHS_EMU >> Q) & 1) return emu::add(lo, emu::from_bits(emu::bits(hi) ^ emu::kSign));
+    return __dsub_rn(lo, hi);
+}
+
 // F extents per variable (F1, F2, F3); the high face of a cell is `step`
-// elements after its low face (1, F1 or F1*F2).
-template <int DIR, bool ACC>
-__global__ void __launch_bounds__(256)
+// elements after its low face (1, F1 or F1*F2).  One thread per cell (j, k)
+// of a plane l, the (j, k) pairs flattened over the block so that every lane
+// has a cell whatever n1 is: the kernel is bound by the FP64 unit, which
+// charges idle lanes.
+template <int DIR, bool ACC, typename Idx>
+__global__ void __launch_bounds__(kThreads)
 advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ inv_d, int nv,
-                  int64_t n1, int64_t n2, int64_t n3, double *__restrict__ rhs) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= n1) return;
-    const int64_t F1 = DIR == 0 ? n1 + 1 : n1;
-    const int64_t F2 = DIR == 1 ? n2 + 1 : n2;
+                  int64_t n1_, int64_t n2_, int64_t n3, double *__restrict__ rhs) {
+    const Idx n1 = (Idx)n1_, n2 = (Idx)n2_;
+    const Idx plane = n1 * n2;
+    const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
+    if (jk >= plane) return;
+    const Idx k = jk / n1, j = jk - k * n1;
+    const int64_t F1 = DIR == 0 ? (int64_t)n1 + 1 : (int64_t)n1;
+    const int64_t F2 = DIR == 1 ? (int64_t)n2 + 1 : (int64_t)n2;
     const int64_t F3 = DIR == 2 ? n3 + 1 : n3;
     const int64_t fplane = F1 * F2 * F3;
-    const int64_t rplane = n1 * n2 * n3;
+    const int64_t rplane = (int64_t)plane * n3;
     const int64_t step = DIR == 0 ? 1 : (DIR == 1 ? F1 : F1 * F2);
-    for (int64_t kl = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; kl < n2 * n3;
-         kl += (int64_t)gridDim.y * blockDim.y) {
-        const int64_t k = kl % n2, l = kl / n2;
-        const double w = __ldg(inv_d + (DIR == 0 ? j : (DIR == 1 ? k : l)));
-        const int64_t lo = j + F1 * (k + F2 * l);  // face c-1 sits at stored position c
+    const double wjk = DIR == 0 ? __ldg(inv_d + j) : (DIR == 1 ? __ldg(inv_d + k) : 0.0);
+    for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
+        const double w = DIR == 2 ? __ldg(inv_d + l) : wjk;
+        const int64_t lo = (int64_t)j + F1 * ((int64_t)k + F2 * l);  // face c-1 at position c
         const double *f = flux + lo;
-        double *r = rhs + j + n1 * kl;
-#pragma unroll 4
-        for (int i = 0; i < nv; ++i) {
-            const double a = __ldg(f + (int64_t)i * fplane);
-            const double b = __ldg(f + (int64_t)i * fplane + step);
-            const double term = __dmul_rn(w, __dsub_rn(a, b));
-            // accumulate form: the term added once to the existing rhs
-            r[(int64_t)i * rplane] = ACC ? __dadd_rn(r[(int64_t)i * rplane], term) : term;
+        double *r = rhs + (int64_t)jk + (int64_t)plane * l;
+        for (int i0 = 0; i0 < nv; i0 += kGroup) {
+            double a[kGroup], b[kGroup], old[kGroup];
+#pragma unroll
+            for (int q = 0; q < kGroup; ++q) {
+                if (i0 + q < nv) {
+                    const int64_t fo = (int64_t)(i0 + q) * fplane;
+                    a[q] = __ldg(f + fo);
+                    b[q] = __ldg(f + fo + step);
+                    if (ACC) old[q] = r[(int64_t)(i0 + q) * rplane];
+                }
+            }
+#define FVF_RHS_Q(Q)                                                                    \
+    if (i0 + Q < nv) {                                                                  \
+        const double term = __dmul_rn(w, face_diff<Q>(a[Q], b[Q]));                     \
+        /* accumulate form: the term added once to the existing rhs */                 \
+        r[(int64_t)(i0 + Q) * rplane] = ACC ? __dadd_rn(old[Q], term) : term;          \
+    }
+            FVF_RHS_Q(0)
+            FVF_RHS_Q(1)
+            FVF_RHS_Q(2)
+            FVF_RHS_Q(3)
+#undef FVF_RHS_Q
         }
     }
+}
+
+template <int DIR, bool ACC>
+void launch_typed(const double *flux, const double *inv_d, int nv, const int64_t n[3],
+                  double *rhs, cudaStream_t stream) {
+    const int64_t plane = n[0] * n[1];
+    const dim3 grid((unsigned)((plane + kThreads - 1) / kThreads),
+                    (unsigned)(n[2] < 65535 ? n[2] : 65535));
+    // 32-bit (j, k) arithmetic while the plane index fits
+    if (plane + kThreads < ((int64_t)1 << 31))
+        advect_rhs_kernel<DIR, ACC, uint32_t><<<grid, kThreads, 0, stream>>>(
+            flux, inv_d, nv, n[0], n[1], n[2], rhs);
+    else
+        advect_rhs_kernel<DIR, ACC, int64_t><<<grid, kThreads, 0, stream>>>(
+            flux, inv_d, nv, n[0], n[1], n[2], rhs);
 }
 
 }  // namespace
@@ -58,21 +110,18 @@ advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ in
 cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
                               const int64_t n[3], int dir, bool accumulate, double *rhs,
                               cudaStream_t stream, uint64_t *launches) {
-    const dim3 block(64, 4);
-    const int64_t gx = (n[0] + 63) / 64;
-    const int64_t gy = (n[1] * n[2] + 3) / 4;
+    const int64_t gx = (n[0] * n[1] + kThreads - 1) / kThreads;
     if (gx > 0x7fffffff) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
-#define FVF_RHS_LAUNCH(D, A) \
-    advect_rhs_kernel<D, A><<<grid, block, 0, stream>>>(flux, inv_d, nv, n[0], n[1], n[2], rhs)
     if (dir == 0) {
-        if (accumulate) FVF_RHS_LAUNCH(0, true); else FVF_RHS_LAUNCH(0, false);
+        if (accumulate) launch_typed<0, true>(flux, inv_d, nv, n, rhs, stream);
+        else launch_typed<0, false>(flux, inv_d, nv, n, rhs, stream);
     } else if (dir == 1) {
-        if (accumulate) FVF_RHS_LAUNCH(1, true); else FVF_RHS_LAUNCH(1, false);
+        if (accumulate) launch_typed<1, true>(flux, inv_d, nv, n, rhs, stream);
+        else launch_typed<1, false>(flux, inv_d, nv, n, rhs, stream);
     } else {
-        if (accumulate) FVF_RHS_LAUNCH(2, true); else FVF_RHS_LAUNCH(2, false);
+        if (accumulate) launch_typed<2, true>(flux, inv_d, nv, n, rhs, stream);
+        else launch_typed<2, false>(flux, inv_d, nv, n, rhs, stream);
     }
-#undef FVF_RHS_LAUNCH
     ++*launches;
     return cudaGetLastError();
 }

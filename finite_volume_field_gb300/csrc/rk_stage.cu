@@ -40,6 +40,9 @@
 #ifndef FVF_RK_EMU
 #define FVF_RK_EMU 0
 #endif
+#ifndef FVF_RK_EMU_Q
+#define FVF_RK_EMU_Q 0xFF
+#endif
 #ifndef FVF_RK_CHUNK
 #define FVF_RK_CHUNK 2
 #endif
@@ -50,15 +53,18 @@ namespace {
 constexpr int kChunk = FVF_RK_CHUNK;
 constexpr int kThreads = 256;
 
+// q is the variable's slot in its load batch (a constant once the batch loop
+// is unrolled): FVF_RK_EMU_Q selects the slots whose additions are emulated.
 template <int BIT>
-__device__ __forceinline__ double add_rn(double x, double y) {
-    if (FVF_RK_EMU & BIT) return emu::add(x, y);
+__device__ __forceinline__ double add_rn(double x, double y, int q) {
+    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> q) & 1)) return emu::add(x, y);
     return __dadd_rn(x, y);
 }
 
 template <int BIT>
-__device__ __forceinline__ double sub_rn(double x, double y) {
-    if (FVF_RK_EMU & BIT) return emu::add(x, emu::from_bits(emu::bits(y) ^ emu::kSign));
+__device__ __forceinline__ double sub_rn(double x, double y, int q) {
+    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> q) & 1))
+        return emu::add(x, emu::from_bits(emu::bits(y) ^ emu::kSign));
     return __dsub_rn(x, y);
 }
 
@@ -112,15 +118,15 @@ rk_stage_kernel(RkStageArgs A) {
                 if (i0 + q < A.nv) {
                     double rr;
                     if (FUSED) {
-                        rr = __dmul_rn(wx, sub_rn<16>(xl[q], xh[q]));
-                        if (FY) rr = add_rn<1>(rr, __dmul_rn(wy, sub_rn<32>(yl[q], yh[q])));
-                        if (FZ) rr = add_rn<2>(rr, __dmul_rn(wz, sub_rn<64>(zl[q], zh[q])));
+                        rr = __dmul_rn(wx, sub_rn<16>(xl[q], xh[q], q));
+                        if (FY) rr = add_rn<1>(rr, __dmul_rn(wy, sub_rn<32>(yl[q], yh[q], q)), q);
+                        if (FZ) rr = add_rn<2>(rr, __dmul_rn(wz, sub_rn<64>(zl[q], zh[q], q)), q);
                     } else {
                         rr = r[q];
                     }
-                    const double t = add_rn<4>(uv[q], __dmul_rn(A.dt, rr));
+                    const double t = add_rn<4>(uv[q], __dmul_rn(A.dt, rr), q);
                     A.out[c + (int64_t)(i0 + q) * cplane] =
-                        add_rn<8>(__dmul_rn(A.a, u0v[q]), __dmul_rn(A.b, t));
+                        add_rn<8>(__dmul_rn(A.a, u0v[q]), __dmul_rn(A.b, t), q);
                 }
             }
         }

@@ -65,6 +65,10 @@ def _load():
     lib.oracle_diffuse2d_f64.restype = cint
     lib.oracle_diffuse2d_f32.argtypes = [vp, vp, i64, i64, flt, i64, cint]
     lib.oracle_diffuse2d_f32.restype = cint
+    lib.oracle_diffuse3d_f64.argtypes = [vp, vp, i64, i64, i64, dbl, i64, cint]
+    lib.oracle_diffuse3d_f64.restype = cint
+    lib.oracle_diffuse3d_f32.argtypes = [vp, vp, i64, i64, i64, flt, i64, cint]
+    lib.oracle_diffuse3d_f32.restype = cint
     lib.oracle_weno_pack.argtypes = [ctypes.POINTER(vp), cint, i64, i64, i64, i64, cint, vp]
     lib.oracle_weno_pack.restype = cint
     lib.oracle_advect_rhs.argtypes = [vp, vp, cint, i64, i64, i64, cint, vp]
@@ -121,6 +125,33 @@ def diffuse2d(u0: np.ndarray, nsteps: int, alpha: float = 0.1, v0: np.ndarray | 
                                         int(nthreads))
     elif u.dtype == np.float32:
         in_v = lib.oracle_diffuse2d_f32(_ptr(u), _ptr(v), nx, ny,
+                                        float(np.float32(alpha)), int(nsteps), int(nthreads))
+    else:
+        raise TypeError("dtype must be float32 or float64")
+    if return_both:
+        return u, v, bool(in_v)
+    return v if in_v else u
+
+
+def diffuse3d(u0: np.ndarray, nsteps: int, alpha: float = 0.1, v0: np.ndarray | None = None,
+              nthreads: int = 1, return_both: bool = False):
+    """``nsteps`` ping-pong applications of the 7-point update on a 3D grid.
+
+    ``u0`` has shape (nz, ny, nx) in C order: element [k, j, i] is u(i, j, k)
+    at address i + nx*(j + ny*k), the column-major layout with i fastest.
+    Otherwise as ``diffuse2d``.
+    """
+    u = np.array(u0, copy=True, order="C")
+    if u.ndim != 3:
+        raise ValueError("u0 must be 3D (nz, ny, nx)")
+    nz, ny, nx = u.shape
+    v = np.zeros_like(u) if v0 is None else np.array(v0, dtype=u.dtype, copy=True, order="C")
+    lib = _load()
+    if u.dtype == np.float64:
+        in_v = lib.oracle_diffuse3d_f64(_ptr(u), _ptr(v), nx, ny, nz, float(alpha), int(nsteps),
+                                        int(nthreads))
+    elif u.dtype == np.float32:
+        in_v = lib.oracle_diffuse3d_f32(_ptr(u), _ptr(v), nx, ny, nz,
                                         float(np.float32(alpha)), int(nsteps), int(nthreads))
     else:
         raise TypeError("dtype must be float32 or float64")

@@ -130,6 +130,99 @@ int oracle_diffuse2d_f32(float *u, float *v, int64_t nx, int64_t ny,
 }
 
 /* ---------------------------------------------------------------------- */
+/* 3D explicit diffusion (7-point)                                        */
+/* ---------------------------------------------------------------------- */
+
+/*
+ * The 7-point variant of the update of [Q] section 3 on a 3D grid (the
+ * 2D scheme with the two z neighbours added and the centre weight 6):
+ *     dst(i,j,k) = c + alpha*(W + E + S + N + B + T - 6c)
+ * with W/E = src(i-+1,j,k), S/N = src(i,j-+1,k), B/T = src(i,j,k-+1), for
+ * interior cells, and dst = 0 on the six boundary faces ([Q] section 5.1
+ * extended to 3D).  Evaluated left to right as in the 2D update:
+ * (((((W + E) + S) + N) + B) + T) - 6c, then alpha times that, then c plus
+ * the product; 6c is its own rounded product (unlike 4c it is not exact).
+ * Column-major layout, i fastest: cell (i,j,k) at i + nx*(j + ny*k).
+ */
+static void step3d_f64(const double *src, double *dst, int64_t nx, int64_t ny, int64_t nz,
+                       double alpha, int nthreads)
+{
+    const int64_t sxy = nx * ny;
+    int64_t k;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (k = 0; k < nz; ++k) {
+        for (int64_t j = 0; j < ny; ++j) {
+            for (int64_t i = 0; i < nx; ++i) {
+                const int64_t c = i + nx * (j + ny * k);
+                if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1 || k == 0 || k == nz - 1) {
+                    dst[c] = 0.0;
+                } else {
+                    dst[c] = src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]
+                                               + src[c + nx] + src[c - sxy] + src[c + sxy]
+                                               - 6.0 * src[c]);
+                }
+            }
+        }
+    }
+}
+
+static void step3d_f32(const float *src, float *dst, int64_t nx, int64_t ny, int64_t nz,
+                       float alpha, int nthreads)
+{
+    const int64_t sxy = nx * ny;
+    int64_t k;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (k = 0; k < nz; ++k) {
+        for (int64_t j = 0; j < ny; ++j) {
+            for (int64_t i = 0; i < nx; ++i) {
+                const int64_t c = i + nx * (j + ny * k);
+                if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1 || k == 0 || k == nz - 1) {
+                    dst[c] = 0.0f;
+                } else {
+                    dst[c] = src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]
+                                               + src[c + nx] + src[c - sxy] + src[c + sxy]
+                                               - 6.0f * src[c]);
+                }
+            }
+        }
+    }
+}
+
+/* nsteps ping-pong applications ([Q] section 5.4, as oracle_diffuse2d_f64).
+ * Returns 1 when the result is in v, 0 when it is in u. */
+int oracle_diffuse3d_f64(double *u, double *v, int64_t nx, int64_t ny, int64_t nz,
+                         double alpha, int64_t nsteps, int nthreads)
+{
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        if (s % 2 == 1)
+            step3d_f64(u, v, nx, ny, nz, alpha, nthreads);
+        else
+            step3d_f64(v, u, nx, ny, nz, alpha, nthreads);
+    }
+    return (int)(nsteps % 2);
+}
+
+int oracle_diffuse3d_f32(float *u, float *v, int64_t nx, int64_t ny, int64_t nz,
+                         float alpha, int64_t nsteps, int nthreads)
+{
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        if (s % 2 == 1)
+            step3d_f32(u, v, nx, ny, nz, alpha, nthreads);
+        else
+            step3d_f32(v, u, nx, ny, nz, alpha, nthreads);
+    }
+    return (int)(nsteps % 2);
+}
+
+/* ---------------------------------------------------------------------- */
 /* 3D box helpers                                                         */
 /* ---------------------------------------------------------------------- */
 

@@ -20,6 +20,7 @@ import pytest
 
 import oracle
 import tests.test_oracle_diffusion as D
+import tests.test_oracle_diffusion3d as D3
 import tests.test_oracle_pack_flux as P
 import tests.test_oracle_rk as R
 
@@ -39,7 +40,8 @@ def _mutant(tmp_path, old: str, new: str, count: int = 1):
                     "-o", str(so), "-lm"], check=True, capture_output=True)
     real = oracle._load()
     lib = ctypes.CDLL(str(so))
-    for name in ("oracle_diffuse2d_f64", "oracle_diffuse2d_f32", "oracle_weno_pack",
+    for name in ("oracle_diffuse2d_f64", "oracle_diffuse2d_f32", "oracle_diffuse3d_f64",
+                 "oracle_diffuse3d_f32", "oracle_weno_pack",
                  "oracle_advect_rhs", "oracle_advect_rhs_add", "oracle_flux_unpack",
                  "oracle_fields_copy", "oracle_rk_axpby", "oracle_max_threads"):
         getattr(lib, name).argtypes = getattr(real, name).argtypes
@@ -55,6 +57,10 @@ STENCIL = ("src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]\n"
            "                                           + src[c + nx] - 4.0 * src[c])")
 STENCIL32 = ("src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]\n"
              "                                           + src[c + nx] - 4.0f * src[c])")
+
+STENCIL3D_32 = ("src[c] + alpha * (src[c - 1] + src[c + 1] + src[c - nx]\n"
+                "                                               + src[c + nx] + src[c - sxy] + src[c + sxy]\n"
+                "                                               - 6.0f * src[c])")
 
 MUTANTS = [
     # (id, old, new, count, pin that must fail)
@@ -106,6 +112,20 @@ MUTANTS = [
      "for (int64_t e = 0; e < total; ++e)\n            dst[i][e]",
      "for (int64_t e = 0; e < total - 1; ++e)\n            dst[i][e]",
      1, lambda: P.test_fields_copy_is_bitwise_identity()),
+    ("3d-centre-weight-4",
+     "- 6.0 * src[c]", "- 4.0 * src[c]",
+     1, lambda: D3.test_one_step_impulse_exact()),
+    ("3d-z-neighbour-index",
+     "src[c - sxy] + src[c + sxy]", "src[c - nx] + src[c + sxy]",
+     1, lambda: D3.test_exact_on_dyadic_inputs_with_nonzero_edges()),
+    ("3d-top-face-not-zeroed",
+     "k == 0 || k == nz - 1) {\n                    dst[c] = 0.0;",
+     "k == 0) {\n                    dst[c] = 0.0;",
+     1, lambda: D3.test_exact_on_dyadic_inputs_with_nonzero_edges()),
+    ("3d-sum-order-fp32",
+     STENCIL3D_32,
+     STENCIL3D_32.replace("src[c - 1] + src[c + 1] + src[c - nx]", "src[c - 1] + (src[c + 1] + src[c - nx])"),
+     1, lambda: D3.test_summation_order_fp32_worked_value()),
     ("stage-coefficients-swapped",
      "const double p = a * u0[e];\n        const double q = b * t;",
      "const double p = b * u0[e];\n        const double q = a * t;",
