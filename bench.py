@@ -492,8 +492,9 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     the physical frame on the 8 x 201^3 flux workload's buffers, the
     conservative-variable copy alone and fused with the pack on the 8 x 207^3
     pack workload's fields, the SSPRK3 stage update (fused with the flux
-    difference, alone, and unfused) on the flux workload, and the latency of
-    the 64 x 64 FP64 diffusion case.  Stage rows count the bytes of the fused
+    difference, alone, and unfused) on the flux workload, the 3D 7-point
+    diffusion (512^3, 20 steps, FP32 and FP64; 10 FP64 operations per interior
+    cell counting 6c) and the latency of the 64 x 64 FP64 diffusion case.  Stage rows count the bytes of the fused
     form (the unfused row's extra rhs traffic is its cost) and 13 FP64
     operations per element (5 for the update alone)."""
     from finite_volume_field_gb300 import api
@@ -579,6 +580,17 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
         api.ssprk3_axpby(u0, u, rhs, RHS_NV, RHS_EXT, a, b, dt, uo, stream)
     record("ssprk3_stage_unfused_xyz", stage_unfused, face_bytes + 24 * cells, cells, 13)
     del u0, u, uo
+    # 3D 7-point diffusion, 512^3, 20 steps per call, FP32 and FP64
+    n3 = 512
+    cells3 = n3 ** 3
+    for name, dt, code, esize, flops in (("diffuse3d_fp32", torch.float32, api.FVF_FP32, 4, 0),
+                                         ("diffuse3d_fp64", torch.float64, api.FVF_FP64, 8, 10)):
+        u3 = torch.rand(cells3, dtype=dt, device=sw.dev)
+        v3 = torch.zeros_like(u3)
+        record(name, lambda u3=u3, v3=v3, code=code: api.diffuse3d_step(
+            u3, v3, n3, n3, n3, 0.1, 20, code, stream), 20 * 2 * esize * cells3,
+            20 * (n3 - 2) ** 3, flops)
+        del u3, v3
     # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
     # (both states live in shared memory), reported per call and per step
     u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)
@@ -786,7 +798,8 @@ def run_ncu_case():
     207^3, the conservative-variable copy alone and fused with the pack x/y/z
     on the same fields (at most about 1.7 GB), flux difference x/y/z on
     8 x 201^3, the SSPRK3 stage fused with the x/y/z flux difference on
-    8 x 201^3 (about 3.1 GB).  FP64 runs 2 single steps, FP32 17 steps (two
+    8 x 201^3 (about 3.1 GB), one 3D 7-point diffusion step on 512^3 in FP32
+    then FP64 (at most 2.1 GB).  FP64 runs 2 single steps, FP32 17 steps (two
     8-step shared-memory launches, then one single step).  Device-generated values (the
     kernels' timing does not depend on them)."""
     import torch
@@ -837,6 +850,12 @@ def run_ncu_case():
     api.ssprk3_stage(u0, u, fl, ws, RHS_NV, RHS_EXT, 0.75, 0.25, 1e-4, u)
     del fl, ws, u0, u
     free()
+    for dt, code in ((torch.float32, api.FVF_FP32), (torch.float64, api.FVF_FP64)):
+        u = torch.rand(512 ** 3, dtype=dt, device="cuda")
+        v = torch.zeros_like(u)
+        api.diffuse3d_step(u, v, 512, 512, 512, 0.1, 1, code)
+        del u, v
+        free()
     print("ncu case done", flush=True)
     return 0
 

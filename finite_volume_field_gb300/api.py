@@ -45,6 +45,8 @@ def load() -> ctypes.CDLL:
     i64, vp, cint = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.diffuse2d_step.argtypes = [vp, vp, i64, i64, ctypes.c_double, i64, cint, vp]
     lib.diffuse2d_step.restype = cint
+    lib.diffuse3d_step.argtypes = [vp, vp, i64, i64, i64, ctypes.c_double, i64, cint, vp]
+    lib.diffuse3d_step.restype = cint
     lib.weno_pack.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint, cint, vp, vp]
     lib.weno_pack.restype = cint
     lib.advect_rhs.argtypes = [vp, vp, cint, ctypes.POINTER(i64), cint, vp, vp]
@@ -69,6 +71,8 @@ def load() -> ctypes.CDLL:
     lib.fvf_status_string.restype = ctypes.c_char_p
     lib.fvf_last_cuda_error.argtypes = []
     lib.fvf_last_cuda_error.restype = cint
+    lib.fvf_device_error.argtypes = [ctypes.POINTER(cint)]
+    lib.fvf_device_error.restype = cint
     lib.fvf_launch_count.argtypes = []
     lib.fvf_launch_count.restype = ctypes.c_uint64
     _lib = lib
@@ -82,6 +86,14 @@ def status_string(status: int) -> str:
 def launch_count() -> int:
     """Kernels launched by the library since it was loaded."""
     return int(load().fvf_launch_count())
+
+
+def device_error() -> int:
+    """Reads and clears the device flag set when a kernel's bounded wait on
+    its own copies expired (0: none).  Synchronises the device."""
+    flag = ctypes.c_int(0)
+    _check("fvf_device_error", load().fvf_device_error(ctypes.byref(flag)))
+    return int(flag.value)
 
 
 def last_cuda_error() -> int:
@@ -148,6 +160,22 @@ def diffuse2d_step(u, v, nx: int, ny: int, alpha: float, nsteps: int, dtype: int
     st = load().diffuse2d_step(_addr(u, tdt, "u"), _addr(v, tdt, "v"), int(nx), int(ny),
                                float(alpha), int(nsteps), int(dtype), _stream(stream))
     _check("diffuse2d_step", st)
+
+
+def diffuse3d_step(u, v, nx: int, ny: int, nz: int, alpha: float, nsteps: int,
+                   dtype: int | None = None, stream=None) -> None:
+    """Enqueue ``nsteps`` ping-pong 7-point diffusion steps on an nx*ny*nz
+    grid (include/fvf.h); dtype as for ``diffuse2d_step``."""
+    if dtype is None:
+        import torch
+        dtype = FVF_FP64 if u.dtype == torch.float64 else FVF_FP32
+    tdt = None
+    if not isinstance(u, int):
+        import torch
+        tdt = torch.float64 if dtype == FVF_FP64 else torch.float32
+    st = load().diffuse3d_step(_addr(u, tdt, "u"), _addr(v, tdt, "v"), int(nx), int(ny), int(nz),
+                               float(alpha), int(nsteps), int(dtype), _stream(stream))
+    _check("diffuse3d_step", st)
 
 
 def weno_pack(fields, nv: int, extents, ghost: int, dir: int, out, stream=None) -> None:

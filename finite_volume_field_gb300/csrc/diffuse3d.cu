@@ -1,0 +1,583 @@
+// diffuse3d.cu -- explicit 3D 7-point diffusion step (FP32 and FP64) with
+// ping-pong buffers, for sm_103a.
+//
+// Operation: the 3D variant of the update of Qiita, "Fortran 2018 GPU
+// acceleration, part 3" (section 3, with the edges of section 5.1 and the
+// ping-pong of section 5.4): for interior cells
+//     dst(i,j,k) = c + alpha*((((((W + E) + S) + N) + B) + T) - 6c)
+// with W/E the i-1/i+1, S/N the j-1/j+1 and B/T the k-1/k+1 neighbours, and
+// dst = 0 on the six boundary faces.  Column-major layout, i contiguous:
+// cell (i,j,k) at i + nx*(j + ny*k).  Every operation is rounded to nearest
+// even on its own in the order written; 6c is its own rounded product (6c is
+// not a power-of-two scaling, so no fused form is exact here).
+//
+// Kernels (both march along k; a block of kTY warps owns a tile of 32*V
+// cells along i by kTY rows along j, V = 4 FP32 or 2 FP64 cells per lane).
+//   bulk   (FP32, rows 16-byte aligned: nx a multiple of 4, 16-byte
+//          buffers): one thread streams whole planes of the tile into a ring
+//          of shared-memory slots with tensor-map bulk copies
+//          (cp.async.bulk.tensor), three planes ahead of the plane being
+//          computed.  A plane is one (32V+2V) x (kTY+2) box: the tile's kTY
+//          rows plus one halo row above and below, each widened by 16 bytes
+//          on both sides for the W/E neighbours; the copy engine zero-fills
+//          the parts outside the grid, and one mbarrier per slot counts the
+//          bytes in.  Every cell then reads c, W, E, S, N, B and T from the
+//          staged planes k-1, k and k+1, so HBM sees each element once per
+//          step (the halo rows and the planes at the ends of a run are the
+//          only re-reads, mostly from L2).  The grid is persistent: about as
+//          many blocks as fit at once, each taking an equal number of (tile,
+//          run of planes) items.  Every mbarrier wait is bounded; if one
+//          expires the block records it in a device flag (fvf_device_error),
+//          waits (bounded) for its copies in flight and returns.
+//   march  (FP64, and FP32 rows that are not 16-byte aligned; V cells per
+//          lane, 1 when unaligned): each lane keeps planes k-1, k, k+1 of its
+//          cells in registers and prefetches k+2; W/E by warp shuffle, S/N
+//          from the tile's rows staged in shared memory.  The grid splits the
+//          planes into runs so that about 8 blocks per SM are in flight.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "fp64_emu.cuh"
+#include "fvf_internal.cuh"
+
+// Number of the five neighbour sums (W+E, +S, +N, +B, +T, in that order) that
+// the FP64 update runs on the integer pipes (fp64_emu.cuh); every choice gives
+// the same bits.
+#ifndef FVF_3D_EMU_SUMS
+#define FVF_3D_EMU_SUMS 3
+#endif
+// 1: aligned FP32 grids take the bulk-copy kernel; 0: the register march
+// kernel.  FP64 always takes the march kernel, which measured faster there
+// (FP64 arithmetic, not memory, bounds the FP64 update).
+#ifndef FVF_3D_BULK
+#define FVF_3D_BULK 1
+#endif
+
+namespace fvf {
+namespace {
+
+constexpr int kTY = 8;  // warps (rows along j) per block
+
+__device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
+__device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
+__device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
+
+template <int I>
+__device__ __forceinline__ float sum_rn(float a, float b) { return __fadd_rn(a, b); }
+template <int I>
+__device__ __forceinline__ double sum_rn(double a, double b) {
+    return I < FVF_3D_EMU_SUMS ? emu::add_same_sign(a, b) : __dadd_rn(a, b);
+}
+
+template <typename T>
+__device__ __forceinline__ T update3(T c, T w, T e, T s, T n, T b, T t, T alpha) {
+    T x = sum_rn<0>(w, e);
+    x = sum_rn<1>(x, s);
+    x = sum_rn<2>(x, n);
+    x = sum_rn<3>(x, b);
+    x = sum_rn<4>(x, t);
+    return add_rn(c, mul_rn(alpha, sub_rn(x, mul_rn(T(6), c))));
+}
+
+template <typename T, int V>
+struct Vec {
+    T v[V];
+};
+
+// Loads this lane's vector of row `row` (cells x0 + lane*V .. +V-1; zeros
+// past the end) and, for lanes 0 and 31, the outside neighbour of the warp's
+// segment (x0 - 1 and x0 + 32V; zero where it does not exist).
+template <typename T, int V>
+__device__ __forceinline__ void load_row(const T *__restrict__ row, int64_t x0, int lane,
+                                         int64_t nx, Vec<T, V> &out, T &xh) {
+    const int64_t xi = x0 + (int64_t)lane * V;
+    if (xi < nx) {
+        if constexpr (V == 4) {
+            const float4 q = __ldg(reinterpret_cast<const float4 *>(row + xi));
+            out.v[0] = q.x; out.v[1] = q.y; out.v[2] = q.z; out.v[3] = q.w;
+        } else if constexpr (V == 2) {
+            const double2 q = __ldg(reinterpret_cast<const double2 *>(row + xi));
+            out.v[0] = q.x; out.v[1] = q.y;
+        } else {
+            out.v[0] = __ldg(row + xi);
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < V; ++v) out.v[v] = T(0);
+    }
+    const int64_t xo = lane == 0 ? x0 - 1 : x0 + 32 * V;
+    xh = ((lane == 0 || lane == 31) && xo >= 0 && xo < nx) ? __ldg(row + xo) : T(0);
+}
+
+template <typename T, int V>
+__device__ __forceinline__ void store_row(T *__restrict__ row, int64_t x0, int lane, int64_t nx,
+                                          const Vec<T, V> &x) {
+    const int64_t xi = x0 + (int64_t)lane * V;
+    if (xi >= nx) return;
+    if constexpr (V == 4) {
+        *reinterpret_cast<float4 *>(row + xi) = make_float4(x.v[0], x.v[1], x.v[2], x.v[3]);
+    } else if constexpr (V == 2) {
+        *reinterpret_cast<double2 *>(row + xi) = make_double2(x.v[0], x.v[1]);
+    } else {
+        row[xi] = x.v[0];
+    }
+}
+
+template <typename T, int V>
+__device__ __forceinline__ void store_vec(T *p, const Vec<T, V> &x) {
+    if constexpr (V == 4) {
+        *reinterpret_cast<float4 *>(p) = make_float4(x.v[0], x.v[1], x.v[2], x.v[3]);
+    } else if constexpr (V == 2) {
+        *reinterpret_cast<double2 *>(p) = make_double2(x.v[0], x.v[1]);
+    } else {
+        *p = x.v[0];
+    }
+}
+
+template <typename T, int V>
+__global__ void __launch_bounds__(32 * kTY)
+diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
+                 int64_t nz, T alpha, int64_t kz_len) {
+    __shared__ T rows[2][kTY + 2][32 * V];
+    const int lane = threadIdx.x, w = threadIdx.y;
+    const int64_t x0 = (int64_t)blockIdx.x * (32 * V);
+    const int64_t j0 = (int64_t)blockIdx.y * kTY;
+    const int64_t j = j0 + w;
+    const int64_t kz0 = (int64_t)blockIdx.z * kz_len;
+    const int64_t kz1 = kz0 + kz_len < nz ? kz0 + kz_len : nz;
+    const int64_t sxy = nx * ny;
+    const bool rowok = j < ny;
+    // halo rows of the tile: warp 0 also carries row j0-1, warp kTY-1 row j0+kTY
+    const int64_t jh = w == 0 ? j0 - 1 : j0 + kTY;
+    const bool hok = (w == 0 || w == kTY - 1) && jh >= 0 && jh < ny;
+    const int hslot = w == 0 ? 0 : kTY + 1;
+    const int64_t klast = kz1 < nz ? kz1 : nz - 1;  // last plane this block reads
+
+    Vec<T, V> prev, cur, next, nn, hcur, hnext, hnn;
+    T xp = T(0), xc = T(0), xn = T(0), xnn = T(0), hx;
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+        prev.v[v] = cur.v[v] = next.v[v] = nn.v[v] = T(0);
+        hcur.v[v] = hnext.v[v] = hnn.v[v] = T(0);
+    }
+    if (rowok) {
+        if (kz0 >= 1) load_row<T, V>(src + j * nx + (kz0 - 1) * sxy, x0, lane, nx, prev, xp);
+        load_row<T, V>(src + j * nx + kz0 * sxy, x0, lane, nx, cur, xc);
+        if (kz0 + 1 <= klast) load_row<T, V>(src + j * nx + (kz0 + 1) * sxy, x0, lane, nx, next, xn);
+    }
+    if (hok) {
+        load_row<T, V>(src + jh * nx + kz0 * sxy, x0, lane, nx, hcur, hx);
+        if (kz0 + 1 <= klast) load_row<T, V>(src + jh * nx + (kz0 + 1) * sxy, x0, lane, nx, hnext, hx);
+    }
+    (void)xp;
+    int buf = 0;
+    for (int64_t k = kz0; k < kz1; ++k) {
+        // stage plane k of the tile's rows (and halo rows) for the S/N reads
+        if (rowok) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) rows[buf][w + 1][lane * V + v] = cur.v[v];
+        }
+        if (hok) {
+#pragma unroll
+            for (int v = 0; v < V; ++v) rows[buf][hslot][lane * V + v] = hcur.v[v];
+        }
+        // prefetch plane k+2
+        if (k + 2 <= klast) {
+            if (rowok) load_row<T, V>(src + j * nx + (k + 2) * sxy, x0, lane, nx, nn, xnn);
+            if (hok) load_row<T, V>(src + jh * nx + (k + 2) * sxy, x0, lane, nx, hnn, hx);
+        }
+        __syncthreads();
+        if (rowok) {
+            Vec<T, V> out;
+            const bool edge = k == 0 || k == nz - 1 || j == 0 || j == ny - 1;
+            // W of the first element and E of the last, from the neighbouring
+            // lanes (the warp-edge lanes use their outside neighbour)
+            const T wl = __shfl_up_sync(0xffffffffu, cur.v[V - 1], 1);
+            const T er = __shfl_down_sync(0xffffffffu, cur.v[0], 1);
+            const T wfirst = lane == 0 ? xc : wl;
+            const T elast = lane == 31 ? xc : er;
+            if (edge) {
+#pragma unroll
+                for (int v = 0; v < V; ++v) out.v[v] = T(0);
+            } else {
+#pragma unroll
+                for (int v = 0; v < V; ++v) {
+                    const int64_t i = x0 + (int64_t)lane * V + v;
+                    const T we = v == 0 ? wfirst : cur.v[v - 1];
+                    const T ea = v == V - 1 ? elast : cur.v[v + 1];
+                    const T so = rows[buf][w][lane * V + v];
+                    const T no = rows[buf][w + 2][lane * V + v];
+                    out.v[v] = (i == 0 || i >= nx - 1)
+                                   ? T(0)
+                                   : update3<T>(cur.v[v], we, ea, so, no, prev.v[v], next.v[v],
+                                                alpha);
+                }
+            }
+            store_row<T, V>(dst + j * nx + k * sxy, x0, lane, nx, out);
+        }
+        prev = cur;
+        cur = next;
+        next = nn;
+        xc = xn;
+        xn = xnn;
+        hcur = hnext;
+        hnext = hnn;
+        buf ^= 1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk-copy kernel
+// ---------------------------------------------------------------------------
+
+#ifndef FVF_3D_RING
+#define FVF_3D_RING 6
+#endif
+#ifndef FVF_3D_KZ
+#define FVF_3D_KZ 32
+#endif
+constexpr int kRing = FVF_3D_RING;           // slots: planes k-1, k, k+1 and kRing-3 ahead
+constexpr int kRows = kTY + 2;               // tile rows plus one halo row each side
+constexpr uint32_t kWaitLimit = 1u << 22;    // try_wait polls before a wait gives up
+
+__device__ int g_device_error;               // nonzero: a bounded wait expired
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity to complete; false if the poll
+// limit expires first.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kWaitLimit; ++it)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// One box of the 3D tensor map at (x, y, z) into shared memory.
+__device__ __forceinline__ void tensor_load(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+template <typename T, int V>
+__device__ __forceinline__ Vec<T, V> ld_stage(const T *p) {
+    Vec<T, V> r;
+    if constexpr (V == 4) {
+        const float4 q = *reinterpret_cast<const float4 *>(p);
+        r.v[0] = q.x; r.v[1] = q.y; r.v[2] = q.z; r.v[3] = q.w;
+    } else {
+        const double2 q = *reinterpret_cast<const double2 *>(p);
+        r.v[0] = q.x; r.v[1] = q.y;
+    }
+    return r;
+}
+
+// Staged row: 32V cells plus a 16-byte margin each side (544 bytes); a slot
+// holds kRows of them, padded to the 128-byte alignment of a tensor copy.
+template <typename T>
+__host__ __device__ constexpr int row_elems() {
+    return 32 * (16 / (int)sizeof(T)) + 2 * (16 / (int)sizeof(T));
+}
+template <typename T>
+__host__ __device__ constexpr size_t slot_bytes() {
+    return ((size_t)kRows * row_elems<T>() * sizeof(T) + 127) / 128 * 128;
+}
+template <typename T>
+__host__ __device__ constexpr size_t bulk_smem_bytes() {
+    return kRing * slot_bytes<T>() + kRing * sizeof(uint64_t) + 128;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kTY)
+diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict__ dst,
+                      int64_t nx, int64_t ny, int64_t nz, T alpha, int64_t kz_len,
+                      int64_t tiles_x, int64_t tiles_y, int64_t items) {
+    constexpr int V = 16 / sizeof(T);        // cells per lane
+    constexpr int P = V;                     // 16 bytes of W/E margin each side of a row
+    constexpr int TX = 32 * V;
+    constexpr int RW = TX + 2 * P;           // staged row length (544 bytes)
+    constexpr int64_t SLOT = (int64_t)(slot_bytes<T>() / sizeof(T));  // elements per slot
+    constexpr uint32_t kBoxBytes = (uint32_t)(kRows * RW * sizeof(T));
+    extern __shared__ unsigned char smem_raw[];
+    // 128-byte aligned base for the tensor copies
+    unsigned char *base = smem_raw + ((128 - (smem_addr(smem_raw) & 127)) & 127);
+    T *stage = reinterpret_cast<T *>(base);  // [kRing][SLOT], rows of RW
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + kRing * slot_bytes<T>());
+    const int lane = threadIdx.x, w = threadIdx.y;
+    const bool producer = lane == 0 && w == 0;
+    const int64_t sxy = nx * ny;
+    if (producer) {
+        for (int s = 0; s < kRing; ++s) mbar_init(smem_addr(&bars[s]), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Planes are loaded in order and numbered t = 0, 1, ... over all items of
+    // this block; plane t sits in slot t % kRing, and its completion is phase
+    // number t / kRing of that slot's mbarrier (parity (t / kRing) & 1).
+    uint32_t tbase = 0;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+        const int64_t tx = item % tiles_x, rest = item / tiles_x;
+        const int64_t ty = rest % tiles_y, run = rest / tiles_y;
+        const int64_t x0 = tx * TX, j0 = ty * kTY, kz0 = run * kz_len;
+        const int64_t kz1 = kz0 + kz_len < nz ? kz0 + kz_len : nz;
+        const int64_t pl0 = kz0 > 0 ? kz0 - 1 : 0;       // planes read: pl0..pl1
+        const int64_t pl1 = kz1 < nz ? kz1 : nz - 1;
+        // one box per plane: x from x0-P (16 bytes left of the tile), rows
+        // j0-1 .. j0+kTY; parts outside the grid arrive as zeros
+        auto issue = [&](int64_t p) {
+            const uint32_t sl = (tbase + (uint32_t)(p - pl0)) % kRing;
+            const uint32_t bar = smem_addr(&bars[sl]);
+            mbar_expect_tx(bar, kBoxBytes);
+            tensor_load(smem_addr(stage + (int64_t)sl * SLOT), &src_map, (int)(x0 - P),
+                        (int)(j0 - 1), (int)p, bar);
+        };
+        auto wait_t = [&](uint32_t t) {
+            return mbar_wait(smem_addr(&bars[t % kRing]), (t / kRing) & 1u);
+        };
+        int64_t issued = pl0 - 1;                         // producer: last plane issued
+        if (producer)
+            for (int64_t p = pl0; p <= pl1 && p < pl0 + kRing; ++p) {
+                issue(p);
+                issued = p;
+            }
+        const int64_t j = j0 + w;
+        const bool rowok = j < ny;
+        const int64_t xi = x0 + (int64_t)lane * V;
+        // every cell of this lane is interior along i: no per-cell i test
+        const bool lane_inner = xi >= 1 && xi + V <= nx - 1;
+        const int64_t ro = (int64_t)(w + 1) * RW + P + lane * V;
+        T *drow = dst + j * nx + kz0 * sxy;
+        // slots and parities of planes k-1, k, k+1, advanced every plane
+        uint32_t tk = tbase + (uint32_t)(kz0 - pl0);
+        uint32_t sc = tk % kRing, pc = (tk / kRing) & 1u;
+        uint32_t sb = (tk + kRing - 1) % kRing, pb = ((tk + kRing - 1) / kRing + 1) & 1u;
+        uint32_t st = (tk + 1) % kRing, pt = ((tk + 1) / kRing) & 1u;
+        for (int64_t k = kz0; k < kz1; ++k) {
+            bool ok = true;
+            if (k - 1 >= pl0) ok = mbar_wait(smem_addr(&bars[sb]), pb) && ok;
+            ok = mbar_wait(smem_addr(&bars[sc]), pc) && ok;
+            if (k + 1 <= pl1) ok = mbar_wait(smem_addr(&bars[st]), pt) && ok;
+            if (__syncthreads_or(!ok)) {
+                // a copy did not land in time: record it, let the copies in
+                // flight finish (bounded) and leave
+                if (producer) {
+                    atomicExch(&g_device_error, 1);
+                    for (int64_t p = k > pl0 ? k - 1 : pl0; p <= issued; ++p)
+                        (void)wait_t(tbase + (uint32_t)(p - pl0));
+                }
+                return;
+            }
+            // every thread is done with plane k-2 (read in the previous
+            // iteration): its slot takes the plane kRing-2 ahead of k
+            if (producer && k - 2 >= pl0 && k - 2 + kRing <= pl1) {
+                issue(k - 2 + kRing);
+                issued = k - 2 + kRing;
+            }
+            if (rowok) {
+                Vec<T, V> out;
+                const bool edge = k == 0 || k == nz - 1 || j == 0 || j == ny - 1;
+                if (edge) {
+#pragma unroll
+                    for (int v = 0; v < V; ++v) out.v[v] = T(0);
+                } else {
+                    const T *rc = stage + (int64_t)sc * SLOT + ro;
+                    const T *rb = stage + (int64_t)sb * SLOT + ro;
+                    const T *rt = stage + (int64_t)st * SLOT + ro;
+                    const Vec<T, V> c = ld_stage<T, V>(rc);
+                    const Vec<T, V> so = ld_stage<T, V>(rc - RW);
+                    const Vec<T, V> no = ld_stage<T, V>(rc + RW);
+                    const Vec<T, V> bo = ld_stage<T, V>(rb);
+                    const Vec<T, V> to = ld_stage<T, V>(rt);
+                    const T wl = __shfl_up_sync(0xffffffffu, c.v[V - 1], 1);
+                    const T er = __shfl_down_sync(0xffffffffu, c.v[0], 1);
+                    const T wfirst = lane == 0 ? rc[-1] : wl;      // margin cell x0-1
+                    const T elast = lane == 31 ? rc[V] : er;       // margin cell x0+32V
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const T we = v == 0 ? wfirst : c.v[v - 1];
+                        const T ea = v == V - 1 ? elast : c.v[v + 1];
+                        const T r = update3<T>(c.v[v], we, ea, so.v[v], no.v[v], bo.v[v],
+                                               to.v[v], alpha);
+                        const int64_t i = xi + v;
+                        out.v[v] = (lane_inner || (i != 0 && i < nx - 1)) ? r : T(0);
+                    }
+                }
+                if (xi < nx) store_vec<T, V>(drow + xi, out);
+            }
+            drow += sxy;
+            sb = sc; pb = pc;
+            sc = st; pc = pt;
+            if (++st == kRing) { st = 0; pt ^= 1u; }
+        }
+        tbase += (uint32_t)(pl1 - pl0 + 1);
+        __syncthreads();  // the next item's first copies reuse slots read above
+    }
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of a whole nx*ny*nz field, box (32V+2V) x (kTY+2) x 1.  False if
+// the driver call is unavailable or refuses the map.
+template <typename T>
+bool encode_field_map(CUtensorMap *map, const T *base, int64_t nx, int64_t ny, int64_t nz) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn || nx >= ((int64_t)1 << 32) || ny >= ((int64_t)1 << 32) || nz >= ((int64_t)1 << 31))
+        return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)nx, (cuuint64_t)ny, (cuuint64_t)nz};
+    const cuuint64_t strides[2] = {(cuuint64_t)(nx * (int64_t)sizeof(T)),
+                                   (cuuint64_t)(nx * ny * (int64_t)sizeof(T))};
+    const cuuint32_t box[3] = {(cuuint32_t)row_elems<T>(), (cuuint32_t)kRows, 1};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    const CUresult r = fn(map, sizeof(T) == 8 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT64
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          3, const_cast<T *>(base), dims, strides, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <typename T>
+cudaError_t launch_bulk(const CUtensorMap &src_map, T *dst, int64_t nx, int64_t ny, int64_t nz,
+                        T alpha, cudaStream_t stream) {
+    constexpr int TX = 32 * (16 / sizeof(T));
+    constexpr size_t smem = bulk_smem_bytes<T>();
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, diffuse3d_bulk_kernel<T>,
+                                                          32 * kTY, smem) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = 1;
+        }
+        per_sm = n;
+    }
+    const int64_t tiles_x = (nx + TX - 1) / TX, tiles_y = (ny + kTY - 1) / kTY;
+    const int64_t kz_len = FVF_3D_KZ;  // planes per item
+    const int64_t runs = (nz + kz_len - 1) / kz_len;
+    const int64_t items = tiles_x * tiles_y * runs;
+    const int64_t maxgrid = (int64_t)per_sm * sm_count();
+    const int64_t waves = (items + maxgrid - 1) / maxgrid;
+    const int64_t grid = (items + waves - 1) / waves;  // equal items per block
+    diffuse3d_bulk_kernel<T><<<(unsigned)grid, dim3(32, kTY), smem, stream>>>(
+        src_map, dst, nx, ny, nz, alpha, kz_len, tiles_x, tiles_y, items);
+    return cudaSuccess;
+}
+
+template <typename T, int V>
+cudaError_t launch_typed(const T *src, T *dst, int64_t nx, int64_t ny, int64_t nz, T alpha,
+                         cudaStream_t stream) {
+    const int64_t gx = (nx + 32 * V - 1) / (32 * V);
+    const int64_t gy = (ny + kTY - 1) / kTY;
+    if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
+    // split the planes into runs so that about 8 blocks per SM are in flight
+    const int64_t want = (int64_t)sm_count() * 8;
+    int64_t runs = (want + gx * gy - 1) / (gx * gy);
+    if (runs < 1) runs = 1;
+    int64_t kz_len = (nz + runs - 1) / runs;
+    if (kz_len < 8) kz_len = nz < 8 ? nz : 8;
+    const int64_t gz = (nz + kz_len - 1) / kz_len;
+    if (gz > 65535) return cudaErrorInvalidValue;
+    diffuse3d_kernel<T, V><<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), dim3(32, kTY), 0,
+                             stream>>>(src, dst, nx, ny, nz, alpha, kz_len);
+    return cudaSuccess;
+}
+
+template <typename T>
+cudaError_t launch_steps(T *u, T *v, int64_t nx, int64_t ny, int64_t nz, T alpha, int64_t nsteps,
+                         cudaStream_t stream, uint64_t *launches) {
+    constexpr int VW = 16 / sizeof(T);
+    const bool vec = nx % VW == 0 && (uintptr_t)u % 16 == 0 && (uintptr_t)v % 16 == 0;
+    // tensor maps of both buffers (each is the source of every other step)
+    CUtensorMap map_u, map_v;
+    const bool bulk = FVF_3D_BULK && sizeof(T) == 4 && vec &&
+                      encode_field_map<T>(&map_u, u, nx, ny, nz) &&
+                      encode_field_map<T>(&map_v, v, nx, ny, nz);
+    for (int64_t s = 1; s <= nsteps; ++s) {
+        const T *src = (s & 1) ? u : v;
+        T *dst = (s & 1) ? v : u;
+        cudaError_t e;
+        if (bulk)
+            e = launch_bulk<T>((s & 1) ? map_u : map_v, dst, nx, ny, nz, alpha, stream);
+        else if (vec)
+            e = launch_typed<T, VW>(src, dst, nx, ny, nz, alpha, stream);
+        else
+            e = launch_typed<T, 1>(src, dst, nx, ny, nz, alpha, stream);
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t read_device_error(int *flag) {
+    int zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(flag, g_device_error, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int));
+    return e;
+}
+
+cudaError_t launch_diffuse3d(void *u, void *v, int64_t nx, int64_t ny, int64_t nz, double alpha,
+                             int64_t nsteps, bool fp64, cudaStream_t stream,
+                             uint64_t *launches) {
+    if (fp64)
+        return launch_steps<double>(static_cast<double *>(u), static_cast<double *>(v), nx, ny,
+                                    nz, alpha, nsteps, stream, launches);
+    return launch_steps<float>(static_cast<float *>(u), static_cast<float *>(v), nx, ny, nz,
+                               (float)alpha, nsteps, stream, launches);
+}
+
+}  // namespace fvf

@@ -131,6 +131,30 @@ FVF_API int diffuse2d_step(void *u, void *v, int64_t nx, int64_t ny, double alph
     return cuda_status(e);
 }
 
+FVF_API int diffuse3d_step(void *u, void *v, int64_t nx, int64_t ny, int64_t nz, double alpha,
+                           int64_t nsteps, int dtype, void *stream) {
+    if (dtype != FVF_FP32 && dtype != FVF_FP64) return FVF_ERR_DTYPE;
+    if (nx < 0 || ny < 0 || nz < 0 || nsteps < 0) return FVF_ERR_SIZE;
+    int64_t t = 0, cells = 0;
+    if (!mul_ok(nx, ny, &t) || !mul_ok(t, nz, &cells)) return FVF_ERR_SIZE;
+    if (!std::isfinite(alpha)) return FVF_ERR_ALPHA;
+    if (dtype == FVF_FP32 && !std::isfinite((float)alpha)) return FVF_ERR_ALPHA;
+    if (cells == 0 || nsteps == 0) return FVF_OK;
+    if (!u || !v) return FVF_ERR_NULL;
+    const uint64_t esize = dtype == FVF_FP64 ? 8 : 4;
+    if ((uintptr_t)u % esize || (uintptr_t)v % esize) return FVF_ERR_ALIGN;
+    const uint64_t bytes = (uint64_t)cells * esize;
+    int st = check_device_array(u, bytes);
+    if (st == FVF_OK) st = check_device_array(v, bytes);
+    if (st != FVF_OK) return st;
+    if (overlaps(u, bytes, v, bytes)) return FVF_ERR_ALIAS;
+    uint64_t launched = 0;
+    const cudaError_t e = launch_diffuse3d(u, v, nx, ny, nz, alpha, nsteps, dtype == FVF_FP64,
+                                           (cudaStream_t)stream, &launched);
+    g_launches += launched;
+    return cuda_status(e);
+}
+
 FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int ghost,
                       int dir, double *out, void *stream) {
     if (!extents) return FVF_ERR_NULL;
@@ -486,5 +510,11 @@ FVF_API const char *fvf_status_string(int status) {
 }
 
 FVF_API int fvf_last_cuda_error(void) { return g_last_cuda_error; }
+
+FVF_API int fvf_device_error(int *flag) {
+    if (!flag) return FVF_ERR_NULL;
+    *flag = 0;
+    return cuda_status(read_device_error(flag));
+}
 
 FVF_API uint64_t fvf_launch_count(void) { return g_launches.load(); }

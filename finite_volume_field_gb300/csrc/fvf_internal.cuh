@@ -54,6 +54,14 @@ cudaError_t launch_diffuse2d(void *u, void *v, int64_t nx, int64_t ny, double al
                              int64_t nsteps, bool fp64, cudaStream_t stream,
                              uint64_t *launches);
 
+cudaError_t launch_diffuse3d(void *u, void *v, int64_t nx, int64_t ny, int64_t nz, double alpha,
+                             int64_t nsteps, bool fp64, cudaStream_t stream,
+                             uint64_t *launches);
+
+// Reads and clears the device flag that kernels with bounded waits set when
+// a wait expires (synchronises the device).
+cudaError_t read_device_error(int *flag);
+
 cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
                              double *out, cudaStream_t stream, uint64_t *launches);
 

@@ -1,6 +1,7 @@
 /*
  * fvf.h -- C ABI of libfvf.so, the GB300 (sm_103a) library of per-cell field
- * sweeps: the explicit 2D 5-point diffusion step with ping-pong buffers, the
+ * sweeps: the explicit 2D 5-point and 3D 7-point diffusion steps with
+ * ping-pong buffers, the
  * multi-variable WENO input pack, the finite-volume flux-difference source
  * (assigned or accumulated), the directional flux copy back to the physical
  * frame, the conservative-variable copy (alone or fused with the pack) and
@@ -99,6 +100,28 @@ extern "C" {
  *   Pointers must be aligned to the element size.
  */
 int diffuse2d_step(void *u, void *v, int64_t nx, int64_t ny, double alpha,
+                   int64_t nsteps, int dtype, void *stream);
+
+/*
+ * diffuse3d_step -- nsteps explicit 7-point diffusion steps on a 3D grid with
+ * ping-pong buffers: the 3D variant of [Q] sections 3, 5.1 and 5.4.
+ *
+ *   u, v    two nx*ny*nz arrays of float (FVF_FP32) or double (FVF_FP64),
+ *           column-major: cell (i,j,k) at i + nx*(j + ny*k).  u holds the
+ *           initial field; they must not overlap.
+ *   alpha   diffusion number (FP32: rounded once to float); any finite
+ *           value (stability needs alpha <= 1/6).
+ *   nsteps  >= 0; step s reads u and writes v when s is odd, the reverse when
+ *           s is even.  Each step computes, for every interior cell
+ *           (1 <= i <= nx-2, 1 <= j <= ny-2, 1 <= k <= nz-2),
+ *               dst = c + alpha*((((((W + E) + S) + N) + B) + T) - 6c)
+ *           with W/E = src(i-+1,j,k), S/N = src(i,j-+1,k),
+ *           B/T = src(i,j,k-+1), 6c rounded on its own, and writes 0 to
+ *           every cell of the six boundary faces of dst.
+ *   Result: in v after an odd nsteps, in u after an even one.  Empty grids
+ *   and nsteps = 0 are no-ops.  Pointers must be aligned to the element size.
+ */
+int diffuse3d_step(void *u, void *v, int64_t nx, int64_t ny, int64_t nz, double alpha,
                    int64_t nsteps, int dtype, void *stream);
 
 /*
@@ -260,6 +283,17 @@ const char *fvf_status_string(int status);
 /* The cudaError_t value behind the calling thread's last FVF_ERR_CUDA
  * (0 if none). */
 int fvf_last_cuda_error(void);
+
+/*
+ * fvf_device_error -- reads and clears the device-side error flag of the
+ * current device.  Kernels that wait on their own asynchronous copies
+ * (diffuse3d_step's bulk-copy kernel) bound every wait; if a wait expires the
+ * kernel sets this flag, lets its copies in flight finish (also bounded) and
+ * returns without completing its work, so the results of that launch are
+ * invalid.  *flag is set to the flag's value (0: no expired wait).
+ * Synchronises the device.  Returns FVF_OK, FVF_ERR_NULL or FVF_ERR_CUDA.
+ */
+int fvf_device_error(int *flag);
 
 /* Number of kernels this library has launched since it was loaded (all
  * threads).  Lets a caller count the library's launches in a region. */

@@ -222,3 +222,27 @@ def test_stage_validation(lib):
               None) == C["FVF_ERR_ALIGN"]
     assert st(4096, 4096, fl, w, 2, ext, 0.75, 0.25, float("nan"), 65536, None) == \
         C["FVF_ERR_ALPHA"]
+
+
+def test_diffuse3d_validation(lib):
+    f = lib.diffuse3d_step
+    assert f(4096, 8192, 4, 4, 4, 0.1, 1, 2, None) == C["FVF_ERR_DTYPE"]
+    assert f(4096, 8192, 4, -4, 4, 0.1, 1, 1, None) == C["FVF_ERR_SIZE"]
+    assert f(4096, 8192, 4, 4, 4, 0.1, -1, 1, None) == C["FVF_ERR_SIZE"]
+    assert f(4096, 8192, 1 << 40, 1 << 40, 4, 0.1, 1, 1, None) == C["FVF_ERR_SIZE"]
+    assert f(4096, 8192, 4, 4, 4, float("nan"), 1, 1, None) == C["FVF_ERR_ALPHA"]
+    assert f(4096, 8192, 4, 4, 4, 1e300, 1, 0, None) == C["FVF_ERR_ALPHA"]
+    assert f(None, None, 4, 0, 4, 0.1, 1, 1, None) == C["FVF_OK"]
+    assert f(None, None, 4, 4, 4, 0.1, 0, 1, None) == C["FVF_OK"]
+    assert f(None, 8192, 4, 4, 4, 0.1, 1, 1, None) == C["FVF_ERR_NULL"]
+    assert f(4100, 8192, 4, 4, 4, 0.1, 1, 1, None) == C["FVF_ERR_ALIGN"]
+    assert f(4096, 8192, 4, 4, 4, 0.1, 1, 1, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_device_error_flag_call(lib):
+    """NULL is refused; without a usable GPU the read reports a CUDA error,
+    with one it reads 0 (no kernel has set the flag)."""
+    assert lib.fvf_device_error(None) == C["FVF_ERR_NULL"]
+    flag = ctypes.c_int(7)
+    st = lib.fvf_device_error(ctypes.byref(flag))
+    assert (st, flag.value) in ((C["FVF_ERR_CUDA"], 0), (C["FVF_OK"], 0))

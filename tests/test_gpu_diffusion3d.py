@@ -1,0 +1,143 @@
+"""GPU parity of diffuse3d_step (3D 7-point diffusion, FP32 and FP64) against
+the CPU oracle, through the C ABI.  Both sides evaluate
+c + alpha*((((((W+E)+S)+N)+B)+T) - 6c) with every operation rounded to
+nearest even, so every cell of both buffers must match bit for bit (NaN
+payloads excepted)."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from finite_volume_field_gb300 import api, inputs
+from tests.gpu_util import assert_bits_equal, canary_intact, guarded, to_dev, to_host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+DT = {np.float32: api.FVF_FP32, np.float64: api.FVF_FP64}
+# (nz, ny, nx): 16-byte rows (vector path: nx a multiple of 4 FP32 / 2 FP64) and
+# ragged rows (one element per lane), several tiles along i (32 lanes x 4 or 2) and
+# j (8 rows), several runs of planes along k, and the degenerate sizes.
+SHAPES = [(9, 10, 12), (5, 6, 7), (3, 3, 3), (1, 5, 5), (4, 1, 9), (6, 7, 1), (2, 2, 2),
+          (20, 17, 130), (11, 33, 129), (40, 9, 64), (17, 12, 257), (12, 25, 66)]
+
+
+def _field(shape, dt, seed, zero_edges=True):
+    u = inputs.uniform_f64(seed, 0, int(np.prod(shape))).reshape(shape).astype(dt)
+    if zero_edges:
+        u[0], u[-1] = 0, 0
+        u[:, 0], u[:, -1] = 0, 0
+        u[:, :, 0], u[:, :, -1] = 0, 0
+    return u
+
+
+def _run(torch, u0, steps, alpha=0.1, v0=None):
+    nz, ny, nx = u0.shape
+    n = u0.size
+    tdt = torch.float64 if u0.dtype == np.float64 else torch.float32
+    wu, u = guarded(torch, n, tdt)
+    wv, v = guarded(torch, n, tdt)
+    u.copy_(to_dev(u0.reshape(-1)))
+    v.copy_(to_dev((np.zeros_like(u0) if v0 is None else v0).reshape(-1)))
+    api.diffuse3d_step(u, v, nx, ny, nz, alpha, steps, DT[u0.dtype.type])
+    torch.cuda.synchronize()
+    assert canary_intact(torch, wu, n) and canary_intact(torch, wv, n), "wrote past a buffer"
+    return to_host(u).reshape(u0.shape), to_host(v).reshape(u0.shape)
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float32])
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("steps", [1, 2, 5])
+def test_small_grids(dt, shape, steps):
+    torch = torch_cuda()
+    u0 = _field(shape, dt, 31, zero_edges=False)
+    v0 = _field(shape, dt, 32, zero_edges=False)   # the first step must overwrite v's edges
+    gu, gv = _run(torch, u0, steps, v0=v0)
+    ou, ov, _ = oracle.diffuse3d(u0, steps, 0.1, v0=v0, return_both=True)
+    assert_bits_equal(gu, ou, what=f"u {shape} {steps}")
+    assert_bits_equal(gv, ov, what=f"v {shape} {steps}")
+
+
+@pytest.mark.parametrize("dt", [np.float64, np.float32])
+def test_impulse_and_special_values(dt):
+    """A centre impulse (exact one-step values at alpha = 1/8), then a field
+    with infinities, NaNs, signed zeros and subnormals."""
+    torch = torch_cuda()
+    u0 = np.zeros((9, 10, 12), dtype=dt)
+    u0[4, 5, 6] = 1
+    _, gv = _run(torch, u0, 1, alpha=0.125)
+    assert gv[4, 5, 6] == dt(0.25) and gv[4, 5, 7] == dt(0.125) and gv[3, 5, 6] == dt(0.125)
+    u0 = _field((8, 9, 16), dt, 33)
+    flat = u0.reshape(-1)
+    specials = np.array([np.inf, -np.inf, np.nan, -0.0, 1e-40 if dt == np.float32 else 1e-310,
+                         3e38 if dt == np.float32 else 1.7e308], dtype=dt)
+    flat[::17] = np.resize(specials, flat[::17].size)
+    gu, gv = _run(torch, u0, 3)
+    ou, ov, _ = oracle.diffuse3d(u0, 3, 0.1, return_both=True)
+    assert_bits_equal(gu, ou, nan_payloads=False)
+    assert_bits_equal(gv, ov, nan_payloads=False)
+
+
+def test_misaligned_rows_take_the_scalar_path():
+    """Buffers that start 4 bytes into an allocation (FP32) are not 16-byte
+    aligned: the same results through the one-element-per-lane kernel."""
+    torch = torch_cuda()
+    shape = (7, 9, 64)
+    u0 = _field(shape, np.float32, 34)
+    n = u0.size
+    bu = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
+    bv = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
+    bu[1:] = to_dev(u0.reshape(-1))
+    api.diffuse3d_step(bu[1:], bv[1:], 64, 9, 7, 0.1, 4, api.FVF_FP32)
+    torch.cuda.synchronize()
+    ou = oracle.diffuse3d(u0, 4, 0.1)
+    assert_bits_equal(to_host(bu[1:]).reshape(shape), ou)
+
+
+def test_launch_count_and_errors():
+    torch = torch_cuda()
+    u = torch.zeros(6 * 7 * 8, dtype=torch.float64, device="cuda")
+    v = torch.zeros_like(u)
+    before = api.launch_count()
+    api.diffuse3d_step(u, v, 8, 7, 6, 0.1, 5, api.FVF_FP64)
+    torch.cuda.synchronize()
+    assert api.launch_count() - before == 5
+    with pytest.raises(api.FvfError) as e:
+        api.diffuse3d_step(u, u[8:], 8, 7, 5, 0.1, 1, api.FVF_FP64)
+    assert e.value.status == 6
+    # a grid far larger than the 336-element buffers (torch's caching
+    # allocator may hand out a larger block than asked for, but not 8 GiB)
+    with pytest.raises(api.FvfError) as e:
+        api.diffuse3d_step(u, v, 1024, 1024, 1024, 0.1, 1, api.FVF_FP64)
+    assert e.value.status == 10
+
+
+@pytest.mark.parametrize("dt", [np.float32, np.float64])
+def test_full_size_512_cubed_20_steps(dt):
+    """512^3, 20 steps, interior uniform [0,1) with zero boundary faces: both
+    buffers compared cell by cell with the oracle (run on all host cores)."""
+    torch = torch_cuda()
+    shape = (512, 512, 512)
+    u0 = _field(shape, dt, 35)
+    du = to_dev(u0.reshape(-1))
+    dv = torch.zeros_like(du)
+    api.diffuse3d_step(du, dv, 512, 512, 512, 0.1, 20, DT[dt])
+    torch.cuda.synchronize()
+    ou, ov, _ = oracle.diffuse3d(u0, 20, 0.1, nthreads=os.cpu_count() or 1, return_both=True)
+    assert_bits_equal(to_host(du).reshape(shape), ou, what="512^3 u")
+    assert_bits_equal(to_host(dv).reshape(shape), ov, what="512^3 v")
+
+
+def test_no_expired_waits():
+    """The bulk-copy kernel bounds its waits on its own copies and flags an
+    expired one on the device; after the runs above and a few more the flag
+    is clear."""
+    torch = torch_cuda()
+    for shape in ((40, 33, 256), (70, 9, 64)):
+        for dt in (np.float32, np.float64):
+            u0 = _field(shape, dt, 36)
+            gu, gv = _run(torch, u0, 3)
+            assert_bits_equal(gv, oracle.diffuse3d(u0, 3, 0.1))
+    assert api.device_error() == 0
