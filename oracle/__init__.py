@@ -83,6 +83,10 @@ def _load():
     lib.oracle_rk_axpby.argtypes = [vp, vp, vp, i64, ctypes.c_double, ctypes.c_double,
                                     ctypes.c_double, vp]
     lib.oracle_rk_axpby.restype = cint
+    lib.oracle_weno_pack_f32.argtypes = [ctypes.POINTER(vp), cint, i64, i64, i64, i64, cint, vp]
+    lib.oracle_weno_pack_f32.restype = cint
+    lib.oracle_advect_rhs_f32.argtypes = [vp, vp, cint, i64, i64, i64, cint, cint, vp]
+    lib.oracle_advect_rhs_f32.restype = cint
     lib.oracle_max_threads.argtypes = []
     lib.oracle_max_threads.restype = cint
     _lib = lib
@@ -195,40 +199,58 @@ def flux_extents(extents, direction):
 def weno_pack(fields, extents, ghost: int, direction: int) -> np.ndarray:
     """The WENO input pack (MFC pull request #2087, "Changes").
 
-    ``fields`` is a list of nv float64 arrays, each holding the stored box in
-    Fortran order (element (j,k,l) at j + N1*(k + N2*l)); any shape with that
-    many elements is accepted.  Returns a flat float64 array of
-    M1*M2*M3*nv elements laid out as described in ``fvf_oracle.c``.
+    ``fields`` is a list of nv arrays, all float64 or all float32 (the FP32
+    form, a 4-byte copy), each holding the stored box in Fortran order
+    (element (j,k,l) at j + N1*(k + N2*l)); any shape with that many elements
+    is accepted, other dtypes are converted to float64.  Returns a flat array
+    of M1*M2*M3*nv elements of the fields' dtype, laid out as described in
+    ``fvf_oracle.c``.
     """
     n1, n2, n3 = (int(x) for x in extents)
     nst = int(np.prod(stored_extents(extents, ghost)))
+    f32 = len(fields) > 0 and all(np.asarray(f).dtype == np.float32 for f in fields)
+    dt = np.float32 if f32 else np.float64
     arrs = []
     for f in fields:
-        a = np.ascontiguousarray(f, dtype=np.float64).reshape(-1)
+        a = np.ascontiguousarray(f, dtype=dt).reshape(-1)
         if a.size != nst:
             raise ValueError(f"field has {a.size} elements, expected {nst}")
         arrs.append(a)
     nv = len(arrs)
-    out = np.empty(int(np.prod(pack_extents(extents, ghost, direction))) * nv, dtype=np.float64)
-    table = (ctypes.c_void_p * nv)(*[_ptr(a) for a in arrs])
-    rc = _load().oracle_weno_pack(table, nv, n1, n2, n3, int(ghost), int(direction), _ptr(out))
+    out = np.empty(int(np.prod(pack_extents(extents, ghost, direction))) * nv, dtype=dt)
+    table = (ctypes.c_void_p * max(1, nv))(*[_ptr(a) for a in arrs])
+    fn = _load().oracle_weno_pack_f32 if f32 else _load().oracle_weno_pack
+    rc = fn(table, nv, n1, n2, n3, int(ghost), int(direction), _ptr(out))
     if rc != 0:
         raise ValueError("bad direction")
     return out
 
 
-def advect_rhs(flux: np.ndarray, inv_d: np.ndarray, nv: int, extents, direction: int) -> np.ndarray:
-    """The flux-difference source (MFC pull request #2087, "Changes",
-    s_compute_advection_source_term); layout as in ``fvf_oracle.c``."""
+def _flux_args(flux, inv_d, nv, extents, direction):
     n1, n2, n3 = (int(x) for x in extents)
-    fl = np.ascontiguousarray(flux, dtype=np.float64).reshape(-1)
-    w = np.ascontiguousarray(inv_d, dtype=np.float64).reshape(-1)
+    f32 = np.asarray(flux).dtype == np.float32
+    dt = np.float32 if f32 else np.float64
+    fl = np.ascontiguousarray(flux, dtype=dt).reshape(-1)
+    w = np.ascontiguousarray(inv_d, dtype=dt).reshape(-1)
     if fl.size != int(np.prod(flux_extents(extents, direction))) * nv:
         raise ValueError("flux size mismatch")
     if w.size != (n1, n2, n3)[direction]:
         raise ValueError("inv_d size mismatch")
-    rhs = np.empty(n1 * n2 * n3 * nv, dtype=np.float64)
-    rc = _load().oracle_advect_rhs(_ptr(fl), _ptr(w), int(nv), n1, n2, n3, int(direction), _ptr(rhs))
+    return n1, n2, n3, f32, dt, fl, w
+
+
+def advect_rhs(flux: np.ndarray, inv_d: np.ndarray, nv: int, extents, direction: int) -> np.ndarray:
+    """The flux-difference source (MFC pull request #2087, "Changes",
+    s_compute_advection_source_term); layout as in ``fvf_oracle.c``.  A
+    float32 flux selects the FP32 form (inv_d converted to float32)."""
+    n1, n2, n3, f32, dt, fl, w = _flux_args(flux, inv_d, nv, extents, direction)
+    rhs = np.empty(n1 * n2 * n3 * nv, dtype=dt)
+    if f32:
+        rc = _load().oracle_advect_rhs_f32(_ptr(fl), _ptr(w), int(nv), n1, n2, n3,
+                                           int(direction), 0, _ptr(rhs))
+    else:
+        rc = _load().oracle_advect_rhs(_ptr(fl), _ptr(w), int(nv), n1, n2, n3, int(direction),
+                                       _ptr(rhs))
     if rc != 0:
         raise ValueError("bad direction")
     return rhs
@@ -238,15 +260,17 @@ def advect_rhs_add(flux: np.ndarray, inv_d: np.ndarray, nv: int, extents, direct
                    rhs: np.ndarray) -> np.ndarray:
     """rhs + the flux-difference term of ``direction`` (returns a new array):
     the accumulating form that builds the finite-volume right-hand side over
-    the directions."""
-    n1, n2, n3 = (int(x) for x in extents)
-    fl = np.ascontiguousarray(flux, dtype=np.float64).reshape(-1)
-    w = np.ascontiguousarray(inv_d, dtype=np.float64).reshape(-1)
-    out = np.array(rhs, dtype=np.float64, copy=True).reshape(-1)
-    if fl.size != int(np.prod(flux_extents(extents, direction))) * nv or out.size != n1 * n2 * n3 * nv:
+    the directions.  A float32 flux selects the FP32 form."""
+    n1, n2, n3, f32, dt, fl, w = _flux_args(flux, inv_d, nv, extents, direction)
+    out = np.array(rhs, dtype=dt, copy=True).reshape(-1)
+    if out.size != n1 * n2 * n3 * nv:
         raise ValueError("size mismatch")
-    rc = _load().oracle_advect_rhs_add(_ptr(fl), _ptr(w), int(nv), n1, n2, n3, int(direction),
-                                       _ptr(out))
+    if f32:
+        rc = _load().oracle_advect_rhs_f32(_ptr(fl), _ptr(w), int(nv), n1, n2, n3,
+                                           int(direction), 1, _ptr(out))
+    else:
+        rc = _load().oracle_advect_rhs_add(_ptr(fl), _ptr(w), int(nv), n1, n2, n3,
+                                           int(direction), _ptr(out))
     if rc != 0:
         raise ValueError("bad direction")
     return out

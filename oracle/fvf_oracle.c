@@ -418,6 +418,86 @@ int oracle_flux_unpack(const double *in, int nv, int64_t n1, int64_t n2, int64_t
 }
 
 /*
+ * FP32 forms of the pack and of the flux difference ([Q] section 6 compares
+ * FP32 with FP64 throughout; the same sweeps on binary32 data).  The pack is
+ * the same element mapping as oracle_weno_pack, as a 4-byte copy.  The flux
+ * difference forms inv_d(c) * (F(c-1) - F(c)) in binary32 arithmetic (one
+ * rounded subtraction, one rounded multiplication) and assigns it, or with
+ * accumulate != 0 adds it once to the existing rhs, as oracle_advect_rhs and
+ * oracle_advect_rhs_add do in binary64.
+ */
+int oracle_weno_pack_f32(const float *const *fields, int nv, int64_t n1, int64_t n2,
+                         int64_t n3, int64_t g, int dir, float *out)
+{
+    const int64_t N1 = stored_extent(n1, g), N2 = stored_extent(n2, g);
+    const int64_t N3 = stored_extent(n3, g);
+    const int64_t g1 = ghost_offset(n1, g), g2 = ghost_offset(n2, g);
+    const int64_t g3 = ghost_offset(n3, g);
+    int64_t M1, M2, M3;
+    (void)N3;
+    if (dir == 0) {
+        M1 = N1; M2 = n2; M3 = n3;
+    } else if (dir == 1) {
+        M1 = N2; M2 = n1; M3 = n3;
+    } else if (dir == 2) {
+        M1 = N3; M2 = n2; M3 = n1;
+    } else {
+        return -1;
+    }
+    for (int i = 0; i < nv; ++i) {
+        const float *f = fields[i];
+        for (int64_t c = 0; c < M3; ++c) {
+            for (int64_t b = 0; b < M2; ++b) {
+                for (int64_t a = 0; a < M1; ++a) {
+                    int64_t j, k, l;
+                    if (dir == 0) {
+                        j = a; k = b + g2; l = c + g3;
+                    } else if (dir == 1) {
+                        j = b + g1; k = a; l = c + g3;
+                    } else {
+                        j = c + g1; k = b + g2; l = a;
+                    }
+                    out[a + M1 * (b + M2 * (c + M3 * (int64_t)i))] =
+                        f[j + N1 * (k + N2 * l)];
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_advect_rhs_f32(const float *flux, const float *inv_d, int nv, int64_t n1,
+                          int64_t n2, int64_t n3, int dir, int accumulate, float *rhs)
+{
+    int64_t F1 = n1, F2 = n2, F3 = n3;
+    if (dir == 0)
+        F1 = n1 + 1;
+    else if (dir == 1)
+        F2 = n2 + 1;
+    else if (dir == 2)
+        F3 = n3 + 1;
+    else
+        return -1;
+    for (int i = 0; i < nv; ++i) {
+        for (int64_t l = 0; l < n3; ++l) {
+            for (int64_t k = 0; k < n2; ++k) {
+                for (int64_t j = 0; j < n1; ++j) {
+                    const int64_t c = dir == 0 ? j : (dir == 1 ? k : l);
+                    const int64_t sj = dir == 0, sk = dir == 1, sl = dir == 2;
+                    const float lo = flux[j + F1 * (k + F2 * (l + F3 * (int64_t)i))];
+                    const float hi =
+                        flux[(j + sj) + F1 * ((k + sk) + F2 * ((l + sl) + F3 * (int64_t)i))];
+                    const float term = inv_d[c] * (lo - hi);
+                    float *r = &rhs[j + n1 * (k + n2 * (l + n3 * (int64_t)i))];
+                    *r = accumulate ? *r + term : term;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/*
  * The conservative-variable copy of [M] "Changes" (s_compute_rhs): field i
  * copied element by element, the whole stored box (ghost cells included),
  * into dst_i.  Returns 0.

@@ -43,7 +43,8 @@ def _mutant(tmp_path, old: str, new: str, count: int = 1):
     for name in ("oracle_diffuse2d_f64", "oracle_diffuse2d_f32", "oracle_diffuse3d_f64",
                  "oracle_diffuse3d_f32", "oracle_weno_pack",
                  "oracle_advect_rhs", "oracle_advect_rhs_add", "oracle_flux_unpack",
-                 "oracle_fields_copy", "oracle_rk_axpby", "oracle_max_threads"):
+                 "oracle_fields_copy", "oracle_rk_axpby", "oracle_weno_pack_f32",
+                 "oracle_advect_rhs_f32", "oracle_max_threads"):
         getattr(lib, name).argtypes = getattr(real, name).argtypes
         getattr(lib, name).restype = getattr(real, name).restype
     oracle._lib = lib
@@ -126,6 +127,12 @@ MUTANTS = [
      STENCIL3D_32,
      STENCIL3D_32.replace("src[c - 1] + src[c + 1] + src[c - nx]", "src[c - 1] + (src[c + 1] + src[c - nx])"),
      1, lambda: D3.test_summation_order_fp32_worked_value()),
+    ("pack-f32-wrong-variable",
+     "const float *f = fields[i];", "const float *f = fields[0];",
+     1, lambda: P.test_pack_f32_coordinate_tags(1)),
+    ("rhs-f32-faces-swapped",
+     "const float term = inv_d[c] * (lo - hi);", "const float term = inv_d[c] * (hi - lo);",
+     1, lambda: P.test_rhs_f32_linear_and_constant_flux(2)),
     ("stage-coefficients-swapped",
      "const double p = a * u0[e];\n        const double q = b * t;",
      "const double p = b * u0[e];\n        const double q = a * t;",

@@ -353,3 +353,87 @@ def test_pack_copy_is_pack_and_copy():
         packed, copies = oracle.weno_pack_copy(fields, extents, g, direction)
         assert np.array_equal(packed, _numpy_pack(fields, extents, g, direction))
         assert all(np.array_equal(a, b) for a, b in zip(copies, fields))
+
+
+# ---------------------------------------------------------------------------
+# FP32 forms of the pack and of the flux difference
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_pack_f32_coordinate_tags(direction):
+    """FP32 fields carrying their own (i, j, k, l) as exact binary32 integers
+    (below 2^24): the FP32 pack must place them as the mapping states."""
+    extents, g = (4, 5, 6), 2
+    N1, N2, N3 = inputs.stored_extents(extents, g)
+    nv = 3
+    fields = []
+    for i in range(nv):
+        l, k, j = np.meshgrid(np.arange(N3), np.arange(N2), np.arange(N1), indexing="ij")
+        fields.append((i * 100000 + j * 1000 + k * 32 + l).astype(np.float32).reshape(-1))
+    out = oracle.weno_pack(fields, extents, g, direction)
+    assert out.dtype == np.float32
+    M1, M2, M3 = oracle.pack_extents(extents, g, direction)
+    for i, c, b, a in itertools.product(range(nv), range(M3), range(M2), range(M1)):
+        val = int(out[a + M1 * (b + M2 * (c + M3 * i))])
+        ti, r = divmod(val, 100000)
+        tj, r = divmod(r, 1000)
+        tk, tl = divmod(r, 32)
+        want = [(a, b + g, c + g), (b + g, a, c + g), (c + g, b + g, a)][direction]
+        assert (ti, tj, tk, tl) == (i,) + want
+
+
+def test_pack_f32_is_the_fp64_pack_of_the_same_values():
+    """Widening binary32 to binary64 is exact, so packing in FP32 then
+    widening equals widening then packing in FP64 (NaN payloads aside, the
+    values are random normals here)."""
+    extents, g = (7, 6, 5), 3
+    fields = inputs.normal_fields(12, 4, extents, g)
+    f32 = [f.astype(np.float32) for f in fields]
+    for direction in range(3):
+        a = oracle.weno_pack(f32, extents, g, direction).astype(np.float64)
+        b = oracle.weno_pack([f.astype(np.float64) for f in f32], extents, g, direction)
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+def test_rhs_f32_linear_and_constant_flux(direction):
+    """FP32: F(f) = f gives exactly -inv_d; a constant flux gives +0."""
+    extents, nv = (4, 5, 6), 2
+    F1, F2, F3 = oracle.flux_extents(extents, direction)
+    l, k, j = np.meshgrid(np.arange(F3), np.arange(F2), np.arange(F1), indexing="ij")
+    pos = ((j, k, l)[direction] - 1.0).astype(np.float32)
+    F = np.tile(pos.reshape(-1), nv)
+    inv_d = inputs.inverse_spacing(5, extents[direction]).astype(np.float32)
+    rhs = oracle.advect_rhs(F, inv_d, nv, extents, direction)
+    assert rhs.dtype == np.float32
+    n1, n2, n3 = extents
+    R = rhs.reshape(nv, n3, n2, n1)
+    shape = [1, 1, 1, 1]
+    shape[3 - direction] = -1
+    assert np.array_equal(R, np.broadcast_to(-inv_d.reshape(shape), R.shape))
+    const = oracle.advect_rhs(np.full_like(F, np.float32(2.5)), inv_d, nv, extents, direction)
+    assert np.all(const == 0) and not np.signbit(const).any()
+
+
+def test_rhs_f32_is_the_rounded_exact_value():
+    """For binary32 inputs of moderate range the difference and the product
+    are exact in binary64, so each FP32 operation equals the binary64 result
+    rounded once to binary32: the FP32 term must be
+    f32(f64(w) * f64(f32(f64(lo) - f64(hi)))), assigned or added."""
+    extents, nv = (9, 8, 7), 3
+    for direction in range(3):
+        flux = inputs.face_fluxes(13, nv, extents, direction).astype(np.float32)
+        w = inputs.inverse_spacing(13, extents[direction], stream=200 + direction).astype(np.float32)
+        F = flux.reshape((nv,) + tuple(oracle.flux_extents(extents, direction))[::-1])
+        lo = np.take(F, np.arange(extents[direction]), axis=3 - direction).astype(np.float64)
+        hi = np.take(F, np.arange(1, extents[direction] + 1), axis=3 - direction).astype(np.float64)
+        shape = [1, 1, 1, 1]
+        shape[3 - direction] = -1
+        diff = (lo - hi).astype(np.float32).astype(np.float64)
+        term = (w.astype(np.float64).reshape(shape) * diff).astype(np.float32)
+        got = oracle.advect_rhs(flux, w, nv, extents, direction)
+        assert np.array_equal(got, term.reshape(-1))
+        base = inputs.normal_f64(14, direction, got.size).astype(np.float32)
+        acc = oracle.advect_rhs_add(flux, w, nv, extents, direction, base)
+        want = (base.astype(np.float64) + term.reshape(-1).astype(np.float64)).astype(np.float32)
+        assert np.array_equal(acc, want)
