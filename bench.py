@@ -492,7 +492,8 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     the physical frame on the 8 x 201^3 flux workload's buffers, the
     conservative-variable copy alone and fused with the pack on the 8 x 207^3
     pack workload's fields, the SSPRK3 stage update (fused with the flux
-    difference, alone, and unfused) on the flux workload, the 3D 7-point
+    difference, alone, and unfused) on the flux workload, the FP32 pack and
+    flux difference on the same workloads, the 3D 7-point
     diffusion (512^3, 20 steps, FP32 and FP64; 10 FP64 operations per interior
     cell counting 6c) and the latency of the 64 x 64 FP64 diffusion case.  Stage rows count the bytes of the fused
     form (the unfused row's extra rhs traffic is its cost) and 13 FP64
@@ -580,6 +581,24 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
         api.ssprk3_axpby(u0, u, rhs, RHS_NV, RHS_EXT, a, b, dt, uo, stream)
     record("ssprk3_stage_unfused_xyz", stage_unfused, face_bytes + 24 * cells, cells, 13)
     del u0, u, uo
+    # FP32 pack (8 x 207^3) and FP32 flux difference (8 x 201^3)
+    f32f = [f.float() for f in sw.pack_fields]
+    pout = torch.empty(sw.pack_out[0].numel(), dtype=torch.float32, device=sw.dev)
+    for k, ax in enumerate("xyz"):
+        npk = _prod(pack_extents(PACK_EXT, PACK_G, k)) * PACK_NV
+        record(f"pack_f32_{ax}",
+               lambda k=k: api.weno_pack_f32(f32f, PACK_NV, PACK_EXT, PACK_G, k, pout, stream),
+               8 * npk, npk)
+    del f32f, pout
+    r32 = torch.empty(cells, dtype=torch.float32, device=sw.dev)
+    for k, ax in enumerate("xyz"):
+        fl32, w32 = sw.rhs_flux[k].float(), sw.rhs_invd[k].float()
+        record(f"rhs_f32_{ax}",
+               lambda fl32=fl32, w32=w32, k=k: api.advect_rhs_f32(fl32, w32, RHS_NV, RHS_EXT, k,
+                                                                  r32, stream),
+               4 * (fl32.numel() + cells + RHS_EXT[k]), cells)
+        del fl32, w32
+    del r32
     # 3D 7-point diffusion, 512^3, 20 steps per call, FP32 and FP64
     n3 = 512
     cells3 = n3 ** 3

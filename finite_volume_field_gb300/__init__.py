@@ -11,10 +11,13 @@ use and raise if it is missing.  ``inputs`` holds the seeded synthetic input
 generators.
 """
 from .api import (FVF_FP32, FVF_FP64, MAX_NV, FvfError, advect_rhs, advect_rhs_add,
-                  device_error, diffuse2d_step, diffuse3d_step, fields_copy, flux_unpack, last_cuda_error, launch_count, load,
-                  ssprk3_axpby, ssprk3_stage, status_string, weno_pack, weno_pack_copy)
+                  advect_rhs_add_f32, advect_rhs_f32, device_error, diffuse2d_step,
+                  diffuse3d_step, fields_copy, flux_unpack, last_cuda_error, launch_count, load,
+                  ssprk3_axpby, ssprk3_stage, status_string, weno_pack, weno_pack_copy,
+                  weno_pack_f32)
 
 __all__ = ["FVF_FP32", "FVF_FP64", "MAX_NV", "FvfError", "advect_rhs", "advect_rhs_add",
-           "device_error", "diffuse2d_step", "diffuse3d_step", "fields_copy", "flux_unpack", "last_cuda_error", "launch_count",
+           "advect_rhs_add_f32", "advect_rhs_f32", "device_error", "diffuse2d_step",
+           "diffuse3d_step", "fields_copy", "flux_unpack", "last_cuda_error", "launch_count",
            "load", "ssprk3_axpby", "ssprk3_stage", "status_string", "weno_pack",
-           "weno_pack_copy"]
+           "weno_pack_copy", "weno_pack_f32"]

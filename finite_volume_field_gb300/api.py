@@ -49,6 +49,12 @@ def load() -> ctypes.CDLL:
     lib.diffuse3d_step.restype = cint
     lib.weno_pack.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint, cint, vp, vp]
     lib.weno_pack.restype = cint
+    lib.weno_pack_f32.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint, cint, vp,
+                                  vp]
+    lib.weno_pack_f32.restype = cint
+    for name in ("advect_rhs_f32", "advect_rhs_add_f32"):
+        getattr(lib, name).argtypes = [vp, vp, cint, ctypes.POINTER(i64), cint, vp, vp]
+        getattr(lib, name).restype = cint
     lib.advect_rhs.argtypes = [vp, vp, cint, ctypes.POINTER(i64), cint, vp, vp]
     lib.advect_rhs.restype = cint
     lib.advect_rhs_add.argtypes = [vp, vp, cint, ctypes.POINTER(i64), cint, vp, vp]
@@ -186,6 +192,36 @@ def weno_pack(fields, nv: int, extents, ghost: int, dir: int, out, stream=None) 
     st = load().weno_pack(table if ptrs else None, int(nv), _extents(extents), int(ghost),
                           int(dir), _addr(out, torch.float64, "out"), _stream(stream))
     _check("weno_pack", st)
+
+
+def weno_pack_f32(fields, nv: int, extents, ghost: int, dir: int, out, stream=None) -> None:
+    """Enqueue the WENO input pack of ``nv`` FP32 fields along ``dir``."""
+    import torch
+    ptrs = [_addr(f, torch.float32, f"fields[{i}]") for i, f in enumerate(list(fields)[:nv])]
+    table = (ctypes.c_void_p * max(1, len(ptrs)))(*ptrs)
+    st = load().weno_pack_f32(table if ptrs else None, int(nv), _extents(extents), int(ghost),
+                              int(dir), _addr(out, torch.float32, "out"), _stream(stream))
+    _check("weno_pack_f32", st)
+
+
+def advect_rhs_f32(flux, inv_d, nv: int, extents, dir: int, rhs, stream=None) -> None:
+    """Enqueue the FP32 flux-difference source along ``dir``."""
+    import torch
+    f32 = torch.float32
+    st = load().advect_rhs_f32(_addr(flux, f32, "flux"), _addr(inv_d, f32, "inv_d"), int(nv),
+                               _extents(extents), int(dir), _addr(rhs, f32, "rhs"),
+                               _stream(stream))
+    _check("advect_rhs_f32", st)
+
+
+def advect_rhs_add_f32(flux, inv_d, nv: int, extents, dir: int, rhs, stream=None) -> None:
+    """Enqueue rhs += the FP32 flux-difference term along ``dir``."""
+    import torch
+    f32 = torch.float32
+    st = load().advect_rhs_add_f32(_addr(flux, f32, "flux"), _addr(inv_d, f32, "inv_d"), int(nv),
+                                   _extents(extents), int(dir), _addr(rhs, f32, "rhs"),
+                                   _stream(stream))
+    _check("advect_rhs_add_f32", st)
 
 
 def advect_rhs(flux, inv_d, nv: int, extents, dir: int, rhs, stream=None) -> None:

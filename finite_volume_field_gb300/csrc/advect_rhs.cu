@@ -5,7 +5,8 @@
 // s_compute_advection_source_term, x/y/z flux differences):
 //     rhs(j,k,l,i) = inv_d(c) * (F(c-1) - F(c))
 // along the swept axis c, one subtraction then one multiplication, each
-// rounded to nearest even (round-to-nearest intrinsics, never contracted).
+// rounded to nearest even (round-to-nearest intrinsics, never contracted), in
+// binary64 or, for the FP32 entry points, binary32.
 // Two FP64 operations per element keep this kernel on GB300's FP64 unit:
 // moving the subtraction to the integer pipes (fp64_emu.cuh) was measured
 // slower here (the integer ALU pipe saturates first), unlike in the
@@ -38,15 +39,23 @@ __device__ __forceinline__ double face_diff(double lo, double hi) {
     return __dsub_rn(lo, hi);
 }
 
+// FP32 form: binary32 operations, each rounded to nearest even.
+template <int Q>
+__device__ __forceinline__ float face_diff(float lo, float hi) { return __fsub_rn(lo, hi); }
+__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
+__device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
+
 // F extents per variable (F1, F2, F3); the high face of a cell is `step`
 // elements after its low face (1, F1 or F1*F2).  One thread per cell (j, k)
 // of a plane l, the (j, k) pairs flattened over the block so that every lane
 // has a cell whatever n1 is: the kernel is bound by the FP64 unit, which
 // charges idle lanes.
-template <int DIR, bool ACC, typename Idx>
+template <int DIR, bool ACC, typename Idx, typename T>
 __global__ void __launch_bounds__(kThreads)
-advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ inv_d, int nv,
-                  int64_t n1_, int64_t n2_, int64_t n3, double *__restrict__ rhs) {
+advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int nv,
+                  int64_t n1_, int64_t n2_, int64_t n3, T *__restrict__ rhs) {
     const Idx n1 = (Idx)n1_, n2 = (Idx)n2_;
     const Idx plane = n1 * n2;
     const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
@@ -58,14 +67,14 @@ advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ in
     const int64_t fplane = F1 * F2 * F3;
     const int64_t rplane = (int64_t)plane * n3;
     const int64_t step = DIR == 0 ? 1 : (DIR == 1 ? F1 : F1 * F2);
-    const double wjk = DIR == 0 ? __ldg(inv_d + j) : (DIR == 1 ? __ldg(inv_d + k) : 0.0);
+    const T wjk = DIR == 0 ? __ldg(inv_d + j) : (DIR == 1 ? __ldg(inv_d + k) : T(0));
     for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
-        const double w = DIR == 2 ? __ldg(inv_d + l) : wjk;
+        const T w = DIR == 2 ? __ldg(inv_d + l) : wjk;
         const int64_t lo = (int64_t)j + F1 * ((int64_t)k + F2 * l);  // face c-1 at position c
-        const double *f = flux + lo;
-        double *r = rhs + (int64_t)jk + (int64_t)plane * l;
+        const T *f = flux + lo;
+        T *r = rhs + (int64_t)jk + (int64_t)plane * l;
         for (int i0 = 0; i0 < nv; i0 += kGroup) {
-            double a[kGroup], b[kGroup], old[kGroup];
+            T a[kGroup], b[kGroup], old[kGroup];
 #pragma unroll
             for (int q = 0; q < kGroup; ++q) {
                 if (i0 + q < nv) {
@@ -77,9 +86,9 @@ advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ in
             }
 #define FVF_RHS_Q(Q)                                                                    \
     if (i0 + Q < nv) {                                                                  \
-        const double term = __dmul_rn(w, face_diff<Q>(a[Q], b[Q]));                     \
+        const T term = mul_rn(w, face_diff<Q>(a[Q], b[Q]));                            \
         /* accumulate form: the term added once to the existing rhs */                 \
-        r[(int64_t)(i0 + Q) * rplane] = ACC ? __dadd_rn(old[Q], term) : term;          \
+        r[(int64_t)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;             \
     }
             FVF_RHS_Q(0)
             FVF_RHS_Q(1)
@@ -90,28 +99,24 @@ advect_rhs_kernel(const double *__restrict__ flux, const double *__restrict__ in
     }
 }
 
-template <int DIR, bool ACC>
-void launch_typed(const double *flux, const double *inv_d, int nv, const int64_t n[3],
-                  double *rhs, cudaStream_t stream) {
+template <int DIR, bool ACC, typename T>
+void launch_typed(const T *flux, const T *inv_d, int nv, const int64_t n[3], T *rhs,
+                  cudaStream_t stream) {
     const int64_t plane = n[0] * n[1];
     const dim3 grid((unsigned)((plane + kThreads - 1) / kThreads),
                     (unsigned)(n[2] < 65535 ? n[2] : 65535));
     // 32-bit (j, k) arithmetic while the plane index fits
     if (plane + kThreads < ((int64_t)1 << 31))
-        advect_rhs_kernel<DIR, ACC, uint32_t><<<grid, kThreads, 0, stream>>>(
+        advect_rhs_kernel<DIR, ACC, uint32_t, T><<<grid, kThreads, 0, stream>>>(
             flux, inv_d, nv, n[0], n[1], n[2], rhs);
     else
-        advect_rhs_kernel<DIR, ACC, int64_t><<<grid, kThreads, 0, stream>>>(
+        advect_rhs_kernel<DIR, ACC, int64_t, T><<<grid, kThreads, 0, stream>>>(
             flux, inv_d, nv, n[0], n[1], n[2], rhs);
 }
 
-}  // namespace
-
-cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
-                              const int64_t n[3], int dir, bool accumulate, double *rhs,
-                              cudaStream_t stream, uint64_t *launches) {
-    const int64_t gx = (n[0] * n[1] + kThreads - 1) / kThreads;
-    if (gx > 0x7fffffff) return cudaErrorInvalidValue;
+template <typename T>
+void launch_dir(const T *flux, const T *inv_d, int nv, const int64_t n[3], int dir,
+                bool accumulate, T *rhs, cudaStream_t stream) {
     if (dir == 0) {
         if (accumulate) launch_typed<0, true>(flux, inv_d, nv, n, rhs, stream);
         else launch_typed<0, false>(flux, inv_d, nv, n, rhs, stream);
@@ -122,6 +127,21 @@ cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
         if (accumulate) launch_typed<2, true>(flux, inv_d, nv, n, rhs, stream);
         else launch_typed<2, false>(flux, inv_d, nv, n, rhs, stream);
     }
+}
+
+}  // namespace
+
+cudaError_t launch_advect_rhs(const void *flux, const void *inv_d, int nv, const int64_t n[3],
+                              int dir, bool accumulate, bool fp32, void *rhs,
+                              cudaStream_t stream, uint64_t *launches) {
+    const int64_t gx = (n[0] * n[1] + kThreads - 1) / kThreads;
+    if (gx > 0x7fffffff) return cudaErrorInvalidValue;
+    if (fp32)
+        launch_dir<float>(static_cast<const float *>(flux), static_cast<const float *>(inv_d), nv,
+                          n, dir, accumulate, static_cast<float *>(rhs), stream);
+    else
+        launch_dir<double>(static_cast<const double *>(flux), static_cast<const double *>(inv_d),
+                           nv, n, dir, accumulate, static_cast<double *>(rhs), stream);
     ++*launches;
     return cudaGetLastError();
 }

@@ -155,8 +155,9 @@ FVF_API int diffuse3d_step(void *u, void *v, int64_t nx, int64_t ny, int64_t nz,
     return cuda_status(e);
 }
 
-FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int ghost,
-                      int dir, double *out, void *stream) {
+// Shared validation and launch of weno_pack (FP64) and weno_pack_f32.
+static int weno_pack_impl(const void *const *fields, int nv, const int64_t extents[3], int ghost,
+                          int dir, void *out, bool fp32, void *stream) {
     if (!extents) return FVF_ERR_NULL;
     if (dir < 0 || dir > 2) return FVF_ERR_DIR;
     if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
@@ -178,13 +179,14 @@ FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents
         return FVF_ERR_SIZE;
     if (elems_out == 0) return FVF_OK;
     if (!fields || !out) return FVF_ERR_NULL;
-    if ((uintptr_t)out % 8) return FVF_ERR_ALIGN;
-    const uint64_t out_bytes = (uint64_t)elems_out * 8, in_bytes = (uint64_t)stored * 8;
+    const uint64_t esize = fp32 ? 4 : 8;
+    if ((uintptr_t)out % esize) return FVF_ERR_ALIGN;
+    const uint64_t out_bytes = (uint64_t)elems_out * esize, in_bytes = (uint64_t)stored * esize;
     FieldTable table;
     std::memset(&table, 0, sizeof(table));
     for (int i = 0; i < nv; ++i) {
         if (!fields[i]) return FVF_ERR_NULL;
-        if ((uintptr_t)fields[i] % 8) return FVF_ERR_ALIGN;
+        if ((uintptr_t)fields[i] % esize) return FVF_ERR_ALIGN;
         table.p[i] = fields[i];
     }
     int st = check_device_array(out, out_bytes);
@@ -193,9 +195,22 @@ FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents
     for (int i = 0; i < nv; ++i)
         if (overlaps(fields[i], in_bytes, out, out_bytes)) return FVF_ERR_ALIAS;
     uint64_t launched = 0;
-    const cudaError_t e = launch_weno_pack(table, nv, box, dir, out, (cudaStream_t)stream, &launched);
+    const cudaError_t e =
+        launch_weno_pack(table, nv, box, dir, out, fp32, (cudaStream_t)stream, &launched);
     g_launches += launched;
     return cuda_status(e);
+}
+
+FVF_API int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int ghost,
+                      int dir, double *out, void *stream) {
+    return weno_pack_impl(reinterpret_cast<const void *const *>(fields), nv, extents, ghost, dir,
+                          out, false, stream);
+}
+
+FVF_API int weno_pack_f32(const float *const *fields, int nv, const int64_t extents[3],
+                          int ghost, int dir, float *out, void *stream) {
+    return weno_pack_impl(reinterpret_cast<const void *const *>(fields), nv, extents, ghost, dir,
+                          out, true, stream);
 }
 
 // Pointer tables of the multi-variable calls: each entry non-NULL and 8-byte
@@ -406,9 +421,8 @@ FVF_API int ssprk3_stage(const double *u0, const double *u, const double *const 
     return rk_stage_impl(u0, u, nullptr, flux, inv_d, nv, extents, a, b, dt, out, true, stream);
 }
 
-static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
-                           const int64_t extents[3], int dir, bool accumulate, double *rhs,
-                           void *stream) {
+static int advect_rhs_impl(const void *flux, const void *inv_d, int nv, const int64_t extents[3],
+                           int dir, bool accumulate, bool fp32, void *rhs, void *stream) {
     if (!extents) return FVF_ERR_NULL;
     if (dir < 0 || dir > 2) return FVF_ERR_DIR;
     if (nv < 0 || nv > FVF_MAX_NV) return FVF_ERR_NV;
@@ -425,9 +439,11 @@ static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
         return FVF_ERR_SIZE;
     if (elems == 0) return FVF_OK;
     if (!flux || !inv_d || !rhs) return FVF_ERR_NULL;
-    if ((uintptr_t)flux % 8 || (uintptr_t)inv_d % 8 || (uintptr_t)rhs % 8) return FVF_ERR_ALIGN;
-    const uint64_t rbytes = (uint64_t)elems * 8, fbytes = (uint64_t)felems * 8;
-    const uint64_t wbytes = (uint64_t)n[dir] * 8;
+    const uint64_t esize = fp32 ? 4 : 8;
+    if ((uintptr_t)flux % esize || (uintptr_t)inv_d % esize || (uintptr_t)rhs % esize)
+        return FVF_ERR_ALIGN;
+    const uint64_t rbytes = (uint64_t)elems * esize, fbytes = (uint64_t)felems * esize;
+    const uint64_t wbytes = (uint64_t)n[dir] * esize;
     int st = check_device_array(flux, fbytes);
     if (st == FVF_OK) st = check_device_array(inv_d, wbytes);
     if (st == FVF_OK) st = check_device_array(rhs, rbytes);
@@ -435,7 +451,7 @@ static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
     if (overlaps(rhs, rbytes, flux, fbytes) || overlaps(rhs, rbytes, inv_d, wbytes))
         return FVF_ERR_ALIAS;
     uint64_t launched = 0;
-    const cudaError_t e = launch_advect_rhs(flux, inv_d, nv, n, dir, accumulate, rhs,
+    const cudaError_t e = launch_advect_rhs(flux, inv_d, nv, n, dir, accumulate, fp32, rhs,
                                             (cudaStream_t)stream, &launched);
     g_launches += launched;
     return cuda_status(e);
@@ -443,12 +459,22 @@ static int advect_rhs_impl(const double *flux, const double *inv_d, int nv,
 
 FVF_API int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
                        int dir, double *rhs, void *stream) {
-    return advect_rhs_impl(flux, inv_d, nv, extents, dir, false, rhs, stream);
+    return advect_rhs_impl(flux, inv_d, nv, extents, dir, false, false, rhs, stream);
 }
 
 FVF_API int advect_rhs_add(const double *flux, const double *inv_d, int nv,
                            const int64_t extents[3], int dir, double *rhs, void *stream) {
-    return advect_rhs_impl(flux, inv_d, nv, extents, dir, true, rhs, stream);
+    return advect_rhs_impl(flux, inv_d, nv, extents, dir, true, false, rhs, stream);
+}
+
+FVF_API int advect_rhs_f32(const float *flux, const float *inv_d, int nv,
+                           const int64_t extents[3], int dir, float *rhs, void *stream) {
+    return advect_rhs_impl(flux, inv_d, nv, extents, dir, false, true, rhs, stream);
+}
+
+FVF_API int advect_rhs_add_f32(const float *flux, const float *inv_d, int nv,
+                               const int64_t extents[3], int dir, float *rhs, void *stream) {
+    return advect_rhs_impl(flux, inv_d, nv, extents, dir, true, true, rhs, stream);
 }
 
 // The inverse of the pack's axis exchange is the same exchange, so the copy
@@ -486,7 +512,8 @@ FVF_API int flux_unpack(const double *sweep_flux, int nv, const int64_t extents[
     std::memset(&table, 0, sizeof(table));
     for (int i = 0; i < nv; ++i) table.p[i] = sweep_flux + (int64_t)i * plane;
     uint64_t launched = 0;
-    const cudaError_t e = launch_weno_pack(table, nv, box, dir, out, (cudaStream_t)stream, &launched);
+    const cudaError_t e =
+        launch_weno_pack(table, nv, box, dir, out, false, (cudaStream_t)stream, &launched);
     g_launches += launched;
     return cuda_status(e);
 }

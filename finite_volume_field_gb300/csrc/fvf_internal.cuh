@@ -9,10 +9,11 @@ namespace fvf {
 
 constexpr int kMaxNv = 64;
 
-// Pointer table of the pack's input fields, passed to the kernel by value
-// (kernel parameter space), so concurrent calls never share state.
+// Pointer table of the pack's input fields (FP64 or FP32 elements, as the
+// launch says), passed to the kernel by value (kernel parameter space), so
+// concurrent calls never share state.
 struct FieldTable {
-    const double *p[kMaxNv];
+    const void *p[kMaxNv];
 };
 
 // Output pointer table of the conservative-variable copies (one array per
@@ -63,7 +64,7 @@ cudaError_t launch_diffuse3d(void *u, void *v, int64_t nx, int64_t ny, int64_t n
 cudaError_t read_device_error(int *flag);
 
 cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
-                             double *out, cudaStream_t stream, uint64_t *launches);
+                             void *out, bool fp32, cudaStream_t stream, uint64_t *launches);
 
 // The conservative-variable copy alone: copy_i[e] = field_i[e] for the
 // `stored` elements of every variable.
@@ -80,8 +81,8 @@ cudaError_t launch_weno_pack_copy(const FieldTable &fields, int nv, const Box &b
 cudaError_t launch_rk_stage(const RkStageArgs &args, bool fused, cudaStream_t stream,
                             uint64_t *launches);
 
-cudaError_t launch_advect_rhs(const double *flux, const double *inv_d, int nv,
-                              const int64_t n[3], int dir, bool accumulate, double *rhs,
+cudaError_t launch_advect_rhs(const void *flux, const void *inv_d, int nv, const int64_t n[3],
+                              int dir, bool accumulate, bool fp32, void *rhs,
                               cudaStream_t stream, uint64_t *launches);
 
 }  // namespace fvf

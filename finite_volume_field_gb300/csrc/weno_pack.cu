@@ -24,9 +24,11 @@ constexpr int kTile = 32;
 constexpr int kRows = 8;  // threads along the second tile axis
 
 // x: out(a, b, c, i) = f_i(a, b+g2, c+g3); (M1, M2, M3) = (N1, n2, n3).
+// T is double or float: the pack is a copy of 8- or 4-byte elements.
+template <typename T>
 __global__ void __launch_bounds__(256)
 pack_x_kernel(FieldTable t, int nv, int64_t N1, int64_t N2, int64_t n2, int64_t n3,
-              int64_t g2, int64_t g3, double *__restrict__ out) {
+              int64_t g2, int64_t g3, T *__restrict__ out) {
     const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (a >= N1) return;
     const int64_t plane = N1 * n2 * n3;
@@ -34,11 +36,11 @@ pack_x_kernel(FieldTable t, int nv, int64_t N1, int64_t N2, int64_t n2, int64_t 
          bc += (int64_t)gridDim.y * blockDim.y) {
         const int64_t b = bc % n2, c = bc / n2;
         const int64_t src = a + N1 * ((b + g2) + N2 * (c + g3));
-        double *o = out + a + N1 * bc;
+        T *o = out + a + N1 * bc;
 #pragma unroll 8
         for (int i = 0; i < kMaxNv; ++i) {
             if (i >= nv) break;
-            o[(int64_t)i * plane] = __ldg(t.p[i] + src);
+            o[(int64_t)i * plane] = __ldg(static_cast<const T *>(t.p[i]) + src);
         }
     }
 }
@@ -64,11 +66,11 @@ struct TransposeGeom {
     int64_t na, nj, nq, jo, qo, pj, pq, pnj, pnq, sa, sq, da, dq, plane, tiles_a, tiles_j;
 };
 
-template <bool COPY>
+template <typename T, bool COPY>
 __global__ void __launch_bounds__(kTile * kRows)
 pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
-                      double *__restrict__ out) {
-    __shared__ double tile[2][kTile][kTile + 1];
+                      T *__restrict__ out) {
+    __shared__ T tile[2][kTile][kTile + 1];
     int64_t blk = blockIdx.x;
     const int64_t ta = blk % G.tiles_a;
     blk /= G.tiles_a;
@@ -86,11 +88,11 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
     if (COPY && (qp < 0 || qp >= G.pnq)) {
         // a transverse ghost slice: copied, not packed (block-uniform branch)
         for (int i = 0; i < nv; ++i) {
-            const double *f = t.p[i];
-            double *c = cp.p[i];
-            double v[kPer];
+            const T *f = static_cast<const T *>(t.p[i]);
+            T *c = reinterpret_cast<T *>(cp.p[i]);
+            T v[kPer];
 #pragma unroll
-            for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : 0.0;
+            for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
 #pragma unroll
             for (int r = 0; r < kPer; ++r)
                 if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
@@ -108,15 +110,15 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
         sok[r] = as < G.na && jp >= 0 && jp < G.pnj;
     }
 
-    double v[kPer];
+    T v[kPer];
     {
-        const double *f = t.p[0];
+        const T *f = static_cast<const T *>(t.p[0]);
 #pragma unroll
-        for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : 0.0;
+        for (int r = 0; r < kPer; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
 #pragma unroll
         for (int r = 0; r < kPer; ++r) tile[0][ty + r * kRows][tx] = v[r];
         if (COPY) {
-            double *c = cp.p[0];
+            T *c = reinterpret_cast<T *>(cp.p[0]);
 #pragma unroll
             for (int r = 0; r < kPer; ++r)
                 if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
@@ -127,10 +129,10 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
         const int buf = i & 1;
         const bool more = i + 1 < nv;
         if (more) {
-            const double *f = t.p[i + 1];
+            const T *f = static_cast<const T *>(t.p[i + 1]);
 #pragma unroll
             for (int r = 0; r < kPer; ++r)
-                v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : 0.0;
+                v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
         }
         const int64_t obase = (int64_t)i * G.plane + dst0;
 #pragma unroll
@@ -140,7 +142,7 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
 #pragma unroll
             for (int r = 0; r < kPer; ++r) tile[buf ^ 1][ty + r * kRows][tx] = v[r];
             if (COPY) {
-                double *c = cp.p[i + 1];
+                T *c = reinterpret_cast<T *>(cp.p[i + 1]);
 #pragma unroll
                 for (int r = 0; r < kPer; ++r)
                     if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
@@ -174,7 +176,7 @@ pack_copy_x_kernel(FieldTable t, CopyTable cp, int nv, int64_t N1, int64_t N2, i
             double x[kBatch];
 #pragma unroll
             for (int r = 0; r < kBatch; ++r)
-                if (i0 + r < nv) x[r] = __ldg(t.p[i0 + r] + src);
+                if (i0 + r < nv) x[r] = __ldg(static_cast<const double *>(t.p[i0 + r]) + src);
 #pragma unroll
             for (int r = 0; r < kBatch; ++r) {
                 if (i0 + r < nv) {
@@ -201,21 +203,23 @@ fields_copy_kernel(FieldTable t, CopyTable cp, int nv, int64_t total) {
                 double2 x[kBatch];
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r)
-                    if (i0 + r < nv) x[r] = __ldg(reinterpret_cast<const double2 *>(t.p[i0 + r]) + e);
+                    if (i0 + r < nv)
+                        x[r] = __ldg(reinterpret_cast<const double2 *>(t.p[i0 + r]) + e);
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r)
                     if (i0 + r < nv) reinterpret_cast<double2 *>(cp.p[i0 + r])[e] = x[r];
             }
         }
         if ((total & 1) && tid == 0)
-            for (int i = 0; i < nv; ++i) cp.p[i][total - 1] = __ldg(t.p[i] + total - 1);
+            for (int i = 0; i < nv; ++i)
+                cp.p[i][total - 1] = __ldg(static_cast<const double *>(t.p[i]) + total - 1);
     } else {
         for (int64_t e = tid; e < total; e += stride) {
             for (int i0 = 0; i0 < nv; i0 += kBatch) {
                 double x[kBatch];
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r)
-                    if (i0 + r < nv) x[r] = __ldg(t.p[i0 + r] + e);
+                    if (i0 + r < nv) x[r] = __ldg(static_cast<const double *>(t.p[i0 + r]) + e);
 #pragma unroll
                 for (int r = 0; r < kBatch; ++r)
                     if (i0 + r < nv) cp.p[i0 + r][e] = x[r];
@@ -254,19 +258,20 @@ static TransposeGeom transpose_geom(const Box &box, int dir, bool copy) {
     return G;
 }
 
-template <bool COPY>
+template <typename T, bool COPY>
 static cudaError_t launch_transpose(const FieldTable &fields, const CopyTable &copies, int nv,
-                                    const Box &box, int dir, double *out, cudaStream_t stream) {
+                                    const Box &box, int dir, T *out, cudaStream_t stream) {
     const TransposeGeom G = transpose_geom(box, dir, COPY);
     const int64_t blocks = G.tiles_a * G.tiles_j * G.nq;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-    pack_transpose_kernel<COPY><<<(unsigned)blocks, dim3(kTile, kRows), 0, stream>>>(
+    pack_transpose_kernel<T, COPY><<<(unsigned)blocks, dim3(kTile, kRows), 0, stream>>>(
         fields, copies, nv, G, out);
     return cudaSuccess;
 }
 
-cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
-                             double *out, cudaStream_t stream, uint64_t *launches) {
+template <typename T>
+static cudaError_t launch_pack_typed(const FieldTable &fields, int nv, const Box &box, int dir,
+                                     T *out, cudaStream_t stream) {
     const int64_t n2 = box.n[1], n3 = box.n[2];
     const int64_t N1 = box.N[0], N2 = box.N[1];
     const int64_t g2 = box.g[1], g3 = box.g[2];
@@ -276,13 +281,20 @@ cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, i
         const int64_t gy = (n2 * n3 + 3) / 4;
         if (gx > 0x7fffffff) return cudaErrorInvalidValue;
         const dim3 grid((unsigned)gx, (unsigned)(gy < 65535 ? gy : 65535));
-        pack_x_kernel<<<grid, block, 0, stream>>>(fields, nv, N1, N2, n2, n3, g2, g3, out);
-    } else {
-        CopyTable none;
-        for (int i = 0; i < kMaxNv; ++i) none.p[i] = nullptr;
-        const cudaError_t e = launch_transpose<false>(fields, none, nv, box, dir, out, stream);
-        if (e != cudaSuccess) return e;
+        pack_x_kernel<T><<<grid, block, 0, stream>>>(fields, nv, N1, N2, n2, n3, g2, g3, out);
+        return cudaSuccess;
     }
+    CopyTable none;
+    for (int i = 0; i < kMaxNv; ++i) none.p[i] = nullptr;
+    return launch_transpose<T, false>(fields, none, nv, box, dir, out, stream);
+}
+
+cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
+                             void *out, bool fp32, cudaStream_t stream, uint64_t *launches) {
+    const cudaError_t e =
+        fp32 ? launch_pack_typed<float>(fields, nv, box, dir, static_cast<float *>(out), stream)
+             : launch_pack_typed<double>(fields, nv, box, dir, static_cast<double *>(out), stream);
+    if (e != cudaSuccess) return e;
     ++*launches;
     return cudaGetLastError();
 }
@@ -300,7 +312,8 @@ cudaError_t launch_weno_pack_copy(const FieldTable &fields, int nv, const Box &b
         pack_copy_x_kernel<<<grid, block, 0, stream>>>(fields, copies, nv, N1, N2, N3, box.n[1],
                                                       box.n[2], box.g[1], box.g[2], out);
     } else {
-        const cudaError_t e = launch_transpose<true>(fields, copies, nv, box, dir, out, stream);
+        const cudaError_t e =
+            launch_transpose<double, true>(fields, copies, nv, box, dir, out, stream);
         if (e != cudaSuccess) return e;
     }
     ++*launches;

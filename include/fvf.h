@@ -2,8 +2,8 @@
  * fvf.h -- C ABI of libfvf.so, the GB300 (sm_103a) library of per-cell field
  * sweeps: the explicit 2D 5-point and 3D 7-point diffusion steps with
  * ping-pong buffers, the
- * multi-variable WENO input pack, the finite-volume flux-difference source
- * (assigned or accumulated), the directional flux copy back to the physical
+ * multi-variable WENO input pack and the finite-volume flux-difference source
+ * (assigned or accumulated; FP64 and FP32), the directional flux copy back to the physical
  * frame, the conservative-variable copy (alone or fused with the pack) and
  * the SSPRK3 stage update (alone or fused with the flux difference).
  *
@@ -148,6 +148,15 @@ int weno_pack(const double *const *fields, int nv, const int64_t extents[3], int
               int dir, double *out, void *stream);
 
 /*
+ * weno_pack_f32 -- weno_pack on FP32 fields: the same element mapping, a
+ * 4-byte bit copy.  Arguments as for weno_pack with float in place of
+ * double (pointers 4-byte aligned).  [Q] section 6 measures FP32 against
+ * FP64 for the same sweeps.
+ */
+int weno_pack_f32(const float *const *fields, int nv, const int64_t extents[3], int ghost,
+                  int dir, float *out, void *stream);
+
+/*
  * advect_rhs -- the finite-volume flux-difference source of [M]
  * ("Changes", s_compute_advection_source_term), one direction per call,
  * assigned (not accumulated):
@@ -182,6 +191,17 @@ int advect_rhs(const double *flux, const double *inv_d, int nv, const int64_t ex
  */
 int advect_rhs_add(const double *flux, const double *inv_d, int nv, const int64_t extents[3],
                    int dir, double *rhs, void *stream);
+
+/*
+ * advect_rhs_f32, advect_rhs_add_f32 -- advect_rhs and advect_rhs_add in
+ * binary32: flux, inv_d and rhs are float arrays of the same layouts, and the
+ * subtraction, multiplication (and, for the accumulating form, addition) are
+ * binary32 operations, each rounded to nearest even.
+ */
+int advect_rhs_f32(const float *flux, const float *inv_d, int nv, const int64_t extents[3],
+                   int dir, float *rhs, void *stream);
+int advect_rhs_add_f32(const float *flux, const float *inv_d, int nv, const int64_t extents[3],
+                       int dir, float *rhs, void *stream);
 
 /*
  * flux_unpack -- the directional flux copy from the sweep frame back to the

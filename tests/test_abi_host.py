@@ -246,3 +246,19 @@ def test_device_error_flag_call(lib):
     flag = ctypes.c_int(7)
     st = lib.fvf_device_error(ctypes.byref(flag))
     assert (st, flag.value) in ((C["FVF_ERR_CUDA"], 0), (C["FVF_OK"], 0))
+
+
+def test_fp32_pack_and_flux_validation(lib):
+    vp = ctypes.c_void_p
+    ext = E3(3, 4, 5)
+    p, a, aa = lib.weno_pack_f32, lib.advect_rhs_f32, lib.advect_rhs_add_f32
+    table = (vp * 2)(4096, 8192)
+    assert p(table, 2, ext, 1, 3, 65536, None) == C["FVF_ERR_DIR"]
+    assert p(table, 2, ext, 1, 0, 65538, None) == C["FVF_ERR_ALIGN"]
+    assert p((vp * 2)(4098, 8192), 2, ext, 1, 0, 65536, None) == C["FVF_ERR_ALIGN"]
+    assert p(table, 2, ext, 1, 0, 65540, None) == C["FVF_ERR_NOT_DEVICE"]   # 4-byte aligned
+    for f in (a, aa):
+        assert f(4096, 8192, 2, ext, 3, 65536, None) == C["FVF_ERR_DIR"]
+        assert f(4096, 8192, 0, ext, 0, None, None) == C["FVF_OK"]
+        assert f(4098, 8192, 2, ext, 0, 65536, None) == C["FVF_ERR_ALIGN"]
+        assert f(4100, 8196, 2, ext, 0, 65540, None) == C["FVF_ERR_NOT_DEVICE"]
