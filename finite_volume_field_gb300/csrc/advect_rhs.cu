@@ -28,7 +28,9 @@ namespace fvf {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kGroup = 4;  // variables per load batch
+// variables per load batch: 4 FP64 or 8 FP32, 64 bytes of face loads each
+template <typename T>
+__host__ __device__ constexpr int group_of() { return 32 / (int)sizeof(T); }
 
 // Face difference F(c-1) - F(c) of variable slot q of a batch: on the FP64
 // unit, or as an exact integer-pipe addition of -F(c) when bit q of
@@ -73,6 +75,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
         const int64_t lo = (int64_t)j + F1 * ((int64_t)k + F2 * l);  // face c-1 at position c
         const T *f = flux + lo;
         T *r = rhs + (int64_t)jk + (int64_t)plane * l;
+        constexpr int kGroup = group_of<T>();
         for (int i0 = 0; i0 < nv; i0 += kGroup) {
             T a[kGroup], b[kGroup], old[kGroup];
 #pragma unroll
@@ -85,7 +88,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
                 }
             }
 #define FVF_RHS_Q(Q)                                                                    \
-    if (i0 + Q < nv) {                                                                  \
+    if (Q < kGroup && i0 + Q < nv) {                                                    \
         const T term = mul_rn(w, face_diff<Q>(a[Q], b[Q]));                            \
         /* accumulate form: the term added once to the existing rhs */                 \
         r[(int64_t)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;             \
@@ -94,6 +97,10 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
             FVF_RHS_Q(1)
             FVF_RHS_Q(2)
             FVF_RHS_Q(3)
+            FVF_RHS_Q(4)
+            FVF_RHS_Q(5)
+            FVF_RHS_Q(6)
+            FVF_RHS_Q(7)
 #undef FVF_RHS_Q
         }
     }
