@@ -610,6 +610,9 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
             u3, v3, n3, n3, n3, 0.1, 20, code, stream), 20 * 2 * esize * cells3,
             20 * (n3 - 2) ** 3, flops)
         del u3, v3
+    # ablation: the one-thread-per-(cell, variable) mapping that the pull
+    # request replaces, against the library's one-thread-per-cell kernels
+    out["collapse4_vs_collapse3"] = time_ablation(torch, sw, stream, timed)
     # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
     # (both states live in shared memory), reported per call and per step
     u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)
@@ -629,6 +632,54 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     out["diffuse_64x64_fp64_32steps"] = {"us_per_call": round(1e3 * t, 2),
                                          "us_per_step": round(1e3 * t / 32, 3)}
     return out
+
+
+def load_ablation():
+    """libfvf_ablation.so (built by buildlib.build_ablation) through ctypes."""
+    import ctypes
+    from finite_volume_field_gb300 import buildlib
+    lib = ctypes.CDLL(str(buildlib.build_ablation()))
+    vp, i64, cint = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.ablation_pack_x_collapse4.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint,
+                                              vp, vp]
+    lib.ablation_rhs_x_collapse4.argtypes = [vp, vp, cint, ctypes.POINTER(i64), vp, vp]
+    return lib
+
+
+def time_ablation(torch, sw, stream, timed):
+    """The x pack (8 x 207^3) and the x flux difference (8 x 201^3) with the
+    one-thread-per-(cell, variable) mapping (collapse 4) and with the
+    library's one-thread-per-cell kernels (collapse 3): time of each and the
+    ratio, and whether the two outputs agree bit for bit."""
+    import ctypes
+    from finite_volume_field_gb300 import api
+    lib = load_ablation()
+    ext = (ctypes.c_int64 * 3)(*PACK_EXT)
+    table = (ctypes.c_void_p * PACK_NV)(*[f.data_ptr() for f in sw.pack_fields])
+    o4 = torch.empty_like(sw.pack_out[0])
+    res = {}
+    t4 = timed(lambda: lib.ablation_pack_x_collapse4(table, PACK_NV, ext, PACK_G, o4.data_ptr(),
+                                                     stream.cuda_stream))
+    t3 = timed(lambda: api.weno_pack(sw.pack_fields, PACK_NV, PACK_EXT, PACK_G, 0, sw.pack_out[0],
+                                     stream))
+    torch.cuda.synchronize()
+    res["pack_x"] = {"collapse4_ms": round(t4, 4), "collapse3_ms": round(t3, 4),
+                     "duration_change": round(t3 / t4 - 1.0, 3),
+                     "same_bits": bool(torch.equal(o4.view(torch.int64),
+                                                   sw.pack_out[0].view(torch.int64)))}
+    rext = (ctypes.c_int64 * 3)(*RHS_EXT)
+    r4 = torch.empty_like(sw.rhs_out[0])
+    t4 = timed(lambda: lib.ablation_rhs_x_collapse4(sw.rhs_flux[0].data_ptr(),
+                                                    sw.rhs_invd[0].data_ptr(), RHS_NV, rext,
+                                                    r4.data_ptr(), stream.cuda_stream))
+    t3 = timed(lambda: api.advect_rhs(sw.rhs_flux[0], sw.rhs_invd[0], RHS_NV, RHS_EXT, 0,
+                                      sw.rhs_out[0], stream))
+    torch.cuda.synchronize()
+    res["rhs_x"] = {"collapse4_ms": round(t4, 4), "collapse3_ms": round(t3, 4),
+                    "duration_change": round(t3 / t4 - 1.0, 3),
+                    "same_bits": bool(torch.equal(r4.view(torch.int64),
+                                                  sw.rhs_out[0].view(torch.int64)))}
+    return res
 
 
 def aggregate(per_rank, world):
@@ -879,6 +930,44 @@ def run_ncu_case():
     return 0
 
 
+def run_ncu_ablation():
+    """The x pack on 8 x 207^3 and the x flux difference on 8 x 201^3, each
+    once with the library kernel (one thread per cell) then once with the
+    ablation kernel (one thread per cell-variable pair), for an Nsight
+    Compute comparison of instructions, DRAM bytes and duration."""
+    import ctypes
+
+    import torch
+    from finite_volume_field_gb300 import api, buildlib
+    if not api.LIB_PATH.exists():
+        buildlib.build()
+    api.load()
+    lib = load_ablation()
+    N = _prod(inputs.stored_extents(PACK_EXT, PACK_G))
+    fields = [torch.randn(N, dtype=torch.float64, device="cuda") for _ in range(PACK_NV)]
+    out = torch.empty(_prod(pack_extents(PACK_EXT, PACK_G, 0)) * PACK_NV, dtype=torch.float64,
+                      device="cuda")
+    api.weno_pack(fields, PACK_NV, PACK_EXT, PACK_G, 0, out)
+    table = (ctypes.c_void_p * PACK_NV)(*[f.data_ptr() for f in fields])
+    lib.ablation_pack_x_collapse4(table, PACK_NV, (ctypes.c_int64 * 3)(*PACK_EXT), PACK_G,
+                                  out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    del fields, out
+    torch.cuda.empty_cache()
+    fe = list(RHS_EXT)
+    fe[0] += 1
+    F = torch.randn(_prod(fe) * RHS_NV, dtype=torch.float64, device="cuda")
+    w = torch.rand(RHS_EXT[0], dtype=torch.float64, device="cuda") + 0.5
+    r = torch.empty(_prod(RHS_EXT) * RHS_NV, dtype=torch.float64, device="cuda")
+    api.advect_rhs(F, w, RHS_NV, RHS_EXT, 0, r)
+    lib.ablation_rhs_x_collapse4(F.data_ptr(), w.data_ptr(), RHS_NV,
+                                 (ctypes.c_int64 * 3)(*RHS_EXT), r.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    print("ncu ablation done", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -887,11 +976,15 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (it is only taken at N=1 anyway)")
+    ap.add_argument("--ncu-ablation", action="store_true",
+                    help="run the collapse-3 / collapse-4 kernel pairs once each (for ncu)")
     ap.add_argument("--ncu-case", action="store_true",
                     help="launch each sweep kernel once at benchmark size (for ncu), no timing")
     args = ap.parse_args(argv)
     if args.ncu_case:
         return run_ncu_case()
+    if args.ncu_ablation:
+        return run_ncu_ablation()
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
