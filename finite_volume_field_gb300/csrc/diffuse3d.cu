@@ -40,6 +40,7 @@
 
 #include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
+#include "mbarrier.cuh"
 
 // Number of the five neighbour sums (W+E, +S, +N, +B, +T, in that order) that
 // the FP64 update runs on the integer pipes (fp64_emu.cuh); every choice gives
@@ -242,54 +243,10 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
 #endif
 constexpr int kRing = FVF_3D_RING;           // slots: planes k-1, k, k+1 and kRing-3 ahead
 constexpr int kRows = kTY + 2;               // tile rows plus one halo row each side
-constexpr uint32_t kWaitLimit = 1u << 22;    // try_wait polls before a wait gives up
 
 __device__ int g_device_error;               // nonzero: a bounded wait expired
 
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Waits for the phase of the given parity to complete; false if the poll
-// limit expires first.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t it = 0; it < kWaitLimit; ++it)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-// One box of the 3D tensor map at (x, y, z) into shared memory.
-__device__ __forceinline__ void tensor_load(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
+using mbar::smem_addr;
 
 template <typename T, int V>
 __device__ __forceinline__ Vec<T, V> ld_stage(const T *p) {
@@ -339,8 +296,8 @@ diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict
     const bool producer = lane == 0 && w == 0;
     const int64_t sxy = nx * ny;
     if (producer) {
-        for (int s = 0; s < kRing; ++s) mbar_init(smem_addr(&bars[s]), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int s = 0; s < kRing; ++s) mbar::init(smem_addr(&bars[s]), 1);
+        mbar::fence_init();
     }
     __syncthreads();
     // Planes are loaded in order and numbered t = 0, 1, ... over all items of
@@ -359,12 +316,12 @@ diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict
         auto issue = [&](int64_t p) {
             const uint32_t sl = (tbase + (uint32_t)(p - pl0)) % kRing;
             const uint32_t bar = smem_addr(&bars[sl]);
-            mbar_expect_tx(bar, kBoxBytes);
-            tensor_load(smem_addr(stage + (int64_t)sl * SLOT), &src_map, (int)(x0 - P),
-                        (int)(j0 - 1), (int)p, bar);
+            mbar::expect_tx(bar, kBoxBytes);
+            mbar::tensor_load_3d(smem_addr(stage + (int64_t)sl * SLOT), &src_map, (int)(x0 - P),
+                                 (int)(j0 - 1), (int)p, bar);
         };
         auto wait_t = [&](uint32_t t) {
-            return mbar_wait(smem_addr(&bars[t % kRing]), (t / kRing) & 1u);
+            return mbar::wait(smem_addr(&bars[t % kRing]), (t / kRing) & 1u);
         };
         int64_t issued = pl0 - 1;                         // producer: last plane issued
         if (producer)
@@ -386,9 +343,9 @@ diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict
         uint32_t st = (tk + 1) % kRing, pt = ((tk + 1) / kRing) & 1u;
         for (int64_t k = kz0; k < kz1; ++k) {
             bool ok = true;
-            if (k - 1 >= pl0) ok = mbar_wait(smem_addr(&bars[sb]), pb) && ok;
-            ok = mbar_wait(smem_addr(&bars[sc]), pc) && ok;
-            if (k + 1 <= pl1) ok = mbar_wait(smem_addr(&bars[st]), pt) && ok;
+            if (k - 1 >= pl0) ok = mbar::wait(smem_addr(&bars[sb]), pb) && ok;
+            ok = mbar::wait(smem_addr(&bars[sc]), pc) && ok;
+            if (k + 1 <= pl1) ok = mbar::wait(smem_addr(&bars[st]), pt) && ok;
             if (__syncthreads_or(!ok)) {
                 // a copy did not land in time: record it, let the copies in
                 // flight finish (bounded) and leave
