@@ -95,8 +95,9 @@ def launch_count() -> int:
 
 
 def device_error() -> int:
-    """Reads and clears the device flag set when a kernel's bounded wait on
-    its own copies expired (0: none).  Synchronises the device."""
+    """Reads and clears the device error flags: bit 1, a kernel's bounded
+    wait on its own copies expired; bit 2 (index-checking builds), a kernel
+    met an out-of-range index.  0: none.  Synchronises the device."""
     flag = ctypes.c_int(0)
     _check("fvf_device_error", load().fvf_device_error(ctypes.byref(flag)))
     return int(flag.value)

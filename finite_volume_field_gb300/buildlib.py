@@ -45,24 +45,35 @@ def sources():
     return sorted(CSRC.glob("*.cu"))
 
 
-def _stale() -> bool:
-    if not LIB.exists():
+CHECK_BUILD = PKG / "_build_check"
+CHECK_LIB = PKG / "libfvf_check.so"
+
+
+def _stale(lib: Path) -> bool:
+    if not lib.exists():
         return True
-    t = LIB.stat().st_mtime
+    t = lib.stat().st_mtime
     deps = list(CSRC.glob("*")) + list(INCLUDE.glob("*.h")) + [Path(__file__)]
     return any(p.stat().st_mtime > t for p in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> Path:
-    """Compile and link libfvf.so if it is missing or older than a source."""
-    if not force and not _stale():
-        return LIB
-    BUILD.mkdir(exist_ok=True)
+def build(force: bool = False, verbose: bool = False, bounds_check: bool = False) -> Path:
+    """Compile and link libfvf.so if it is missing or older than a source.
+
+    With ``bounds_check`` the same sources are built with
+    -DFVF_BOUNDS_CHECK=1 into libfvf_check.so: a debug build (for small
+    grids) whose kernels test every global index before using it and record
+    a failure instead of accessing memory (read back by fvf_device_error)."""
+    lib, build_dir = (CHECK_LIB, CHECK_BUILD) if bounds_check else (LIB, BUILD)
+    if not force and not _stale(lib):
+        return lib
+    build_dir.mkdir(exist_ok=True)
     cc = nvcc()
+    extra = ["-DFVF_BOUNDS_CHECK=1"] if bounds_check else []
 
     def compile_one(src: Path):
-        obj = BUILD / (src.stem + ".o")
-        cmd = [cc, *NVCC_FLAGS, "-c", str(src), "-o", str(obj)]
+        obj = build_dir / (src.stem + ".o")
+        cmd = [cc, *NVCC_FLAGS, *extra, "-c", str(src), "-o", str(obj)]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
 
@@ -73,17 +84,17 @@ def build(force: bool = False, verbose: bool = False) -> Path:
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src.name}:\n{r.stdout}\n{r.stderr}")
         report.append(f"== {src.name}\n{r.stderr}")
-    (BUILD / "ptxas.txt").write_text("\n".join(report))
-    tmp = LIB.with_suffix(f".so.tmp{os.getpid()}")
+    (build_dir / "ptxas.txt").write_text("\n".join(report))
+    tmp = lib.with_suffix(f".so.tmp{os.getpid()}")
     link = [cc, "-shared", *ARCH, "-cudart", "static", *[str(o) for _, o, _ in results],
             "-o", str(tmp)]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     if verbose:
-        print((BUILD / "ptxas.txt").read_text())
-    return LIB
+        print((build_dir / "ptxas.txt").read_text())
+    return lib
 
 
 ABLATION_SRC = PKG / "ablation" / "collapse4.cu"

@@ -69,12 +69,17 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
     const int64_t fplane = F1 * F2 * F3;
     const int64_t rplane = (int64_t)plane * n3;
     const int64_t step = DIR == 0 ? 1 : (DIR == 1 ? F1 : F1 * F2);
-    const T wjk = DIR == 0 ? __ldg(inv_d + j) : (DIR == 1 ? __ldg(inv_d + k) : T(0));
+    const int64_t nw = DIR == 0 ? (int64_t)n1 : (DIR == 1 ? (int64_t)n2 : n3);  // inv_d extent
+    const int64_t fall = fplane * nv, rall = rplane * nv;  // flux and rhs extents
+    (void)nw; (void)fall; (void)rall;
+    const T wjk = DIR == 0 ? (FVF_IN(j, nw) ? __ldg(inv_d + j) : T(0))
+                           : (DIR == 1 ? (FVF_IN(k, nw) ? __ldg(inv_d + k) : T(0)) : T(0));
     for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
-        const T w = DIR == 2 ? __ldg(inv_d + l) : wjk;
+        const T w = DIR == 2 ? (FVF_IN(l, nw) ? __ldg(inv_d + l) : T(0)) : wjk;
         const int64_t lo = (int64_t)j + F1 * ((int64_t)k + F2 * l);  // face c-1 at position c
+        const int64_t ro = (int64_t)jk + (int64_t)plane * l;
         const T *f = flux + lo;
-        T *r = rhs + (int64_t)jk + (int64_t)plane * l;
+        T *r = rhs + ro;
         constexpr int kGroup = group_of<T>();
         for (int i0 = 0; i0 < nv; i0 += kGroup) {
             T a[kGroup], b[kGroup], old[kGroup];
@@ -82,16 +87,19 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
             for (int q = 0; q < kGroup; ++q) {
                 if (i0 + q < nv) {
                     const int64_t fo = (int64_t)(i0 + q) * fplane;
-                    a[q] = __ldg(f + fo);
-                    b[q] = __ldg(f + fo + step);
-                    if (ACC) old[q] = r[(int64_t)(i0 + q) * rplane];
+                    a[q] = FVF_IN(lo + fo, fall) ? __ldg(f + fo) : T(0);
+                    b[q] = FVF_IN(lo + fo + step, fall) ? __ldg(f + fo + step) : T(0);
+                    if (ACC)
+                        old[q] = FVF_IN(ro + (int64_t)(i0 + q) * rplane, rall)
+                                     ? r[(int64_t)(i0 + q) * rplane] : T(0);
                 }
             }
 #define FVF_RHS_Q(Q)                                                                    \
     if (Q < kGroup && i0 + Q < nv) {                                                    \
         const T term = mul_rn(w, face_diff<Q>(a[Q], b[Q]));                            \
         /* accumulate form: the term added once to the existing rhs */                 \
-        r[(int64_t)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;             \
+        if (FVF_IN(ro + (int64_t)(i0 + Q) * rplane, rall))                              \
+            r[(int64_t)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;         \
     }
             FVF_RHS_Q(0)
             FVF_RHS_Q(1)
@@ -137,6 +145,8 @@ void launch_dir(const T *flux, const T *inv_d, int nv, const int64_t n[3], int d
 }
 
 }  // namespace
+
+FVF_BOUNDS_READER(read_bounds_rhs)
 
 cudaError_t launch_advect_rhs(const void *flux, const void *inv_d, int nv, const int64_t n[3],
                               int dir, bool accumulate, bool fp32, void *rhs,

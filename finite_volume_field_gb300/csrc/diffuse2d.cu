@@ -131,9 +131,10 @@ diffuse_step_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, 
     for (int64_t j = (int64_t)blockIdx.y * kBy + threadIdx.y; j < ny;
          j += (int64_t)gridDim.y * kBy) {
         const int64_t c = i + nx * j;
+        if (!FVF_IN(c, nx * ny)) continue;
         if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1) {
             dst[c] = T(0);
-        } else {
+        } else if (FVF_IN(c - nx, nx * ny) && FVF_IN(c + nx, nx * ny)) {
             dst[c] = update<T>(src[c], src[c - 1], src[c + 1], src[c - nx], src[c + nx], alpha);
         }
     }
@@ -198,7 +199,7 @@ __device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int
     for (int k = 0; k < V; ++k) r.c.v[k] = T(0);
     r.w_out = T(0);
     r.e_out = T(0);
-    if (active && j >= 0 && j < ny) {
+    if (active && j >= 0 && j < ny && FVF_IN(nx * j + col + V - 1, nx * ny)) {
         const T *row = src + nx * j;
         r.c = load16<T>(row + col);
         if (lane == 0 && col > 0) r.w_out = __ldg(row + col - 1);
@@ -238,7 +239,7 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
             const bool edge = edge_row || i == 0 || i == nx - 1;
             out.v[k] = edge ? T(0) : update<T>(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha);
         }
-        if (active) store16<T>(dst + nx * j + col, out);
+        if (active && FVF_IN(nx * j + col + V - 1, nx * ny)) store16<T>(dst + nx * j + col, out);
         rs = rc;
         rc = rn;
         rn = rnn;
@@ -346,7 +347,8 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
             const int li = lane + 32 * a;
             const int64_t gi = gi0 + li;
             T val = T(0);
-            if (gi >= 0 && gi < nx && gj >= 0 && gj < ny) val = __ldg(src + gi + nx * gj);
+            if (gi >= 0 && gi < nx && gj >= 0 && gj < ny && FVF_IN(gi + nx * gj, nx * ny))
+                val = __ldg(src + gi + nx * gj);
             buf0[lj * kTbW + li] = val;
         }
     }
@@ -417,7 +419,8 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
         for (int a = 0; a < kTbCx; ++a) {
             const int li = lane + 32 * a;
             const int64_t gi = gi0 + li;
-            if (li >= kTbSteps && li < kTbSteps + kTbX && gi >= 0 && gi < nx)
+            if (li >= kTbSteps && li < kTbSteps + kTbX && gi >= 0 && gi < nx &&
+                FVF_IN(gi + nx * gj, nx * ny))
                 dst[gi + nx * gj] = fin[lj * kTbW + li];
         }
     }
@@ -455,7 +458,8 @@ diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restric
     const int r0 = rank * band;
     const int rows = max(0, min(band, ny - r0));
     const int cells = rows * nx;
-    for (int c = threadIdx.x; c < cells; c += kClusterThreads) st0[c] = u0[(int64_t)r0 * nx + c];
+    for (int c = threadIdx.x; c < cells; c += kClusterThreads)
+        if (FVF_IN((int64_t)r0 * nx + c, (int64_t)nx * ny)) st0[c] = u0[(int64_t)r0 * nx + c];
     cluster.sync();
     for (int64_t s = 1; s <= nsteps; ++s) {
         T *in = (s & 1) ? st0 : st1;
@@ -480,6 +484,7 @@ diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restric
     const T *last = (nsteps & 1) ? st1 : st0, *prev = (nsteps & 1) ? st0 : st1;
     T *res = (nsteps & 1) ? v : u, *oth = (nsteps & 1) ? u : v;
     for (int c = threadIdx.x; c < cells; c += kClusterThreads) {
+        if (!FVF_IN((int64_t)r0 * nx + c, (int64_t)nx * ny)) continue;
         res[(int64_t)r0 * nx + c] = last[c];
         oth[(int64_t)r0 * nx + c] = prev[c];
     }
@@ -628,6 +633,8 @@ cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
 }
 
 }  // namespace
+
+FVF_BOUNDS_READER(read_bounds_diffuse2d)
 
 cudaError_t launch_diffuse2d(void *u, void *v, int64_t nx, int64_t ny, double alpha,
                              int64_t nsteps, bool fp64, cudaStream_t stream,

@@ -92,11 +92,14 @@ struct Vec {
 // Loads this lane's vector of row `row` (cells x0 + lane*V .. +V-1; zeros
 // past the end) and, for lanes 0 and 31, the outside neighbour of the warp's
 // segment (x0 - 1 and x0 + 32V; zero where it does not exist).
+// `off` is the row's offset in its nx*ny*nz array (index checks only).
 template <typename T, int V>
 __device__ __forceinline__ void load_row(const T *__restrict__ row, int64_t x0, int lane,
-                                         int64_t nx, Vec<T, V> &out, T &xh) {
+                                         int64_t nx, Vec<T, V> &out, T &xh, int64_t off,
+                                         int64_t total) {
+    (void)off; (void)total;
     const int64_t xi = x0 + (int64_t)lane * V;
-    if (xi < nx) {
+    if (xi < nx && FVF_IN(off + xi + V - 1, total)) {
         if constexpr (V == 4) {
             const float4 q = __ldg(reinterpret_cast<const float4 *>(row + xi));
             out.v[0] = q.x; out.v[1] = q.y; out.v[2] = q.z; out.v[3] = q.w;
@@ -111,14 +114,16 @@ __device__ __forceinline__ void load_row(const T *__restrict__ row, int64_t x0, 
         for (int v = 0; v < V; ++v) out.v[v] = T(0);
     }
     const int64_t xo = lane == 0 ? x0 - 1 : x0 + 32 * V;
-    xh = ((lane == 0 || lane == 31) && xo >= 0 && xo < nx) ? __ldg(row + xo) : T(0);
+    xh = ((lane == 0 || lane == 31) && xo >= 0 && xo < nx && FVF_IN(off + xo, total))
+             ? __ldg(row + xo) : T(0);
 }
 
 template <typename T, int V>
 __device__ __forceinline__ void store_row(T *__restrict__ row, int64_t x0, int lane, int64_t nx,
-                                          const Vec<T, V> &x) {
+                                          const Vec<T, V> &x, int64_t off, int64_t total) {
+    (void)off; (void)total;
     const int64_t xi = x0 + (int64_t)lane * V;
-    if (xi >= nx) return;
+    if (xi >= nx || !FVF_IN(off + xi + V - 1, total)) return;
     if constexpr (V == 4) {
         *reinterpret_cast<float4 *>(row + xi) = make_float4(x.v[0], x.v[1], x.v[2], x.v[3]);
     } else if constexpr (V == 2) {
@@ -165,14 +170,18 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
         prev.v[v] = cur.v[v] = next.v[v] = nn.v[v] = T(0);
         hcur.v[v] = hnext.v[v] = hnn.v[v] = T(0);
     }
+    const int64_t total = sxy * nz;
+    auto load = [&](int64_t jr, int64_t kp, Vec<T, V> &o, T &h) {
+        load_row<T, V>(src + jr * nx + kp * sxy, x0, lane, nx, o, h, jr * nx + kp * sxy, total);
+    };
     if (rowok) {
-        if (kz0 >= 1) load_row<T, V>(src + j * nx + (kz0 - 1) * sxy, x0, lane, nx, prev, xp);
-        load_row<T, V>(src + j * nx + kz0 * sxy, x0, lane, nx, cur, xc);
-        if (kz0 + 1 <= klast) load_row<T, V>(src + j * nx + (kz0 + 1) * sxy, x0, lane, nx, next, xn);
+        if (kz0 >= 1) load(j, kz0 - 1, prev, xp);
+        load(j, kz0, cur, xc);
+        if (kz0 + 1 <= klast) load(j, kz0 + 1, next, xn);
     }
     if (hok) {
-        load_row<T, V>(src + jh * nx + kz0 * sxy, x0, lane, nx, hcur, hx);
-        if (kz0 + 1 <= klast) load_row<T, V>(src + jh * nx + (kz0 + 1) * sxy, x0, lane, nx, hnext, hx);
+        load(jh, kz0, hcur, hx);
+        if (kz0 + 1 <= klast) load(jh, kz0 + 1, hnext, hx);
     }
     (void)xp;
     int buf = 0;
@@ -188,8 +197,8 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
         }
         // prefetch plane k+2
         if (k + 2 <= klast) {
-            if (rowok) load_row<T, V>(src + j * nx + (k + 2) * sxy, x0, lane, nx, nn, xnn);
-            if (hok) load_row<T, V>(src + jh * nx + (k + 2) * sxy, x0, lane, nx, hnn, hx);
+            if (rowok) load(j, k + 2, nn, xnn);
+            if (hok) load(jh, k + 2, hnn, hx);
         }
         __syncthreads();
         if (rowok) {
@@ -218,7 +227,7 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
                                                 alpha);
                 }
             }
-            store_row<T, V>(dst + j * nx + k * sxy, x0, lane, nx, out);
+            store_row<T, V>(dst + j * nx + k * sxy, x0, lane, nx, out, j * nx + k * sxy, total);
         }
         prev = cur;
         cur = next;
@@ -391,7 +400,8 @@ diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict
                         out.v[v] = (lane_inner || (i != 0 && i < nx - 1)) ? r : T(0);
                     }
                 }
-                if (xi < nx) store_vec<T, V>(drow + xi, out);
+                if (xi < nx && FVF_IN((drow - dst) + xi + V - 1, sxy * nz))
+                    store_vec<T, V>(drow + xi, out);
             }
             drow += sxy;
             sb = sc; pb = pc;
@@ -519,6 +529,8 @@ cudaError_t launch_steps(T *u, T *v, int64_t nx, int64_t ny, int64_t nz, T alpha
 }
 
 }  // namespace
+
+FVF_BOUNDS_READER(read_bounds_diffuse3d)
 
 cudaError_t read_device_error(int *flag) {
     int zero = 0;

@@ -541,7 +541,18 @@ FVF_API int fvf_last_cuda_error(void) { return g_last_cuda_error; }
 FVF_API int fvf_device_error(int *flag) {
     if (!flag) return FVF_ERR_NULL;
     *flag = 0;
-    return cuda_status(read_device_error(flag));
+    int waits = 0, bounds = 0, b = 0;
+    cudaError_t e = read_device_error(&waits);
+    cudaError_t (*const readers[])(int *) = {read_bounds_diffuse2d, read_bounds_diffuse3d,
+                                             read_bounds_pack, read_bounds_rhs, read_bounds_rk};
+    for (auto rd : readers) {
+        if (e != cudaSuccess) break;
+        e = rd(&b);
+        bounds |= b;
+    }
+    if (e != cudaSuccess) return cuda_status(e);
+    *flag = (waits ? 1 : 0) | (bounds ? 2 : 0);
+    return FVF_OK;
 }
 
 FVF_API uint64_t fvf_launch_count(void) { return g_launches.load(); }

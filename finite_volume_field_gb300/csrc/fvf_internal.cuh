@@ -5,6 +5,40 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Index checks for debug builds.  Built with -DFVF_BOUNDS_CHECK=1 (for
+// small grids; buildlib.build(bounds_check=True) makes libfvf_check.so),
+// FVF_IN(i, n) tests a global index against the extent of the array it
+// addresses before the access it guards; a failing test records itself in
+// the translation unit's flag (read through fvf_device_error) and the access
+// is skipped -- nothing traps.  In release builds FVF_IN is the constant true
+// and the generated code is unchanged.
+#ifndef FVF_BOUNDS_CHECK
+#define FVF_BOUNDS_CHECK 0
+#endif
+#if FVF_BOUNDS_CHECK
+static __device__ int g_bounds_failed;
+static __device__ __forceinline__ bool fvf_in_bounds(int64_t i, int64_t n) {
+    if (i >= 0 && i < n) return true;
+    atomicExch(&g_bounds_failed, 1);
+    return false;
+}
+#define FVF_IN(i, n) fvf_in_bounds((int64_t)(i), (int64_t)(n))
+#define FVF_BOUNDS_READER(fn)                                                    \
+    cudaError_t fn(int *failed) {                                                \
+        int zero = 0;                                                            \
+        cudaError_t e = cudaMemcpyFromSymbol(failed, g_bounds_failed, sizeof(int)); \
+        if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_bounds_failed, &zero, sizeof(int)); \
+        return e;                                                                \
+    }
+#else
+#define FVF_IN(i, n) true
+#define FVF_BOUNDS_READER(fn)     \
+    cudaError_t fn(int *failed) { \
+        *failed = 0;              \
+        return cudaSuccess;       \
+    }
+#endif
+
 namespace fvf {
 
 constexpr int kMaxNv = 64;
@@ -62,6 +96,14 @@ cudaError_t launch_diffuse3d(void *u, void *v, int64_t nx, int64_t ny, int64_t n
 // Reads and clears the device flag that kernels with bounded waits set when
 // a wait expires (synchronises the device).
 cudaError_t read_device_error(int *flag);
+
+// Each kernel file's index-check flag (always 0 unless built with
+// FVF_BOUNDS_CHECK); reading clears it.
+cudaError_t read_bounds_diffuse2d(int *failed);
+cudaError_t read_bounds_diffuse3d(int *failed);
+cudaError_t read_bounds_pack(int *failed);
+cudaError_t read_bounds_rhs(int *failed);
+cudaError_t read_bounds_rk(int *failed);
 
 cudaError_t launch_weno_pack(const FieldTable &fields, int nv, const Box &box, int dir,
                              void *out, bool fp32, cudaStream_t stream, uint64_t *launches);

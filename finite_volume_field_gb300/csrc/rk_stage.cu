@@ -80,10 +80,13 @@ rk_stage_kernel(RkStageArgs A) {
     const int64_t cplane = (int64_t)plane_jk * n3;  // cells per variable
     const int64_t fxp = (int64_t)(n1 + 1) * n2 * n3, fyp = (int64_t)n1 * (n2 + 1) * n3,
                   fzp = (int64_t)plane_jk * (n3 + 1);
-    const double wx = FUSED ? __ldg(A.w[0] + j) : 0.0;
-    const double wy = FY ? __ldg(A.w[1] + k) : 0.0;
+    const int64_t call = cplane * A.nv;  // extents of the cell and face arrays
+    const int64_t xall = (FUSED ? fxp : cplane) * A.nv, yall = fyp * A.nv, zall = fzp * A.nv;
+    (void)call; (void)xall; (void)yall; (void)zall;
+    const double wx = FUSED && FVF_IN(j, n1) ? __ldg(A.w[0] + j) : 0.0;
+    const double wy = FY && FVF_IN(k, n2) ? __ldg(A.w[1] + k) : 0.0;
     for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
-        const double wz = FZ ? __ldg(A.w[2] + l) : 0.0;
+        const double wz = FZ && FVF_IN(l, n3) ? __ldg(A.w[2] + l) : 0.0;
         const int64_t c = (int64_t)jk + (int64_t)plane_jk * l;
         const int64_t xlo = (int64_t)j + (int64_t)(n1 + 1) * ((int64_t)k + (int64_t)n2 * l);
         const int64_t ylo = (int64_t)j + (int64_t)n1 * ((int64_t)k + (int64_t)(n2 + 1) * l);
@@ -95,21 +98,25 @@ rk_stage_kernel(RkStageArgs A) {
             for (int q = 0; q < kChunk; ++q) {
                 if (i0 + q < A.nv) {
                     const int64_t iv = i0 + q;
-                    u0v[q] = A.u0[c + iv * cplane];
-                    uv[q] = A.u[c + iv * cplane];
+                    const bool cin = FVF_IN(c + iv * cplane, call);
+                    u0v[q] = cin ? A.u0[c + iv * cplane] : 0.0;
+                    uv[q] = cin ? A.u[c + iv * cplane] : 0.0;
                     if (FUSED) {
-                        xl[q] = __ldg(A.f[0] + xlo + iv * fxp);
-                        xh[q] = __ldg(A.f[0] + xlo + iv * fxp + 1);
+                        const bool in = FVF_IN(xlo + iv * fxp + 1, xall);
+                        xl[q] = in ? __ldg(A.f[0] + xlo + iv * fxp) : 0.0;
+                        xh[q] = in ? __ldg(A.f[0] + xlo + iv * fxp + 1) : 0.0;
                     } else {
-                        r[q] = __ldg(A.f[0] + c + iv * cplane);
+                        r[q] = cin ? __ldg(A.f[0] + c + iv * cplane) : 0.0;
                     }
                     if (FY) {
-                        yl[q] = __ldg(A.f[1] + ylo + iv * fyp);
-                        yh[q] = __ldg(A.f[1] + ylo + iv * fyp + n1);
+                        const bool in = FVF_IN(ylo + iv * fyp + n1, yall);
+                        yl[q] = in ? __ldg(A.f[1] + ylo + iv * fyp) : 0.0;
+                        yh[q] = in ? __ldg(A.f[1] + ylo + iv * fyp + n1) : 0.0;
                     }
                     if (FZ) {
-                        zl[q] = __ldg(A.f[2] + zlo + iv * fzp);
-                        zh[q] = __ldg(A.f[2] + zlo + iv * fzp + plane_jk);
+                        const bool in = FVF_IN(zlo + iv * fzp + plane_jk, zall);
+                        zl[q] = in ? __ldg(A.f[2] + zlo + iv * fzp) : 0.0;
+                        zh[q] = in ? __ldg(A.f[2] + zlo + iv * fzp + plane_jk) : 0.0;
                     }
                 }
             }
@@ -125,8 +132,9 @@ rk_stage_kernel(RkStageArgs A) {
                         rr = r[q];
                     }
                     const double t = add_rn<4>(uv[q], __dmul_rn(A.dt, rr), q);
-                    A.out[c + (int64_t)(i0 + q) * cplane] =
-                        add_rn<8>(__dmul_rn(A.a, u0v[q]), __dmul_rn(A.b, t), q);
+                    if (FVF_IN(c + (int64_t)(i0 + q) * cplane, call))
+                        A.out[c + (int64_t)(i0 + q) * cplane] =
+                            add_rn<8>(__dmul_rn(A.a, u0v[q]), __dmul_rn(A.b, t), q);
                 }
             }
         }
@@ -148,6 +156,8 @@ cudaError_t launch_typed(const RkStageArgs &A, cudaStream_t stream) {
 }
 
 }  // namespace
+
+FVF_BOUNDS_READER(read_bounds_rk)
 
 cudaError_t launch_rk_stage(const RkStageArgs &A, bool fused, cudaStream_t stream,
                             uint64_t *launches) {

@@ -57,7 +57,9 @@ pack_x_kernel(FieldTable t, int nv, int64_t N1, int64_t N2, int64_t n2, int64_t 
             const T *f = static_cast<const T *>(t.p[i]);
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                if (ok[r]) o[r][(int64_t)i * plane] = __ldg(f + src[r]);
+                if (ok[r] && FVF_IN(src[r], N1 * N2 * (n3 + 2 * g3)) &&
+                    FVF_IN(o[r] - out + (int64_t)i * plane, plane * nv))
+                    o[r][(int64_t)i * plane] = __ldg(f + src[r]);
         }
     }
 }
@@ -81,6 +83,7 @@ constexpr int kPer = kTile / kRows;
 
 struct TransposeGeom {
     int64_t na, nj, nq, jo, qo, pj, pq, pnj, pnq, sa, sq, da, dq, plane, tiles_a, tiles_j;
+    int64_t stored;  // elements of one field's stored box (index checks)
 };
 
 // Halves of the tile along a (one 32-wide half for both element sizes; a
@@ -118,10 +121,13 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
             T *c = reinterpret_cast<T *>(cp.p[i]);
             T v[LP];
 #pragma unroll
-            for (int r = 0; r < LP; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
+            for (int r = 0; r < LP; ++r)
+                v[r] = lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored)
+                           ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
+                if (lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored))
+                    c[src0 + G.sa * (r * kRows)] = v[r];
         }
         return;
     }
@@ -143,14 +149,17 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
     {
         const T *f = static_cast<const T *>(t.p[0]);
 #pragma unroll
-        for (int r = 0; r < LP; ++r) v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
+        for (int r = 0; r < LP; ++r)
+            v[r] = lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored)
+                       ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
 #pragma unroll
         for (int r = 0; r < LP; ++r) tile[0][ty + r * kRows][tx] = v[r];
         if (COPY) {
             T *c = reinterpret_cast<T *>(cp.p[0]);
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
+                if (lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored))
+                    c[src0 + G.sa * (r * kRows)] = v[r];
         }
     }
     __syncthreads();
@@ -161,14 +170,16 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
             const T *f = static_cast<const T *>(t.p[i + 1]);
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                v[r] = lok[r] ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
+                v[r] = lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored)
+                           ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
         }
         const int64_t obase = (int64_t)i * G.plane + dst0;
 #pragma unroll
         for (int h = 0; h < H; ++h) {
 #pragma unroll
             for (int r = 0; r < kPer; ++r)
-                if (sok[h * kPer + r])
+                if (sok[h * kPer + r] &&
+                    FVF_IN(obase + h * kTile + G.da * (r * kRows), G.plane * nv))
                     out[obase + h * kTile + G.da * (r * kRows)] =
                         tile[buf][h * kTile + tx][ty + r * kRows];
         }
@@ -179,7 +190,8 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                 T *c = reinterpret_cast<T *>(cp.p[i + 1]);
 #pragma unroll
                 for (int r = 0; r < LP; ++r)
-                    if (lok[r]) c[src0 + G.sa * (r * kRows)] = v[r];
+                    if (lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored))
+                        c[src0 + G.sa * (r * kRows)] = v[r];
             }
         }
         __syncthreads();
@@ -206,16 +218,19 @@ pack_copy_x_kernel(FieldTable t, CopyTable cp, int nv, int64_t N1, int64_t N2, i
         const bool packed = b >= 0 && b < n2 && c >= 0 && c < n3;
         const int64_t src = a + N1 * bc;
         const int64_t dst = a + N1 * (b + n2 * c);
+        const bool sin = FVF_IN(src, N1 * N2 * N3);
         for (int i0 = 0; i0 < nv; i0 += kBatch) {
             double x[kBatch];
 #pragma unroll
             for (int r = 0; r < kBatch; ++r)
-                if (i0 + r < nv) x[r] = __ldg(static_cast<const double *>(t.p[i0 + r]) + src);
+                if (i0 + r < nv && sin)
+                    x[r] = __ldg(static_cast<const double *>(t.p[i0 + r]) + src);
 #pragma unroll
             for (int r = 0; r < kBatch; ++r) {
-                if (i0 + r < nv) {
+                if (i0 + r < nv && sin) {
                     cp.p[i0 + r][src] = x[r];
-                    if (packed) out[(int64_t)(i0 + r) * plane + dst] = x[r];
+                    if (packed && FVF_IN((int64_t)(i0 + r) * plane + dst, plane * nv))
+                        out[(int64_t)(i0 + r) * plane + dst] = x[r];
                 }
             }
         }
@@ -233,6 +248,7 @@ fields_copy_kernel(FieldTable t, CopyTable cp, int nv, int64_t total) {
     if (V2) {
         const int64_t pairs = total >> 1;
         for (int64_t e = tid; e < pairs; e += stride) {
+            if (!FVF_IN(2 * e + 1, total)) continue;
             for (int i0 = 0; i0 < nv; i0 += kBatch) {
                 double2 x[kBatch];
 #pragma unroll
@@ -264,6 +280,8 @@ fields_copy_kernel(FieldTable t, CopyTable cp, int nv, int64_t total) {
 
 }  // namespace
 
+FVF_BOUNDS_READER(read_bounds_pack)
+
 // Launch geometry of the transposing kernel for dir 1 or 2 (see above).
 static TransposeGeom transpose_geom(const Box &box, int dir, bool copy) {
     const int64_t n1 = box.n[0], n2 = box.n[1], n3 = box.n[2];
@@ -282,6 +300,7 @@ static TransposeGeom transpose_geom(const Box &box, int dir, bool copy) {
     }
     G.pnj = n1;
     G.pnq = nq;
+    G.stored = N1 * N2 * N3;
     if (copy) {
         G.nj = N1; G.nq = Nq; G.jo = 0; G.qo = 0; G.pj = g1; G.pq = gq;
     } else {

@@ -305,12 +305,14 @@ const char *fvf_status_string(int status);
 int fvf_last_cuda_error(void);
 
 /*
- * fvf_device_error -- reads and clears the device-side error flag of the
- * current device.  Kernels that wait on their own asynchronous copies
- * (diffuse3d_step's bulk-copy kernel) bound every wait; if a wait expires the
- * kernel sets this flag, lets its copies in flight finish (also bounded) and
- * returns without completing its work, so the results of that launch are
- * invalid.  *flag is set to the flag's value (0: no expired wait).
+ * fvf_device_error -- reads and clears the device-side error flags of the
+ * current device.  *flag gets a bit mask, 0 when nothing was recorded:
+ *   1  a kernel that waits on its own asynchronous copies (diffuse3d_step's
+ *      bulk-copy kernel) gave up a bounded wait, let its copies in flight
+ *      finish (also bounded) and returned without completing its work: the
+ *      results of that launch are invalid;
+ *   2  (index-checking debug builds only, libfvf_check.so) a kernel met a
+ *      global index outside its array and skipped that access.
  * Synchronises the device.  Returns FVF_OK, FVF_ERR_NULL or FVF_ERR_CUDA.
  */
 int fvf_device_error(int *flag);
