@@ -642,6 +642,34 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     # ablation: the one-thread-per-(cell, variable) mapping that the pull
     # request replaces, against the library's one-thread-per-cell kernels
     out["collapse4_vs_collapse3"] = time_ablation(torch, sw, stream, timed)
+    # ablations of the 2D FP32 diffusion kernels on the 8192^2 grid: 16-byte
+    # vectors (rows aligned) against one cell per thread (the same buffers one
+    # element in, which the library serves with its scalar kernel), and the
+    # shared-memory blocked kernel (200 steps in one call) against 200
+    # single-step calls (the vector march kernel)
+    n2 = DIFF_N * DIFF_N
+    whole_u = torch.empty(n2 + 4, dtype=torch.float32, device=sw.dev)
+    whole_v = torch.zeros_like(whole_u)
+    flat = sw.u32.reshape(-1)
+    whole_u.copy_(torch.cat([flat, flat[:4]]))
+    t_vec = timed(lambda: api.diffuse2d_step(whole_u[:n2], whole_v[:n2], DIFF_N, DIFF_N, 0.1, 1,
+                                             api.FVF_FP32, stream))
+    t_sca = timed(lambda: api.diffuse2d_step(whole_u[1:n2 + 1], whole_v[1:n2 + 1], DIFF_N, DIFF_N,
+                                             0.1, 1, api.FVF_FP32, stream))
+    out["vector_vs_scalar_fp32_step"] = {"vector_ms": round(t_vec, 4), "scalar_ms": round(t_sca, 4),
+                                         "speedup": round(t_sca / t_vec, 3)}
+
+    def single_steps():
+        for s_ in range(DIFF_STEPS):
+            a, b = (whole_u[:n2], whole_v[:n2]) if s_ % 2 == 0 else (whole_v[:n2], whole_u[:n2])
+            api.diffuse2d_step(a, b, DIFF_N, DIFF_N, 0.1, 1, api.FVF_FP32, stream)
+    t_blk = timed(lambda: api.diffuse2d_step(whole_u[:n2], whole_v[:n2], DIFF_N, DIFF_N, 0.1,
+                                             DIFF_STEPS, api.FVF_FP32, stream))
+    t_one = timed(single_steps)
+    out["blocked_vs_single_step_fp32_200steps"] = {"blocked_ms": round(t_blk, 3),
+                                                   "single_step_ms": round(t_one, 3),
+                                                   "speedup": round(t_one / t_blk, 3)}
+    del whole_u, whole_v
     # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
     # (both states live in shared memory), reported per call and per step
     u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)
