@@ -406,7 +406,7 @@ def ncu_traffic(kernel: str):
     p = ROOT / "profiles" / "ncu_traffic.txt"
     if not p.exists():
         return None
-    src_hash = source_hash()
+    src_hash = source_hash(kernel)
     for line in p.read_text().splitlines():
         m = re.match(r"^(\S+)\s+(\d+)\s+(\S+)", line.strip())
         if m and m.group(1) == kernel and m.group(3) == src_hash:
@@ -414,10 +414,26 @@ def ncu_traffic(kernel: str):
     return None
 
 
-def source_hash():
+# Source files whose code a benchmark row's kernels are built from.
+ROW_SOURCES = {
+    "diffuse_fp64": ("diffuse2d.cu", "fp64_emu.cuh", "fvf_internal.cuh"),
+    "diffuse_fp32": ("diffuse2d.cu", "fp64_emu.cuh", "fvf_internal.cuh"),
+    "pack_x": ("weno_pack.cu", "fvf_internal.cuh"),
+    "pack_y": ("weno_pack.cu", "fvf_internal.cuh"),
+    "pack_z": ("weno_pack.cu", "fvf_internal.cuh"),
+    "rhs_x": ("advect_rhs.cu", "fp64_emu.cuh", "fvf_internal.cuh"),
+    "rhs_y": ("advect_rhs.cu", "fp64_emu.cuh", "fvf_internal.cuh"),
+    "rhs_z": ("advect_rhs.cu", "fp64_emu.cuh", "fvf_internal.cuh"),
+}
+
+
+def source_hash(row: str | None = None):
+    """Hash of the kernel sources of a benchmark row (all of csrc/ for None):
+    a committed ncu traffic figure is used only while it matches."""
+    names = ROW_SOURCES.get(row) if row else None
     h = hashlib.sha256()
     for f in sorted((ROOT / "finite_volume_field_gb300" / "csrc").glob("*")):
-        if f.suffix in (".cu", ".cuh", ".h"):
+        if f.suffix in (".cu", ".cuh", ".h") and (names is None or f.name in names):
             h.update(f.name.encode())
             h.update(f.read_bytes())
     return h.hexdigest()[:12]

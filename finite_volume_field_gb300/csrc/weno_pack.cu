@@ -86,19 +86,12 @@ struct TransposeGeom {
     int64_t stored;  // elements of one field's stored box (index checks)
 };
 
-// Halves of the tile along a (one 32-wide half for both element sizes; a
-// 64-wide tile for 4-byte elements measured slower).
-template <typename T>
-__host__ __device__ constexpr int tile_halves() { return 1; }
-
 template <typename T, bool COPY>
 __global__ void __launch_bounds__(kTile * kRows)
 pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                       T *__restrict__ out) {
-    constexpr int H = tile_halves<T>();
-    constexpr int TA = kTile * H;        // tile extent along a
-    constexpr int LP = TA / kRows;       // loads per thread and variable
-    constexpr int SP = kPer * H;         // stores per thread and variable
+    constexpr int TA = kTile;            // tile extent along a
+    constexpr int LP = kPer;             // loads per thread and variable
     __shared__ T tile[2][TA][kTile + 1];
     int64_t blk = blockIdx.x;
     const int64_t ta = blk % G.tiles_a;
@@ -131,18 +124,14 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
         }
         return;
     }
-    // store side: lanes along a (contiguous in the output, one 32-wide half
-    // of the tile at a time), rows along j
+    // store side: lanes along a (contiguous in the output), rows along j
     const int64_t jp0 = j0 + ty - G.pj;
     const int64_t dst0 = a0 + tx + G.da * jp0 + G.dq * qp;
-    bool sok[SP];
+    bool sok[kPer];
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-#pragma unroll
-        for (int r = 0; r < kPer; ++r) {
-            const int64_t jp = jp0 + r * kRows;
-            sok[h * kPer + r] = a0 + h * kTile + tx < G.na && jp >= 0 && jp < G.pnj;
-        }
+    for (int r = 0; r < kPer; ++r) {
+        const int64_t jp = jp0 + r * kRows;
+        sok[r] = a0 + tx < G.na && jp >= 0 && jp < G.pnj;
     }
 
     T v[LP];
@@ -175,14 +164,9 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
         }
         const int64_t obase = (int64_t)i * G.plane + dst0;
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-#pragma unroll
-            for (int r = 0; r < kPer; ++r)
-                if (sok[h * kPer + r] &&
-                    FVF_IN(obase + h * kTile + G.da * (r * kRows), G.plane * nv))
-                    out[obase + h * kTile + G.da * (r * kRows)] =
-                        tile[buf][h * kTile + tx][ty + r * kRows];
-        }
+        for (int r = 0; r < kPer; ++r)
+            if (sok[r] && FVF_IN(obase + G.da * (r * kRows), G.plane * nv))
+                out[obase + G.da * (r * kRows)] = tile[buf][tx][ty + r * kRows];
         if (more) {
 #pragma unroll
             for (int r = 0; r < LP; ++r) tile[buf ^ 1][ty + r * kRows][tx] = v[r];
@@ -314,9 +298,7 @@ static TransposeGeom transpose_geom(const Box &box, int dir, bool copy) {
 template <typename T, bool COPY>
 static cudaError_t launch_transpose(const FieldTable &fields, const CopyTable &copies, int nv,
                                     const Box &box, int dir, T *out, cudaStream_t stream) {
-    TransposeGeom G = transpose_geom(box, dir, COPY);
-    constexpr int TA = kTile * tile_halves<T>();
-    G.tiles_a = (G.na + TA - 1) / TA;
+    const TransposeGeom G = transpose_geom(box, dir, COPY);
     const int64_t blocks = G.tiles_a * G.tiles_j * G.nq;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
     pack_transpose_kernel<T, COPY><<<(unsigned)blocks, dim3(kTile, kRows), 0, stream>>>(
