@@ -248,8 +248,9 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
 
 template <typename T>
 int march_blocks_per_sm() {
-    static int cached = 0;
-    if (cached == 0) {
+    static int cached[64] = {0};  // per device; a repeated fill writes the same value
+    const int d = device_slot();
+    if (cached[d] == 0) {
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, diffuse_march_kernel<T>,
                                                           kMarchThreads, 0) != cudaSuccess ||
@@ -257,9 +258,9 @@ int march_blocks_per_sm() {
             cudaGetLastError();
             n = 8;
         }
-        cached = n;
+        cached[d] = n;
     }
-    return cached;
+    return cached[d];
 }
 
 // ---------------------------------------------------------------------------
@@ -500,16 +501,20 @@ int cluster_band(int64_t nx, int64_t ny, int64_t nsteps) {
     return (int)band;
 }
 
+// The dynamic shared-memory attribute, set once per device.
 template <typename T>
 cudaError_t cluster_prepare() {
-    static cudaError_t status = cudaErrorNotReady;
-    if (status == cudaErrorNotReady) {
-        status = cudaFuncSetAttribute(diffuse_cluster_kernel<T>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kClusterMaxBytes);
-        if (status != cudaSuccess) cudaGetLastError();
+    static cudaError_t status[64] = {};
+    static bool done[64] = {};
+    const int d = device_slot();
+    if (!done[d]) {
+        status[d] = cudaFuncSetAttribute(diffuse_cluster_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kClusterMaxBytes);
+        if (status[d] != cudaSuccess) cudaGetLastError();
+        done[d] = true;
     }
-    return status;
+    return status[d];
 }
 
 constexpr size_t tblock_smem_bytes(size_t elem) { return 2 * (size_t)kTbW * kTbH * elem; }
@@ -529,14 +534,17 @@ bool use_tblock(int64_t nx, int64_t ny, int64_t nsteps) {
 
 template <typename T>
 cudaError_t tblock_prepare() {
-    static cudaError_t status = cudaErrorNotReady;
-    if (status == cudaErrorNotReady) {
-        status = cudaFuncSetAttribute(diffuse_tblock_kernel<T>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)tblock_smem_bytes(sizeof(T)));
-        if (status != cudaSuccess) cudaGetLastError();
+    static cudaError_t status[64] = {};
+    static bool done[64] = {};
+    const int d = device_slot();
+    if (!done[d]) {
+        status[d] = cudaFuncSetAttribute(diffuse_tblock_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tblock_smem_bytes(sizeof(T)));
+        if (status[d] != cudaSuccess) cudaGetLastError();
+        done[d] = true;
     }
-    return status;
+    return status[d];
 }
 
 // One-step launches (march or scalar kernel), configured once per call.

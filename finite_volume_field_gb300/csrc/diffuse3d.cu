@@ -471,7 +471,8 @@ cudaError_t launch_bulk(const CUtensorMap &src_map, T *dst, int64_t nx, int64_t 
                         T alpha, cudaStream_t stream) {
     constexpr int TX = 32 * (16 / sizeof(T));
     constexpr size_t smem = bulk_smem_bytes<T>();
-    static int per_sm = 0;
+    static int per_sm_dev[64] = {0};  // per device: the attribute and occupancy
+    int &per_sm = per_sm_dev[device_slot()];
     if (per_sm == 0) {
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(diffuse3d_bulk_kernel<T>,

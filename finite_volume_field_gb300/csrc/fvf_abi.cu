@@ -26,6 +26,15 @@ namespace fvf {
 static std::atomic<uint64_t> g_launches{0};
 static thread_local int g_last_cuda_error = 0;
 
+int device_slot() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+        cudaGetLastError();
+        return 0;
+    }
+    return dev < 63 ? dev : 63;
+}
+
 int sm_count() {
     static int cached[64] = {0};
     int dev = 0;

@@ -82,6 +82,10 @@ struct RkStageArgs {
 // Multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Index of the current device in the per-device caches of the launchers
+// (0..63; devices beyond 63 share the last slot).
+int device_slot();
+
 // Each launcher enqueues its kernels on `stream`, adds the number of kernels
 // it launched to *launches and returns the first launch error (cudaSuccess
 // if none).  Arguments have already been validated by the caller.
