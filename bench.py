@@ -49,6 +49,10 @@ FALLBACK_HBM_GBS = 6800.0
 FP64_NOMINAL_TFLOPS = 1.25   # FP64 rate of the part (FMA counted as 2 flops)
 # Algorithmic FP64 flops per output element of the FP64 arithmetic sweeps.
 FP64_FLOPS = {"diffuse_fp64": 7, "rhs_x": 2, "rhs_y": 2, "rhs_z": 2}
+# FP64-unit instructions per element as built: the diffusion update has 6
+# (3 sums, the fused s - 4c, the multiply, the add), 2 of the sums run on the
+# integer pipes; the flux difference has a subtraction and a multiplication.
+FP64_INSTR = {"diffuse_fp64": 4, "rhs_x": 2, "rhs_y": 2, "rhs_z": 2}
 
 # ---------------------------------------------------------------------------
 # Workload definition (sizes, compulsory bytes, cell-var counts)
@@ -716,7 +720,23 @@ def load_ablation():
     lib.ablation_pack_x_collapse4.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint,
                                               vp, vp]
     lib.ablation_rhs_x_collapse4.argtypes = [vp, vp, cint, ctypes.POINTER(i64), vp, vp]
+    lib.bench_issue_rate.argtypes = [cint, cint, ctypes.POINTER(ctypes.c_double)]
     return lib
+
+
+def measured_issue_rates():
+    """Arithmetic issue rates of this GPU from the probes in the benchmark
+    library (operations per second; an FMA counts once): the denominators of
+    the FP64-bound rows."""
+    import ctypes
+    lib = load_ablation()
+    names = {0: "fp64_add", 1: "fp64_mul", 2: "fp64_fma", 3: "fp32_fma", 4: "int32_alu"}
+    out = {}
+    for op, name in names.items():
+        r = ctypes.c_double(0.0)
+        if lib.bench_issue_rate(op, 3, ctypes.byref(r)) == 0:
+            out[name] = round(r.value / 1e12, 4)
+    return out   # T operations per second
 
 
 def time_ablation(torch, sw, stream, timed):
@@ -855,6 +875,7 @@ def run_gpu(args):
     del sw2
 
     extras = time_extra_sweeps(torch, sw, stream)
+    rates = measured_issue_rates() if rank == 0 else {}
 
     mine = {"ms_per_step": ms_per_step, "e2e_ms_per_step": e2e_ms, "launches": launches}
     if world > 1:
@@ -907,6 +928,16 @@ def run_gpu(args):
                 roof.update(bound="alu", achieved=roof["fp64"]["achieved"],
                             peak=FP64_NOMINAL_TFLOPS, unit="TFLOP/s", frac=roof["fp64"]["frac"],
                             peak_source="nominal FP64 rate of the part (recipe unit table)")
+            # the same launch against this GPU's measured FP64 issue rate:
+            # the FP64-unit instructions the kernel issues per element as
+            # built (FP64_INSTR), over the launch time
+            peak_ops = rates.get("fp64_fma")
+            if peak_ops:
+                ops = FP64_INSTR[dom] * r["per_launch_cells"] / (launch_ms * 1e-3) / 1e12
+                roof["fp64_issue"] = {"achieved_tops": round(ops, 4),
+                                      "measured_peak_tops": peak_ops,
+                                      "frac": round(ops / peak_ops, 4),
+                                      "instructions_per_element": FP64_INSTR[dom]}
         line = {
             "impl": "gb300", "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -926,6 +957,7 @@ def run_gpu(args):
                     "ms_per_step": round(e2e_ms, 3), "steps": e2e_steps},
             "gpu_launches": launches,
             "clocks": clocks,
+            "measured_rates_tops": rates,
             "extra_sweeps": extras,
         }
         if world == 1 and not args.no_cpu_baseline:
