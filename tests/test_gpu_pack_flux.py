@@ -192,6 +192,49 @@ def test_multivar_sequence_4800x1200():
     assert_bits_equal(to_host(ry), wry, what="rhs y")
 
 
+def test_multivar_sequence_4800x1200_as_cuda_graph():
+    """The same sequence in the launch configuration the benchmark times: the
+    100 repetitions captured once into a CUDA graph through the same library
+    calls, then replayed twice; outputs (cleared before the replays) compared
+    with the oracle."""
+    torch = torch_cuda()
+    extents, g, nv = (4800, 1200, 1), 2, 7
+    seed = inputs.config_seed(5)
+    fields = inputs.multivar_fields_2d(seed, extents, g)
+    fx = inputs.face_fluxes(seed, nv, extents, 0)
+    fy = inputs.face_fluxes(seed, nv, extents, 1)
+    wx = inputs.inverse_spacing(seed, 4800, stream=200)
+    wy = inputs.inverse_spacing(seed, 1200, stream=201)
+    df = [to_dev(f) for f in fields]
+    dfx, dfy, dwx, dwy = to_dev(fx), to_dev(fy), to_dev(wx), to_dev(wy)
+    px = torch.zeros(4804 * 1200 * nv, dtype=torch.float64, device="cuda")
+    py = torch.zeros(1204 * 4800 * nv, dtype=torch.float64, device="cuda")
+    rx = torch.zeros(4800 * 1200 * nv, dtype=torch.float64, device="cuda")
+    ry = torch.zeros_like(rx)
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    n0 = api.launch_count()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        s = torch.cuda.current_stream()
+        for _ in range(100):
+            api.weno_pack(df, nv, extents, g, 0, px, s)
+            api.weno_pack(df, nv, extents, g, 1, py, s)
+            api.advect_rhs(dfx, dwx, nv, extents, 0, rx, s)
+            api.advect_rhs(dfy, dwy, nv, extents, 1, ry, s)
+    assert api.launch_count() - n0 == 400
+    for t in (px, py, rx, ry):
+        t.zero_()
+    torch.cuda.synchronize()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    wpx, wpy, wrx, wry = oracle.multivar_sweep_2d(fields, fx, fy, wx, wy, nv, extents, g)
+    assert_bits_equal(to_host(px), wpx, what="pack x")
+    assert_bits_equal(to_host(py), wpy, what="pack y")
+    assert_bits_equal(to_host(rx), wrx, what="rhs x")
+    assert_bits_equal(to_host(ry), wry, what="rhs y")
+
+
 # ---------------------------------------------------------------------------
 # Accumulating flux difference and the directional flux copy (unpack)
 # ---------------------------------------------------------------------------
