@@ -86,28 +86,35 @@ struct TransposeGeom {
     int64_t stored;  // elements of one field's stored box (index checks)
 };
 
-template <typename T, bool COPY>
+template <typename T, bool COPY, typename Idx>
 __global__ void __launch_bounds__(kTile * kRows)
 pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                       T *__restrict__ out) {
+    // geometry in the index type of this instantiation: 32-bit when every
+    // index the block forms fits (the launcher checks), else 64-bit
+    const Idx na = (Idx)G.na, nj = (Idx)G.nj, jo = (Idx)G.jo, qo = (Idx)G.qo;
+    const Idx pj = (Idx)G.pj, pq = (Idx)G.pq, pnj = (Idx)G.pnj, pnq = (Idx)G.pnq;
+    const Idx sa = (Idx)G.sa, sq = (Idx)G.sq, da = (Idx)G.da, dq = (Idx)G.dq;
+    const Idx plane = (Idx)G.plane, tiles_a = (Idx)G.tiles_a, tiles_j = (Idx)G.tiles_j;
+    const Idx stored = (Idx)G.stored;
     constexpr int TA = kTile;            // tile extent along a
     constexpr int LP = kPer;             // loads per thread and variable
     __shared__ T tile[2][TA][kTile + 1];
-    int64_t blk = blockIdx.x;
-    const int64_t ta = blk % G.tiles_a;
-    blk /= G.tiles_a;
-    const int64_t tj = blk % G.tiles_j;
-    const int64_t q = blk / G.tiles_j;
-    const int64_t a0 = ta * TA, j0 = tj * kTile;
+    Idx blk = (Idx)blockIdx.x;
+    const Idx ta = blk % tiles_a;
+    blk /= tiles_a;
+    const Idx tj = blk % tiles_j;
+    const Idx q = blk / tiles_j;
+    const Idx a0 = ta * TA, j0 = tj * kTile;
     const int tx = threadIdx.x, ty = threadIdx.y;
     // load side: lanes along j (contiguous in the field), rows along a
-    const int64_t jl = j0 + tx;
-    const int64_t src0 = (jl + G.jo) + G.sa * (a0 + ty) + G.sq * (q + G.qo);
+    const Idx jl = j0 + tx;
+    const Idx src0 = (jl + jo) + sa * (a0 + ty) + sq * (q + qo);
     bool lok[LP];
 #pragma unroll
-    for (int r = 0; r < LP; ++r) lok[r] = jl < G.nj && a0 + ty + r * kRows < G.na;
-    const int64_t qp = q - G.pq;
-    if (COPY && (qp < 0 || qp >= G.pnq)) {
+    for (int r = 0; r < LP; ++r) lok[r] = jl < nj && a0 + ty + r * kRows < na;
+    const Idx qp = q - pq;
+    if (COPY && (qp < 0 || qp >= pnq)) {
         // a transverse ghost slice: copied, not packed (block-uniform branch)
         for (int i = 0; i < nv; ++i) {
             const T *f = static_cast<const T *>(t.p[i]);
@@ -115,23 +122,23 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
             T v[LP];
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                v[r] = lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored)
-                           ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
+                v[r] = lok[r] && FVF_IN(src0 + sa * (r * kRows), stored)
+                           ? __ldg(f + src0 + sa * (r * kRows)) : T(0);
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                if (lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored))
-                    c[src0 + G.sa * (r * kRows)] = v[r];
+                if (lok[r] && FVF_IN(src0 + sa * (r * kRows), stored))
+                    c[src0 + sa * (r * kRows)] = v[r];
         }
         return;
     }
     // store side: lanes along a (contiguous in the output), rows along j
-    const int64_t jp0 = j0 + ty - G.pj;
-    const int64_t dst0 = a0 + tx + G.da * jp0 + G.dq * qp;
+    const Idx jp0 = j0 + ty - pj;
+    const Idx dst0 = a0 + tx + da * jp0 + dq * qp;
     bool sok[kPer];
 #pragma unroll
     for (int r = 0; r < kPer; ++r) {
-        const int64_t jp = jp0 + r * kRows;
-        sok[r] = a0 + tx < G.na && jp >= 0 && jp < G.pnj;
+        const Idx jp = jp0 + r * kRows;
+        sok[r] = a0 + tx < na && jp >= 0 && jp < pnj;
     }
 
     T v[LP];
@@ -139,16 +146,16 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
         const T *f = static_cast<const T *>(t.p[0]);
 #pragma unroll
         for (int r = 0; r < LP; ++r)
-            v[r] = lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored)
-                       ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
+            v[r] = lok[r] && FVF_IN(src0 + sa * (r * kRows), stored)
+                       ? __ldg(f + src0 + sa * (r * kRows)) : T(0);
 #pragma unroll
         for (int r = 0; r < LP; ++r) tile[0][ty + r * kRows][tx] = v[r];
         if (COPY) {
             T *c = reinterpret_cast<T *>(cp.p[0]);
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                if (lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored))
-                    c[src0 + G.sa * (r * kRows)] = v[r];
+                if (lok[r] && FVF_IN(src0 + sa * (r * kRows), stored))
+                    c[src0 + sa * (r * kRows)] = v[r];
         }
     }
     __syncthreads();
@@ -159,14 +166,14 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
             const T *f = static_cast<const T *>(t.p[i + 1]);
 #pragma unroll
             for (int r = 0; r < LP; ++r)
-                v[r] = lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored)
-                           ? __ldg(f + src0 + G.sa * (r * kRows)) : T(0);
+                v[r] = lok[r] && FVF_IN(src0 + sa * (r * kRows), stored)
+                           ? __ldg(f + src0 + sa * (r * kRows)) : T(0);
         }
-        const int64_t obase = (int64_t)i * G.plane + dst0;
+        const Idx obase = (Idx)i * plane + dst0;
 #pragma unroll
         for (int r = 0; r < kPer; ++r)
-            if (sok[r] && FVF_IN(obase + G.da * (r * kRows), G.plane * nv))
-                out[obase + G.da * (r * kRows)] = tile[buf][tx][ty + r * kRows];
+            if (sok[r] && FVF_IN(obase + da * (r * kRows), plane * nv))
+                out[obase + da * (r * kRows)] = tile[buf][tx][ty + r * kRows];
         if (more) {
 #pragma unroll
             for (int r = 0; r < LP; ++r) tile[buf ^ 1][ty + r * kRows][tx] = v[r];
@@ -174,8 +181,8 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                 T *c = reinterpret_cast<T *>(cp.p[i + 1]);
 #pragma unroll
                 for (int r = 0; r < LP; ++r)
-                    if (lok[r] && FVF_IN(src0 + G.sa * (r * kRows), G.stored))
-                        c[src0 + G.sa * (r * kRows)] = v[r];
+                    if (lok[r] && FVF_IN(src0 + sa * (r * kRows), stored))
+                        c[src0 + sa * (r * kRows)] = v[r];
             }
         }
         __syncthreads();
@@ -301,8 +308,18 @@ static cudaError_t launch_transpose(const FieldTable &fields, const CopyTable &c
     const TransposeGeom G = transpose_geom(box, dir, COPY);
     const int64_t blocks = G.tiles_a * G.tiles_j * G.nq;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-    pack_transpose_kernel<T, COPY><<<(unsigned)blocks, dim3(kTile, kRows), 0, stream>>>(
-        fields, copies, nv, G, out);
+    // 32-bit indices (fewer registers, more blocks per SM: 4-8% faster at
+    // 8 x 207^3) while every index a block forms, including those of the rows
+    // and columns past the box edge that it computes but does not use, fits
+    const int64_t lim = (int64_t)1 << 31;
+    const bool narrow = G.stored + 8 * G.sa + G.sq + 64 < lim &&
+                        G.plane * nv + 40 * G.da + G.dq + 64 < lim && blocks < lim;
+    if (narrow)
+        pack_transpose_kernel<T, COPY, int32_t><<<(unsigned)blocks, dim3(kTile, kRows), 0,
+                                                  stream>>>(fields, copies, nv, G, out);
+    else
+        pack_transpose_kernel<T, COPY, int64_t><<<(unsigned)blocks, dim3(kTile, kRows), 0,
+                                                  stream>>>(fields, copies, nv, G, out);
     return cudaSuccess;
 }
 
