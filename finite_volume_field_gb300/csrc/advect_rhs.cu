@@ -7,10 +7,15 @@
 // along the swept axis c, one subtraction then one multiplication, each
 // rounded to nearest even (round-to-nearest intrinsics, never contracted), in
 // binary64 or, for the FP32 entry points, binary32.
-// Two FP64 operations per element keep this kernel on GB300's FP64 unit:
-// moving the subtraction to the integer pipes (fp64_emu.cuh) was measured
-// slower here (the integer ALU pipe saturates first), unlike in the
-// diffusion update.
+// Two FP64 operations per element would keep this kernel on GB300's FP64
+// unit, well below the HBM roof.  The multiplication by inv_d runs on the
+// integer pipes instead (fp64_emu.cuh: an exact binary64 product, the factor
+// prepared once per cell) for three of every four variables
+// (FVF_RHS_EMU_MUL = 7, one bit per slot of a load batch); on GB300 this
+// measured 20-26% faster than all-FP64 and than emulating all four (the
+// integer pipes saturate then).  Moving the subtraction instead measured
+// slower: the exact addition costs about twice the integer instructions of
+// the product.
 //
 // Mapping ("Why this is faster" on the same page): one thread per spatial
 // cell; the inverse spacing is loaded once per cell, outside the variable
@@ -22,6 +27,9 @@
 
 #ifndef FVF_RHS_EMU
 #define FVF_RHS_EMU 0
+#endif
+#ifndef FVF_RHS_EMU_MUL
+#define FVF_RHS_EMU_MUL 7
 #endif
 
 namespace fvf {
@@ -44,8 +52,31 @@ __device__ __forceinline__ double face_diff(double lo, double hi) {
 // FP32 form: binary32 operations, each rounded to nearest even.
 template <int Q>
 __device__ __forceinline__ float face_diff(float lo, float hi) { return __fsub_rn(lo, hi); }
-__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
-__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+// inv_d(c) times a face difference: on the FP64 unit, or on the integer
+// pipes (fp64_emu.cuh, the factor prepared once per cell) for the variable
+// slots whose bit is set in FVF_RHS_EMU_MUL.
+template <typename T>
+struct Scale;
+
+template <>
+struct Scale<double> {
+    double w;
+    emu::MulConst m;
+    __device__ explicit Scale(double w_) : w(w_), m(emu::mul_const(w_)) {}
+    template <int Q>
+    __device__ __forceinline__ double apply(double d) const {
+        if ((FVF_RHS_EMU_MUL >> Q) & 1) return emu::from_bits(emu::mul_const_bits(emu::bits(d), m));
+        return __dmul_rn(w, d);
+    }
+};
+
+template <>
+struct Scale<float> {
+    float w;
+    __device__ explicit Scale(float w_) : w(w_) {}
+    template <int Q>
+    __device__ __forceinline__ float apply(float d) const { return __fmul_rn(w, d); }
+};
 __device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
 __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
 
@@ -75,7 +106,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
     const T wjk = DIR == 0 ? (FVF_IN(j, nw) ? __ldg(inv_d + j) : T(0))
                            : (DIR == 1 ? (FVF_IN(k, nw) ? __ldg(inv_d + k) : T(0)) : T(0));
     for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
-        const T w = DIR == 2 ? (FVF_IN(l, nw) ? __ldg(inv_d + l) : T(0)) : wjk;
+        const Scale<T> w(DIR == 2 ? (FVF_IN(l, nw) ? __ldg(inv_d + l) : T(0)) : wjk);
         const int64_t lo = (int64_t)j + F1 * ((int64_t)k + F2 * l);  // face c-1 at position c
         const int64_t ro = (int64_t)jk + (int64_t)plane * l;
         const T *f = flux + lo;
@@ -96,7 +127,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
             }
 #define FVF_RHS_Q(Q)                                                                    \
     if (Q < kGroup && i0 + Q < nv) {                                                    \
-        const T term = mul_rn(w, face_diff<Q>(a[Q], b[Q]));                            \
+        const T term = w.template apply<Q>(face_diff<Q>(a[Q], b[Q]));                  \
         /* accumulate form: the term added once to the existing rhs */                 \
         if (FVF_IN(ro + (int64_t)(i0 + Q) * rplane, rall))                              \
             r[(int64_t)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;         \

@@ -42,11 +42,19 @@ namespace cg = cooperative_groups;
 //   FVF_FP64_EMU_SUMS: how many of the three neighbour sums (W+E, +S, +N, in
 //                      that order) run on the integer pipes (0..3);
 //   FVF_FP64_EMU_T:    1 to also compute s - 4c on the integer pipes.
+//   FVF_FP64_EMU_MUL:  1 to compute alpha * (s - 4c) on the integer pipes.
+//   FVF_FP64_EMU_LAST: 1 to compute the final c + alpha * (s - 4c) there.
 #ifndef FVF_FP64_EMU_SUMS
 #define FVF_FP64_EMU_SUMS 2
 #endif
 #ifndef FVF_FP64_EMU_T
 #define FVF_FP64_EMU_T 0
+#endif
+#ifndef FVF_FP64_EMU_MUL
+#define FVF_FP64_EMU_MUL 0
+#endif
+#ifndef FVF_FP64_EMU_LAST
+#define FVF_FP64_EMU_LAST 0
 #endif
 
 namespace fvf {
@@ -112,7 +120,16 @@ __device__ __forceinline__ double update<double>(double c, double w, double e, d
 #else
     t = Rn<double>::sub4(sum, c);
 #endif
-    return __dadd_rn(c, __dmul_rn(alpha, t));
+#if FVF_FP64_EMU_MUL
+    const double p = emu::from_bits(emu::mul_const_bits(emu::bits(t), emu::mul_const(alpha)));
+#else
+    const double p = __dmul_rn(alpha, t);
+#endif
+#if FVF_FP64_EMU_LAST
+    return emu::add(c, p);
+#else
+    return __dadd_rn(c, p);
+#endif
 }
 
 // ---------------------------------------------------------------------------

@@ -43,11 +43,17 @@
 #include "fvf_internal.cuh"
 #include "mbarrier.cuh"
 
-// Number of the five neighbour sums (W+E, +S, +N, +B, +T, in that order) that
-// the FP64 update runs on the integer pipes (fp64_emu.cuh); every choice gives
-// the same bits.
+// How the FP64 update splits its work between the FP64 unit and the integer
+// pipes (fp64_emu.cuh); every choice gives the same bits.  FVF_3D_EMU_SUMS:
+// how many of the five neighbour sums (W+E, +S, +N, +B, +T, in that order)
+// run on the integer pipes; FVF_3D_EMU_MUL: bit 1 the product alpha * (...),
+// bit 2 the product 6c.  Two sums and both products measured fastest on
+// GB300 (6% below three sums and no product).
 #ifndef FVF_3D_EMU_SUMS
-#define FVF_3D_EMU_SUMS 3
+#define FVF_3D_EMU_SUMS 2
+#endif
+#ifndef FVF_3D_EMU_MUL
+#define FVF_3D_EMU_MUL 3
 #endif
 // 1: aligned FP32 grids take the bulk-copy kernel; 0: the register march
 // kernel.  FP64 always takes the march kernel, which measured faster there
@@ -65,14 +71,21 @@ __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, 
 __device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
 __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
 __device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
-__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
-__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
 
 template <int I>
 __device__ __forceinline__ float sum_rn(float a, float b) { return __fadd_rn(a, b); }
 template <int I>
 __device__ __forceinline__ double sum_rn(double a, double b) {
     return I < FVF_3D_EMU_SUMS ? emu::add_same_sign(a, b) : __dadd_rn(a, b);
+}
+
+// k * x with the factor k fixed for the sweep
+template <int BIT>
+__device__ __forceinline__ float mulk_rn(float k, float x) { return __fmul_rn(k, x); }
+template <int BIT>
+__device__ __forceinline__ double mulk_rn(double k, double x) {
+    if (FVF_3D_EMU_MUL & BIT) return emu::from_bits(emu::mul_const_bits(emu::bits(x), emu::mul_const(k)));
+    return __dmul_rn(k, x);
 }
 
 template <typename T>
@@ -82,7 +95,7 @@ __device__ __forceinline__ T update3(T c, T w, T e, T s, T n, T b, T t, T alpha)
     x = sum_rn<2>(x, n);
     x = sum_rn<3>(x, b);
     x = sum_rn<4>(x, t);
-    return add_rn(c, mul_rn(alpha, sub_rn(x, mul_rn(T(6), c))));
+    return add_rn(c, mulk_rn<1>(alpha, sub_rn(x, mulk_rn<2>(T(6), c))));
 }
 
 template <typename T, int V>

@@ -1,13 +1,14 @@
-// fp64_emu.cuh -- IEEE 754 binary64 addition on the integer pipes.
+// fp64_emu.cuh -- IEEE 754 binary64 addition and multiplication on the
+// integer pipes.
 //
 // GB300 issues FP64 adds, multiplies and FMAs at about 1/70 of its FP32 and
 // integer rate, so a sweep doing a few FP64 operations per element is bound
 // by the FP64 pipe well below the HBM roof.  The functions here compute the
-// correctly rounded (round-to-nearest-even) binary64 sum with 32/64-bit
-// integer instructions, which run on the full-rate pipes in parallel with the
-// FP64 unit, and contain no FP64 instruction at all.  The result is
-// bit-identical to a hardware add for every input except that every NaN
-// result is the one quiet NaN 0x7FFFFFFFFFFFFFFF.
+// correctly rounded (round-to-nearest-even) binary64 sum and product with
+// 32/64-bit integer instructions, which run on the full-rate pipes in
+// parallel with the FP64 unit, and contain no FP64 instruction at all.  The
+// result is bit-identical to a hardware add or multiply for every input
+// except that every NaN result is the one quiet NaN 0x7FFFFFFFFFFFFFFF.
 //
 // Method: the textbook binary floating-point addition (J.-M. Muller et al.,
 // "Handbook of Floating-Point Arithmetic", 2nd ed., chapter 7; D. Goldberg,
@@ -215,6 +216,127 @@ FVF_HD uint64_t add_same_sign_bits(uint64_t A, uint64_t B) {
 }
 
 FVF_HD double add(double a, double b) { return from_bits(add_bits(bits(a), bits(b))); }
+
+// ---------------------------------------------------------------------------
+// Multiplication.  The same textbook method (Muller et al., chapter 7): the
+// product of the two 53-bit significands, both placed at the top of a 64-bit
+// word, is a 128-bit value with its leading one in bit 127 or 126; a one-bit
+// normalisation, a sticky bit for the low 64 bits, and the rounding and
+// packing of the addition above.  The 64 x 64-bit product is formed from
+// four 32 x 32 -> 64-bit products, integer multiply-adds that issue on the
+// FMA pipe rather than the ALU pipe the additions load.
+// ---------------------------------------------------------------------------
+
+// hi:lo = a * b exactly.  Every partial sum stays below 2^64.
+FVF_HD void mul_64x64(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo) {
+    const uint32_t al = (uint32_t)a, ah = (uint32_t)(a >> 32);
+    const uint32_t bl = (uint32_t)b, bh = (uint32_t)(b >> 32);
+    const uint64_t p0 = (uint64_t)al * bl;
+    const uint64_t p1 = (uint64_t)al * bh + (p0 >> 32);
+    const uint64_t p2 = (uint64_t)ah * bl + (uint32_t)p1;
+    *hi = (uint64_t)ah * bh + (p1 >> 32) + (p2 >> 32);
+    *lo = (p2 << 32) | (uint32_t)p0;
+}
+
+// Complete binary64 multiplication in integer arithmetic, every input: NaN
+// and infinity rules (inf * 0 is NaN), signed zeros, subnormal operands
+// (normalised first), gradual underflow with a sticky bit, overflow to
+// infinity.
+FVF_HD uint64_t mul_full_int(uint64_t A, uint64_t B) {
+    const uint64_t sgn = (A ^ B) & kSign;
+    const uint64_t mA = A & ~kSign, mB = B & ~kSign;
+    if (mA > kInf || mB > kInf) return kQuietNaN;
+    if (mA == kInf || mB == kInf) return (mA == 0 || mB == 0) ? kQuietNaN : (sgn | kInf);
+    if (mA == 0 || mB == 0) return sgn;
+    int ea = (int)(mA >> 52), eb = (int)(mB >> 52);
+    uint64_t fa = mA & kFrac, fb = mB & kFrac;
+    if (ea) {
+        fa |= kHidden;
+    } else {                                     // subnormal: leading one up to bit 52
+        const int sh = clz64(fa) - 11;
+        fa <<= sh;
+        ea = 1 - sh;
+    }
+    if (eb) {
+        fb |= kHidden;
+    } else {
+        const int sh = clz64(fb) - 11;
+        fb <<= sh;
+        eb = 1 - sh;
+    }
+    uint64_t hi, lo;
+    mul_64x64(fa << 11, fb << 11, &hi, &lo);     // in [2^126, 2^128)
+    const uint32_t c = (uint32_t)(hi >> 63);
+    if (!c) {                                    // leading one to bit 127
+        hi = (hi << 1) | (lo >> 63);
+        lo <<= 1;
+    }
+    uint64_t s = hi | (uint64_t)(lo != 0);       // sticky
+    int e = ea + eb - 1023 + (int)c;             // biased exponent of the result
+    if (e < 1) {                                 // below the normal range
+        const int sh = 1 - e;
+        uint64_t t = sh < 64 ? (s >> sh) : 0;
+        t |= (uint64_t)(sh < 64 ? ((t << sh) != s) : (s != 0));
+        s = t;
+        e = 1;
+    }
+    uint64_t mant = s >> 11;
+    const uint32_t rb = (uint32_t)s & 0x7FFu;
+    mant += (rb + (uint32_t)(mant & 1) + 0x3FFu) >> 11;
+    if (e >= 0x7FF) return sgn | kInf;
+    return sgn | (((uint64_t)(e - 1) << 52) + mant);
+}
+
+// One factor fixed for a whole sweep (the diffusion coefficient): its
+// significand placed at the top of a 64-bit word and its exponent, prepared
+// once.  `fast` is 0 when the factor is zero, subnormal, infinite or NaN;
+// every product then takes the complete algorithm.
+struct MulConst {
+    uint64_t bits;   // the factor's bit pattern
+    uint64_t k;      // significand << 11, in [2^63, 2^64)
+    uint64_t sign;   // its sign bit
+    int32_t adj;     // biased exponent - 1023
+    uint32_t fast;
+};
+
+FVF_HD MulConst mul_const(double alpha) {
+    MulConst m;
+    m.bits = bits(alpha);
+    const uint32_t e = (uint32_t)(m.bits >> 52) & 0x7FFu;
+    m.k = ((m.bits & kFrac) | kHidden) << 11;
+    m.sign = m.bits & kSign;
+    m.adj = (int32_t)e - 1023;
+    m.fast = (e - 1u) < 2046u;
+    return m;
+}
+
+// Fast path of t * alpha: t normal and the result normal (before rounding),
+// which leaves no special case.  The sticky bit from the low product half
+// makes every rounding exact, ties included.
+FVF_HD bool mul_const_fast_int(uint64_t T, const MulConst &m, uint64_t *out) {
+    const uint32_t th = (uint32_t)(T >> 32), tl = (uint32_t)T;
+    const uint32_t et = (th >> 20) & 0x7FFu;
+    // the significand with its implicit one, shifted to the top of the word
+    const uint64_t ft = ((uint64_t)(th | 0x00100000u) << 43) | ((uint64_t)tl << 11);
+    uint64_t hi, lo;
+    mul_64x64(ft, m.k, &hi, &lo);
+    const uint32_t c = (uint32_t)(hi >> 63);
+    const uint64_t s = hi << (c ^ 1u);
+    const int e = (int)et + m.adj + (int)c;
+    uint64_t mant = s >> 11;
+    const uint32_t rb = ((uint32_t)s & 0x7FFu) | (uint32_t)(lo != 0);
+    mant += (rb + (uint32_t)(mant & 1) + 0x3FFu) >> 11;
+    *out = ((T & kSign) ^ m.sign) | (((uint64_t)(e - 1) << 52) + mant);
+    return m.fast & ((et - 1u) < 2046u) & ((uint32_t)(e - 1) < 2046u);
+}
+
+FVF_HD uint64_t mul_const_bits(uint64_t T, const MulConst &m) {
+    uint64_t r;
+    if (!mul_const_fast_int(T, m, &r)) r = mul_full_int(T, m.bits);
+    return r;
+}
+
+FVF_HD double mul(double a, double b) { return from_bits(mul_full_int(bits(a), bits(b))); }
 
 // Fastest when a and b have the same sign; correct for any operands.
 FVF_HD double add_same_sign(double a, double b) {

@@ -25,15 +25,17 @@
 //
 // FP64 throughput.  The fused 3D update is 13 FP64 operations per element
 // against 48 bytes of HBM traffic, far above GB300's FP64-to-bandwidth
-// ratio, so the FP64 unit bounds it; this kernel issues FP64 operations at
-// the unit's measured rate.  FVF_RK_EMU selects additions that run as exact
-// integer-pipe binary64 additions (fp64_emu.cuh) instead, in parallel with
-// the FP64 unit: bit 1 the y term, 2 the z term, 4 u + dt*rhs, 8 the final
-// sum, 16/32/64 the x/y/z face differences.  Every choice measured slower
-// than none (the added latency of the integer chains in front of the
-// dependent FP64 operations costs more than the FP64 issue slots it frees),
-// so the default is 0.  FVF_RK_CHUNK is the number of variables per load
-// batch (2 measured best of 2, 4 and 8).
+// ratio.  Its six multiplications run on the integer pipes instead, as exact
+// binary64 products by factors prepared once (fp64_emu.cuh), leaving the
+// seven additions on the FP64 unit: FVF_RK_EMU_MUL selects them (1/2/4 the
+// x/y/z inverse spacings, 8 dt, 16 a, 32 b), and all six with one variable
+// per load batch (FVF_RK_CHUNK = 1) measured fastest on GB300, 36% below the
+// all-FP64 kernel.  FVF_RK_EMU selects additions that run as exact
+// integer-pipe additions as well: bit 1 the y term, 2 the z term, 4
+// u + dt*rhs, 8 the final sum, 16/32/64 the x/y/z face differences.  An
+// addition costs about twice the integer instructions of a product, and
+// every choice of them measured slower on the all-FP64 kernel, so the
+// default is 0.
 #include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
 
@@ -43,8 +45,14 @@
 #ifndef FVF_RK_EMU_Q
 #define FVF_RK_EMU_Q 0xFF
 #endif
+#ifndef FVF_RK_EMU_MUL
+#define FVF_RK_EMU_MUL 63
+#endif
+#ifndef FVF_RK_EMU_MUL_Q
+#define FVF_RK_EMU_MUL_Q 0xFF
+#endif
 #ifndef FVF_RK_CHUNK
-#define FVF_RK_CHUNK 2
+#define FVF_RK_CHUNK 1
 #endif
 
 namespace fvf {
@@ -68,6 +76,16 @@ __device__ __forceinline__ double sub_rn(double x, double y, int q) {
     return __dsub_rn(x, y);
 }
 
+// w * x on the FP64 unit, or on the integer pipes with the factor w prepared
+// in m (fp64_emu.cuh) when BIT is set in FVF_RK_EMU_MUL (1/2/4 the x/y/z
+// inverse spacings, 8 dt, 16 a, 32 b) and slot q in FVF_RK_EMU_MUL_Q.
+template <int BIT>
+__device__ __forceinline__ double mul_rn(double w, const emu::MulConst &m, double x, int q) {
+    if ((FVF_RK_EMU_MUL & BIT) && ((FVF_RK_EMU_MUL_Q >> q) & 1))
+        return emu::from_bits(emu::mul_const_bits(emu::bits(x), m));
+    return __dmul_rn(w, x);
+}
+
 template <bool FUSED, bool FY, bool FZ, typename Idx>
 __global__ void __launch_bounds__(kThreads)
 rk_stage_kernel(RkStageArgs A) {
@@ -85,8 +103,12 @@ rk_stage_kernel(RkStageArgs A) {
     (void)call; (void)xall; (void)yall; (void)zall;
     const double wx = FUSED && FVF_IN(j, n1) ? __ldg(A.w[0] + j) : 0.0;
     const double wy = FY && FVF_IN(k, n2) ? __ldg(A.w[1] + k) : 0.0;
+    const emu::MulConst mx = emu::mul_const(wx), my = emu::mul_const(wy);
+    const emu::MulConst mdt = emu::mul_const(A.dt), ma = emu::mul_const(A.a),
+                        mb = emu::mul_const(A.b);
     for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
         const double wz = FZ && FVF_IN(l, n3) ? __ldg(A.w[2] + l) : 0.0;
+        const emu::MulConst mz = emu::mul_const(wz);
         const int64_t c = (int64_t)jk + (int64_t)plane_jk * l;
         const int64_t xlo = (int64_t)j + (int64_t)(n1 + 1) * ((int64_t)k + (int64_t)n2 * l);
         const int64_t ylo = (int64_t)j + (int64_t)n1 * ((int64_t)k + (int64_t)(n2 + 1) * l);
@@ -125,16 +147,18 @@ rk_stage_kernel(RkStageArgs A) {
                 if (i0 + q < A.nv) {
                     double rr;
                     if (FUSED) {
-                        rr = __dmul_rn(wx, sub_rn<16>(xl[q], xh[q], q));
-                        if (FY) rr = add_rn<1>(rr, __dmul_rn(wy, sub_rn<32>(yl[q], yh[q], q)), q);
-                        if (FZ) rr = add_rn<2>(rr, __dmul_rn(wz, sub_rn<64>(zl[q], zh[q], q)), q);
+                        rr = mul_rn<1>(wx, mx, sub_rn<16>(xl[q], xh[q], q), q);
+                        if (FY)
+                            rr = add_rn<1>(rr, mul_rn<2>(wy, my, sub_rn<32>(yl[q], yh[q], q), q), q);
+                        if (FZ)
+                            rr = add_rn<2>(rr, mul_rn<4>(wz, mz, sub_rn<64>(zl[q], zh[q], q), q), q);
                     } else {
                         rr = r[q];
                     }
-                    const double t = add_rn<4>(uv[q], __dmul_rn(A.dt, rr), q);
+                    const double t = add_rn<4>(uv[q], mul_rn<8>(A.dt, mdt, rr, q), q);
                     if (FVF_IN(c + (int64_t)(i0 + q) * cplane, call))
-                        A.out[c + (int64_t)(i0 + q) * cplane] =
-                            add_rn<8>(__dmul_rn(A.a, u0v[q]), __dmul_rn(A.b, t), q);
+                        A.out[c + (int64_t)(i0 + q) * cplane] = add_rn<8>(
+                            mul_rn<16>(A.a, ma, u0v[q], q), mul_rn<32>(A.b, mb, t, q), q);
                 }
             }
         }

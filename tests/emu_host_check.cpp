@@ -1,6 +1,7 @@
-// Host check of the integer-pipe binary64 addition (fp64_emu.cuh): every sum
-// must be bit-identical to the host CPU's IEEE 754 addition (round to nearest
-// even).  Built with -O2 -ffp-contract=off; prints "mismatches N cases M".
+// Host check of the integer-pipe binary64 addition and multiplication
+// (fp64_emu.cuh): every sum and product must be bit-identical to the host
+// CPU's IEEE 754 operation (round to nearest even).  Built with -O2
+// -ffp-contract=off; prints "mismatches N cases M".
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -24,7 +25,37 @@ static double native_add(double a, double b) {
     return r;
 }
 
+static double native_mul(double a, double b) {
+    volatile double x = a, y = b;
+    volatile double r = x * y;
+    return r;
+}
+
 static uint64_t mismatches = 0, cases = 0;
+
+static bool is_nan(uint64_t x) { return ((x >> 52) & 0x7FF) == 0x7FF && (x & kFrac); }
+
+static void report(const char *what, uint64_t A, uint64_t B, uint64_t got, uint64_t want) {
+    if (got == want || (is_nan(got) && is_nan(want))) return;
+    if (mismatches < 10)
+        std::printf("%s mismatch: %016llx, %016llx -> got %016llx want %016llx\n", what,
+                    (unsigned long long)A, (unsigned long long)B, (unsigned long long)got,
+                    (unsigned long long)want);
+    ++mismatches;
+}
+
+// a * b by the complete algorithm, and by the fixed-factor fast path (with
+// its fallback) with either operand as the fixed factor
+static void check_mul(uint64_t A, uint64_t B) {
+    const double a = from_bits(A), b = from_bits(B);
+    const uint64_t want = bits(native_mul(a, b));
+    ++cases;
+    report("mul full", A, B, mul_full_int(A, B), want);
+    report("mul const", A, B, mul_const_bits(A, mul_const(b)), want);
+    report("mul const swapped", B, A, mul_const_bits(B, mul_const(a)), want);
+    uint64_t fast;
+    if (mul_const_fast_int(A, mul_const(b), &fast)) report("mul fast", A, B, fast, want);
+}
 
 static void check(uint64_t A, uint64_t B) {
     const double a = from_bits(A), b = from_bits(B);
@@ -126,6 +157,35 @@ int main(int argc, char **argv) {
         for (int j = 0; j < ns; ++j) check(specials[i], specials[j]);
     for (long i = 0; i < n / 10; ++i)
         for (int j = 0; j < ns; ++j) check(specials[j], next_u64());
+    // products: random patterns, exponents that put the product anywhere from
+    // deep underflow to overflow, ties (significands with few bits), subnormal
+    // operands, the diffusion's own factors (0 < alpha <= 1/4, t of any size)
+    for (long i = 0; i < n; ++i) check_mul(next_u64(), next_u64());
+    for (long i = 0; i < 2 * n; ++i) {
+        const uint64_t ea = next_u64() % 2048;
+        const int64_t target = (int64_t)(next_u64() % 2300) - 130;   // biased result exponent
+        int64_t eb = target + 1023 - (int64_t)ea;
+        if (eb < 0) eb = next_u64() % 3;
+        if (eb > 2047) eb = 2047 - next_u64() % 3;
+        check_mul(make(next_u64() & 1, ea, next_u64()), make(next_u64() & 1, (uint64_t)eb, next_u64()));
+    }
+    for (long i = 0; i < n; ++i) {
+        // significands with at most 26 + 27 significant bits: exact products and halfway cases
+        const uint64_t fa = next_u64() & (kFrac & ~((1ull << (next_u64() % 53)) - 1));
+        const uint64_t fb = next_u64() & (kFrac & ~((1ull << (next_u64() % 53)) - 1));
+        check_mul(make(next_u64() & 1, 1 + next_u64() % 2046, fa), make(next_u64() & 1, 1 + next_u64() % 2046, fb));
+        check_mul(make(next_u64() & 1, 0, next_u64()), make(next_u64() & 1, next_u64() % 2048, next_u64()));
+    }
+    for (long i = 0; i < n; ++i) {
+        const double alpha = 0.25 * (double)(next_u64() >> 11) * 0x1p-53;
+        check_mul(next_u64(), bits(alpha));
+        check_mul(make(next_u64() & 1, 900 + next_u64() % 250, next_u64()), bits(alpha));
+        check_mul(bits(0.1), make(next_u64() & 1, next_u64() % 2048, next_u64()));
+    }
+    for (int i = 0; i < ns; ++i)
+        for (int j = 0; j < ns; ++j) check_mul(specials[i], specials[j]);
+    for (long i = 0; i < n / 10; ++i)
+        for (int j = 0; j < ns; ++j) check_mul(specials[j], next_u64());
     std::printf("mismatches %llu cases %llu\n", (unsigned long long)mismatches,
                 (unsigned long long)cases);
     return mismatches != 0;

@@ -86,8 +86,8 @@ def test_ragged_random_fields(dt, nx, ny):
 @pytest.mark.parametrize("dt", [np.float64, np.float32])
 def test_special_values(dt):
     """Huge values (4c overflows: the kernel's two-operation branch), inf,
-    NaN, signed zeros and subnormals, with alpha 0.1 and 0.3; bit-exact up to
-    NaN payloads."""
+    NaN, signed zeros and subnormals, with alpha 0.1, 0.3, 0 and the smallest
+    subnormal; bit-exact up to NaN payloads."""
     torch = torch_cuda()
     nx, ny = 37, 23
     rng_bits = inputs.random_bits(3, 1, nx * ny)
@@ -102,7 +102,8 @@ def test_special_values(dt):
     flat = u0.reshape(-1)
     for s, b in zip(specials, rng_bits[: len(specials)]):
         flat[int(b % (nx * ny))] = dt(s)
-    for alpha in (0.1, 0.3):
+    tiny = 1e-45 if dt == np.float32 else 5e-324
+    for alpha in (0.1, 0.3, 0.0, tiny):
         for steps in (1, 3):
             gu, gv = _run_gpu(torch, u0, steps, alpha=alpha)
             ou, ov, _ = oracle.diffuse2d(u0, steps, alpha=alpha, return_both=True)

@@ -74,10 +74,14 @@ def test_impulse_and_special_values(dt):
     specials = np.array([np.inf, -np.inf, np.nan, -0.0, 1e-40 if dt == np.float32 else 1e-310,
                          3e38 if dt == np.float32 else 1.7e308], dtype=dt)
     flat[::17] = np.resize(specials, flat[::17].size)
-    gu, gv = _run(torch, u0, 3)
-    ou, ov, _ = oracle.diffuse3d(u0, 3, 0.1, return_both=True)
-    assert_bits_equal(gu, ou, nan_payloads=False)
-    assert_bits_equal(gv, ov, nan_payloads=False)
+    # alpha 0 and a subnormal alpha: every product takes the complete
+    # (slow-path) multiplication; 1/6 and 0.1 the fixed-factor fast path
+    tiny = 1e-40 if dt == np.float32 else 5e-324
+    for alpha in (0.1, 1.0 / 6.0, 0.0, tiny):
+        gu, gv = _run(torch, u0, 3, alpha=alpha)
+        ou, ov, _ = oracle.diffuse3d(u0, 3, alpha, return_both=True)
+        assert_bits_equal(gu, ou, nan_payloads=False, what=f"u alpha={alpha}")
+        assert_bits_equal(gv, ov, nan_payloads=False, what=f"v alpha={alpha}")
 
 
 def test_misaligned_rows_take_the_scalar_path():

@@ -101,22 +101,35 @@ def test_rhs_small(extents, direction, nv):
 
 
 def test_rhs_special_values_and_alias():
-    """inf/NaN/huge fluxes (subtraction overflow), subnormal spacing; and an
-    rhs overlapping the flux is refused."""
+    """inf/NaN/huge/subnormal fluxes (subtraction overflow, products below
+    the normal range), zero, subnormal, huge and infinite spacings, in every
+    direction and every variable slot of a load batch (the products of some
+    slots run on the integer pipes); and an rhs overlapping the flux is
+    refused."""
     torch = torch_cuda()
-    extents, nv = (17, 9, 5), 3
+    extents = (17, 9, 5)
+    for nv in (3, 5):
+        for direction in range(3):
+            flux = inputs.face_fluxes(9, nv, extents, direction)
+            flux[::5] = 1.7e308
+            flux[1::7] = -1.7e308
+            flux[2::11] = np.inf
+            flux[3::13] = np.nan
+            flux[4::17] = -0.0
+            flux[5::19] = 5e-324
+            flux[6::23] = -2.2e-308
+            inv_d = inputs.inverse_spacing(9, extents[direction])
+            inv_d[0] = 5e-324
+            inv_d[1] = 1e300
+            inv_d[2] = 0.0
+            inv_d[3] = np.inf
+            inv_d[4] = 1e-310
+            got = _gpu_rhs(torch, flux, inv_d, nv, extents, direction)
+            want = oracle.advect_rhs(flux, inv_d, nv, extents, direction)
+            assert_bits_equal(got, want, nan_payloads=False, what=f"dir {direction} nv {nv}")
+    nv = 3
     flux = inputs.face_fluxes(9, nv, extents, 0)
-    flux[::5] = 1.7e308
-    flux[1::7] = -1.7e308
-    flux[2::11] = np.inf
-    flux[3::13] = np.nan
-    flux[4::17] = -0.0
     inv_d = inputs.inverse_spacing(9, 17)
-    inv_d[3] = 5e-324
-    inv_d[4] = 1e300
-    got = _gpu_rhs(torch, flux, inv_d, nv, extents, 0)
-    want = oracle.advect_rhs(flux, inv_d, nv, extents, 0)
-    assert_bits_equal(got, want, nan_payloads=False)
     F = to_dev(flux)
     with pytest.raises(api.FvfError) as e:
         api.advect_rhs(F, to_dev(inv_d), nv, extents, 0, F[: 17 * 9 * 5 * nv])

@@ -70,7 +70,9 @@ def test_stage_small(extents, present, nv):
 
 def test_special_values():
     """Infinities, NaNs, signed zeros, subnormals and overflow in every
-    input; a = 0 still multiplies u0 (0*inf = NaN)."""
+    input, the inverse spacings included; zero and subnormal coefficients (the
+    integer-pipe products then take their complete path); a = 0 still
+    multiplies u0 (0*inf = NaN)."""
     torch = torch_cuda()
     extents, nv = (37, 6, 5), 2
     fl, w, u0, u = _case(inputs.config_seed(8), extents, nv)
@@ -80,10 +82,13 @@ def test_special_values():
         arr[::step] = np.resize(specials, arr[::step].size)
     rhs = inputs.normal_f64(9, 0, u.size)
     rhs[::5] = np.resize(specials, rhs[::5].size)
-    for a, b in COEFS + [(0.0, 0.0)]:
-        got = _gpu_stage(torch, u0, u, fl, w, nv, extents, a, b, 1e300)
-        assert_bits_equal(got, oracle.ssprk3_stage(u0, u, fl, w, nv, extents, a, b, 1e300),
-                          nan_payloads=False, what=f"special stage a={a}")
+    for d, x in enumerate(w):
+        x[d::4] = np.resize(np.array([0.0, 5e-324, 1e300, np.inf]), x[d::4].size)
+    for a, b in COEFS + [(0.0, 0.0), (5e-324, -1e-310)]:
+        for dt in (1e300, 0.21, 0.0, 5e-324):
+            got = _gpu_stage(torch, u0, u, fl, w, nv, extents, a, b, dt)
+            assert_bits_equal(got, oracle.ssprk3_stage(u0, u, fl, w, nv, extents, a, b, dt),
+                              nan_payloads=False, what=f"special stage a={a} dt={dt}")
         out = torch.empty(u.size, dtype=torch.float64, device="cuda")
         api.ssprk3_axpby(to_dev(u0), to_dev(u), to_dev(rhs), nv, extents, a, b, 0.5, out)
         torch.cuda.synchronize()
