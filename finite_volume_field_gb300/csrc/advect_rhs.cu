@@ -31,6 +31,16 @@
 #ifndef FVF_RHS_EMU_MUL
 #define FVF_RHS_EMU_MUL 7
 #endif
+#ifndef FVF_RHS_F32_GROUP
+#define FVF_RHS_F32_GROUP 8
+#endif
+// FP32 form: at least this many blocks per SM (a register cap that keeps
+// more loads in flight for 4-byte elements; measured 20% faster on GB300).
+// The FP64 form takes no minimum (0): a minimum of 1 already changed the
+// compiler's register allocation and measured slower.
+#ifndef FVF_RHS_F32_MINB
+#define FVF_RHS_F32_MINB 4
+#endif
 
 namespace fvf {
 namespace {
@@ -38,7 +48,7 @@ namespace {
 constexpr int kThreads = 256;
 // variables per load batch: 4 FP64 or 8 FP32, 64 bytes of face loads each
 template <typename T>
-__host__ __device__ constexpr int group_of() { return 32 / (int)sizeof(T); }
+__host__ __device__ constexpr int group_of() { return sizeof(T) == 4 ? FVF_RHS_F32_GROUP : 4; }
 
 // Face difference F(c-1) - F(c) of variable slot q of a batch: on the FP64
 // unit, or as an exact integer-pipe addition of -F(c) when bit q of
@@ -85,30 +95,33 @@ __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, 
 // of a plane l, the (j, k) pairs flattened over the block so that every lane
 // has a cell whatever n1 is: the kernel is bound by the FP64 unit, which
 // charges idle lanes.
-template <int DIR, bool ACC, typename Idx, typename T>
-__global__ void __launch_bounds__(kThreads)
+template <int DIR, bool ACC, typename Idx, typename Off, typename T>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 4 ? FVF_RHS_F32_MINB : 0)
 advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int nv,
-                  int64_t n1_, int64_t n2_, int64_t n3, T *__restrict__ rhs) {
+                  int64_t n1_, int64_t n2_, int64_t n3_, T *__restrict__ rhs) {
     const Idx n1 = (Idx)n1_, n2 = (Idx)n2_;
     const Idx plane = n1 * n2;
     const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
     if (jk >= plane) return;
     const Idx k = jk / n1, j = jk - k * n1;
-    const int64_t F1 = DIR == 0 ? (int64_t)n1 + 1 : (int64_t)n1;
-    const int64_t F2 = DIR == 1 ? (int64_t)n2 + 1 : (int64_t)n2;
-    const int64_t F3 = DIR == 2 ? n3 + 1 : n3;
-    const int64_t fplane = F1 * F2 * F3;
-    const int64_t rplane = (int64_t)plane * n3;
-    const int64_t step = DIR == 0 ? 1 : (DIR == 1 ? F1 : F1 * F2);
-    const int64_t nw = DIR == 0 ? (int64_t)n1 : (DIR == 1 ? (int64_t)n2 : n3);  // inv_d extent
-    const int64_t fall = fplane * nv, rall = rplane * nv;  // flux and rhs extents
+    // flat offsets in Off: 32-bit when every element index of both arrays
+    // fits (the launcher checks), else 64-bit
+    const Off n3 = (Off)n3_;
+    const Off F1 = DIR == 0 ? (Off)n1 + 1 : (Off)n1;
+    const Off F2 = DIR == 1 ? (Off)n2 + 1 : (Off)n2;
+    const Off F3 = DIR == 2 ? n3 + 1 : n3;
+    const Off fplane = F1 * F2 * F3;
+    const Off rplane = (Off)plane * n3;
+    const Off step = DIR == 0 ? 1 : (DIR == 1 ? F1 : F1 * F2);
+    const Off nw = DIR == 0 ? (Off)n1 : (DIR == 1 ? (Off)n2 : n3);  // inv_d extent
+    const Off fall = fplane * nv, rall = rplane * nv;  // flux and rhs extents
     (void)nw; (void)fall; (void)rall;
     const T wjk = DIR == 0 ? (FVF_IN(j, nw) ? __ldg(inv_d + j) : T(0))
                            : (DIR == 1 ? (FVF_IN(k, nw) ? __ldg(inv_d + k) : T(0)) : T(0));
-    for (int64_t l = blockIdx.y; l < n3; l += gridDim.y) {
+    for (Off l = blockIdx.y; l < n3; l += gridDim.y) {
         const Scale<T> w(DIR == 2 ? (FVF_IN(l, nw) ? __ldg(inv_d + l) : T(0)) : wjk);
-        const int64_t lo = (int64_t)j + F1 * ((int64_t)k + F2 * l);  // face c-1 at position c
-        const int64_t ro = (int64_t)jk + (int64_t)plane * l;
+        const Off lo = (Off)j + F1 * ((Off)k + F2 * l);  // face c-1 at position c
+        const Off ro = (Off)jk + (Off)plane * l;
         const T *f = flux + lo;
         T *r = rhs + ro;
         constexpr int kGroup = group_of<T>();
@@ -117,20 +130,20 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
 #pragma unroll
             for (int q = 0; q < kGroup; ++q) {
                 if (i0 + q < nv) {
-                    const int64_t fo = (int64_t)(i0 + q) * fplane;
+                    const Off fo = (Off)(i0 + q) * fplane;
                     a[q] = FVF_IN(lo + fo, fall) ? __ldg(f + fo) : T(0);
                     b[q] = FVF_IN(lo + fo + step, fall) ? __ldg(f + fo + step) : T(0);
                     if (ACC)
-                        old[q] = FVF_IN(ro + (int64_t)(i0 + q) * rplane, rall)
-                                     ? r[(int64_t)(i0 + q) * rplane] : T(0);
+                        old[q] = FVF_IN(ro + (Off)(i0 + q) * rplane, rall)
+                                     ? r[(Off)(i0 + q) * rplane] : T(0);
                 }
             }
 #define FVF_RHS_Q(Q)                                                                    \
     if (Q < kGroup && i0 + Q < nv) {                                                    \
         const T term = w.template apply<Q>(face_diff<Q>(a[Q], b[Q]));                  \
         /* accumulate form: the term added once to the existing rhs */                 \
-        if (FVF_IN(ro + (int64_t)(i0 + Q) * rplane, rall))                              \
-            r[(int64_t)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;         \
+        if (FVF_IN(ro + (Off)(i0 + Q) * rplane, rall))                                  \
+            r[(Off)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;             \
     }
             FVF_RHS_Q(0)
             FVF_RHS_Q(1)
@@ -140,9 +153,26 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
             FVF_RHS_Q(5)
             FVF_RHS_Q(6)
             FVF_RHS_Q(7)
+            FVF_RHS_Q(8)
+            FVF_RHS_Q(9)
+            FVF_RHS_Q(10)
+            FVF_RHS_Q(11)
+            FVF_RHS_Q(12)
+            FVF_RHS_Q(13)
+            FVF_RHS_Q(14)
+            FVF_RHS_Q(15)
 #undef FVF_RHS_Q
         }
     }
+}
+
+// Which forms take 32-bit flat offsets, as measured on GB300 at 8 x 201^3:
+// the FP32 form (3-20% faster), the FP64 z forms and the assigning FP64 y
+// form (2-3% faster); the other FP64 forms measured 1-16% slower, the
+// compiler's register allocation of the emulated products differing.
+template <int DIR, bool ACC, typename T>
+constexpr bool off32() {
+    return sizeof(T) == 4 || DIR == 2 || (DIR == 1 && !ACC);
 }
 
 template <int DIR, bool ACC, typename T>
@@ -151,12 +181,20 @@ void launch_typed(const T *flux, const T *inv_d, int nv, const int64_t n[3], T *
     const int64_t plane = n[0] * n[1];
     const dim3 grid((unsigned)((plane + kThreads - 1) / kThreads),
                     (unsigned)(n[2] < 65535 ? n[2] : 65535));
-    // 32-bit (j, k) arithmetic while the plane index fits
-    if (plane + kThreads < ((int64_t)1 << 31))
-        advect_rhs_kernel<DIR, ACC, uint32_t, T><<<grid, kThreads, 0, stream>>>(
+    // 32-bit (j, k) arithmetic while the plane index fits, and, for the
+    // forms where off32<>() says so, 32-bit flat offsets too while every flux
+    // and rhs element index fits (the flux array, one face layer larger
+    // along the swept axis, is the larger)
+    const int64_t lim = (int64_t)1 << 31;
+    const int64_t fall = (n[0] + 1) * (n[1] + 1) * (n[2] + 1) * nv;
+    if (off32<DIR, ACC, T>() && fall + plane + kThreads < lim)
+        advect_rhs_kernel<DIR, ACC, uint32_t, uint32_t, T><<<grid, kThreads, 0, stream>>>(
+            flux, inv_d, nv, n[0], n[1], n[2], rhs);
+    else if (plane + kThreads < lim)
+        advect_rhs_kernel<DIR, ACC, uint32_t, int64_t, T><<<grid, kThreads, 0, stream>>>(
             flux, inv_d, nv, n[0], n[1], n[2], rhs);
     else
-        advect_rhs_kernel<DIR, ACC, int64_t, T><<<grid, kThreads, 0, stream>>>(
+        advect_rhs_kernel<DIR, ACC, int64_t, int64_t, T><<<grid, kThreads, 0, stream>>>(
             flux, inv_d, nv, n[0], n[1], n[2], rhs);
 }
 

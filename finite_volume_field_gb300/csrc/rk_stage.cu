@@ -30,12 +30,12 @@
 // seven additions on the FP64 unit: FVF_RK_EMU_MUL selects them (1/2/4 the
 // x/y/z inverse spacings, 8 dt, 16 a, 32 b), and all six with one variable
 // per load batch (FVF_RK_CHUNK = 1) measured fastest on GB300, 36% below the
-// all-FP64 kernel.  FVF_RK_EMU selects additions that run as exact
-// integer-pipe additions as well: bit 1 the y term, 2 the z term, 4
-// u + dt*rhs, 8 the final sum, 16/32/64 the x/y/z face differences.  An
-// addition costs about twice the integer instructions of a product, and
-// every choice of them measured slower on the all-FP64 kernel, so the
-// default is 0.
+// all-FP64 kernel (the update alone, FVF_RK_CHUNK_AXPBY = 1, measured
+// fastest with one variable per batch as well).  FVF_RK_EMU selects
+// additions that run as exact integer-pipe additions as well: bit 1 the y
+// term, 2 the z term, 4 u + dt*rhs, 8 the final sum, 16/32/64 the x/y/z face
+// differences.  An addition costs about twice the integer instructions of a
+// product, and every choice of them measured slower, so the default is 0.
 #include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
 
@@ -54,11 +54,13 @@
 #ifndef FVF_RK_CHUNK
 #define FVF_RK_CHUNK 1
 #endif
+#ifndef FVF_RK_CHUNK_AXPBY
+#define FVF_RK_CHUNK_AXPBY 1
+#endif
 
 namespace fvf {
 namespace {
 
-constexpr int kChunk = FVF_RK_CHUNK;
 constexpr int kThreads = 256;
 
 // q is the variable's slot in its load batch (a constant once the batch loop
@@ -89,6 +91,7 @@ __device__ __forceinline__ double mul_rn(double w, const emu::MulConst &m, doubl
 template <bool FUSED, bool FY, bool FZ, typename Idx>
 __global__ void __launch_bounds__(kThreads)
 rk_stage_kernel(RkStageArgs A) {
+    constexpr int kChunk = FUSED ? FVF_RK_CHUNK : FVF_RK_CHUNK_AXPBY;
     const Idx n1 = (Idx)A.n[0], n2 = (Idx)A.n[1];
     const Idx plane_jk = n1 * n2;
     const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
