@@ -63,27 +63,28 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// q is the variable's slot in its load batch (a constant once the batch loop
-// is unrolled): FVF_RK_EMU_Q selects the slots whose additions are emulated.
+// v is the variable's index: FVF_RK_EMU_Q selects, by v mod 8, the variables
+// whose additions are emulated (a warp-uniform choice: every lane of a warp
+// works on the same variable).
 template <int BIT>
-__device__ __forceinline__ double add_rn(double x, double y, int q) {
-    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> q) & 1)) return emu::add(x, y);
+__device__ __forceinline__ double add_rn(double x, double y, int v) {
+    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> (v & 7)) & 1)) return emu::add(x, y);
     return __dadd_rn(x, y);
 }
 
 template <int BIT>
-__device__ __forceinline__ double sub_rn(double x, double y, int q) {
-    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> q) & 1))
+__device__ __forceinline__ double sub_rn(double x, double y, int v) {
+    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> (v & 7)) & 1))
         return emu::add(x, emu::from_bits(emu::bits(y) ^ emu::kSign));
     return __dsub_rn(x, y);
 }
 
 // w * x on the FP64 unit, or on the integer pipes with the factor w prepared
 // in m (fp64_emu.cuh) when BIT is set in FVF_RK_EMU_MUL (1/2/4 the x/y/z
-// inverse spacings, 8 dt, 16 a, 32 b) and slot q in FVF_RK_EMU_MUL_Q.
+// inverse spacings, 8 dt, 16 a, 32 b) and bit v mod 8 in FVF_RK_EMU_MUL_Q.
 template <int BIT>
-__device__ __forceinline__ double mul_rn(double w, const emu::MulConst &m, double x, int q) {
-    if ((FVF_RK_EMU_MUL & BIT) && ((FVF_RK_EMU_MUL_Q >> q) & 1))
+__device__ __forceinline__ double mul_rn(double w, const emu::MulConst &m, double x, int v) {
+    if ((FVF_RK_EMU_MUL & BIT) && ((FVF_RK_EMU_MUL_Q >> (v & 7)) & 1))
         return emu::from_bits(emu::mul_const_bits(emu::bits(x), m));
     return __dmul_rn(w, x);
 }
@@ -148,20 +149,21 @@ rk_stage_kernel(RkStageArgs A) {
 #pragma unroll
             for (int q = 0; q < kChunk; ++q) {
                 if (i0 + q < A.nv) {
+                    const int v = i0 + q;
                     double rr;
                     if (FUSED) {
-                        rr = mul_rn<1>(wx, mx, sub_rn<16>(xl[q], xh[q], q), q);
+                        rr = mul_rn<1>(wx, mx, sub_rn<16>(xl[q], xh[q], v), v);
                         if (FY)
-                            rr = add_rn<1>(rr, mul_rn<2>(wy, my, sub_rn<32>(yl[q], yh[q], q), q), q);
+                            rr = add_rn<1>(rr, mul_rn<2>(wy, my, sub_rn<32>(yl[q], yh[q], v), v), v);
                         if (FZ)
-                            rr = add_rn<2>(rr, mul_rn<4>(wz, mz, sub_rn<64>(zl[q], zh[q], q), q), q);
+                            rr = add_rn<2>(rr, mul_rn<4>(wz, mz, sub_rn<64>(zl[q], zh[q], v), v), v);
                     } else {
                         rr = r[q];
                     }
-                    const double t = add_rn<4>(uv[q], mul_rn<8>(A.dt, mdt, rr, q), q);
-                    if (FVF_IN(c + (int64_t)(i0 + q) * cplane, call))
-                        A.out[c + (int64_t)(i0 + q) * cplane] = add_rn<8>(
-                            mul_rn<16>(A.a, ma, u0v[q], q), mul_rn<32>(A.b, mb, t, q), q);
+                    const double t = add_rn<4>(uv[q], mul_rn<8>(A.dt, mdt, rr, v), v);
+                    if (FVF_IN(c + (int64_t)v * cplane, call))
+                        A.out[c + (int64_t)v * cplane] = add_rn<8>(
+                            mul_rn<16>(A.a, ma, u0v[q], v), mul_rn<32>(A.b, mb, t, v), v);
                 }
             }
         }
