@@ -41,6 +41,15 @@
 
 #include <stdint.h>
 
+// 1: bits() assembles the pattern from the value's two 32-bit words instead
+// of one 64-bit reinterpretation.  The results are the same; the generated
+// code differs (the compiler can no longer see a test on the exponent field
+// as a test on the double), and which form is faster depends on the kernel,
+// so a translation unit chooses before including this header.
+#ifndef FVF_EMU_BITS_HILO
+#define FVF_EMU_BITS_HILO 0
+#endif
+
 #if defined(__CUDACC__)
 #define FVF_HD __host__ __device__ __forceinline__
 #else
@@ -55,7 +64,9 @@ constexpr uint64_t kFrac = 0x000FFFFFFFFFFFFFull;
 constexpr uint64_t kHidden = 0x0010000000000000ull;
 
 FVF_HD uint64_t bits(double x) {
-#if defined(__CUDA_ARCH__)
+#if defined(__CUDA_ARCH__) && FVF_EMU_BITS_HILO
+    return ((uint64_t)(uint32_t)__double2hiint(x) << 32) | (uint32_t)__double2loint(x);
+#elif defined(__CUDA_ARCH__)
     return (uint64_t)__double_as_longlong(x);
 #else
     uint64_t u;
@@ -299,12 +310,22 @@ struct MulConst {
     uint32_t fast;
 };
 
+// The factor's fields are taken from its two 32-bit words: built from the
+// 64-bit pattern, the range test below was measured to cost one FP64-pipe
+// instruction per call on GB300 (the compiler may turn a test on a double's
+// exponent field into a floating-point comparison).
 FVF_HD MulConst mul_const(double alpha) {
+#if defined(__CUDA_ARCH__)
+    const uint32_t hi = (uint32_t)__double2hiint(alpha), lo = (uint32_t)__double2loint(alpha);
+#else
+    const uint64_t b = bits(alpha);
+    const uint32_t hi = (uint32_t)(b >> 32), lo = (uint32_t)b;
+#endif
     MulConst m;
-    m.bits = bits(alpha);
-    const uint32_t e = (uint32_t)(m.bits >> 52) & 0x7FFu;
-    m.k = ((m.bits & kFrac) | kHidden) << 11;
-    m.sign = m.bits & kSign;
+    const uint32_t e = (hi >> 20) & 0x7FFu;
+    m.bits = ((uint64_t)hi << 32) | lo;
+    m.k = ((uint64_t)((hi & 0xFFFFFu) | 0x100000u) << 43) | ((uint64_t)lo << 11);
+    m.sign = (uint64_t)(hi & 0x80000000u) << 32;
     m.adj = (int32_t)e - 1023;
     m.fast = (e - 1u) < 2046u;
     return m;
