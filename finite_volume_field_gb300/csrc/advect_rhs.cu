@@ -13,7 +13,8 @@
 // prepared once per cell) for three of every four variables
 // (FVF_RHS_EMU_MUL = 7, one bit per slot of a load batch); on GB300 this
 // measured 20-26% faster than all-FP64 and than emulating all four (the
-// integer pipes saturate then).  Moving the subtraction instead measured
+// integer pipes saturate then).  The accumulating form takes all four
+// (FVF_RHS_EMU_MUL_ACC).  Moving the subtraction instead measured
 // slower: the exact addition costs about twice the integer instructions of
 // the product.
 //
@@ -30,6 +31,11 @@
 #endif
 #ifndef FVF_RHS_EMU_MUL
 #define FVF_RHS_EMU_MUL 7
+#endif
+// the same for the accumulating form, whose extra read and add change the
+// balance: all four slots measured 2-7% faster there
+#ifndef FVF_RHS_EMU_MUL_ACC
+#define FVF_RHS_EMU_MUL_ACC 15
 #endif
 #ifndef FVF_RHS_F32_GROUP
 #define FVF_RHS_F32_GROUP 8
@@ -64,7 +70,7 @@ template <int Q>
 __device__ __forceinline__ float face_diff(float lo, float hi) { return __fsub_rn(lo, hi); }
 // inv_d(c) times a face difference: on the FP64 unit, or on the integer
 // pipes (fp64_emu.cuh, the factor prepared once per cell) for the variable
-// slots whose bit is set in FVF_RHS_EMU_MUL.
+// slots whose bit is set in MASK.
 template <typename T>
 struct Scale;
 
@@ -73,9 +79,9 @@ struct Scale<double> {
     double w;
     emu::MulConst m;
     __device__ explicit Scale(double w_) : w(w_), m(emu::mul_const(w_)) {}
-    template <int Q>
+    template <int MASK, int Q>
     __device__ __forceinline__ double apply(double d) const {
-        if ((FVF_RHS_EMU_MUL >> Q) & 1) return emu::from_bits(emu::mul_const_bits(emu::bits(d), m));
+        if ((MASK >> Q) & 1) return emu::from_bits(emu::mul_const_bits(emu::bits(d), m));
         return __dmul_rn(w, d);
     }
 };
@@ -84,7 +90,7 @@ template <>
 struct Scale<float> {
     float w;
     __device__ explicit Scale(float w_) : w(w_) {}
-    template <int Q>
+    template <int MASK, int Q>
     __device__ __forceinline__ float apply(float d) const { return __fmul_rn(w, d); }
 };
 __device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
@@ -125,6 +131,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
         const T *f = flux + lo;
         T *r = rhs + ro;
         constexpr int kGroup = group_of<T>();
+        constexpr int kMulMask = ACC ? FVF_RHS_EMU_MUL_ACC : FVF_RHS_EMU_MUL;
         for (int i0 = 0; i0 < nv; i0 += kGroup) {
             T a[kGroup], b[kGroup], old[kGroup];
 #pragma unroll
@@ -140,7 +147,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
             }
 #define FVF_RHS_Q(Q)                                                                    \
     if (Q < kGroup && i0 + Q < nv) {                                                    \
-        const T term = w.template apply<Q>(face_diff<Q>(a[Q], b[Q]));                  \
+        const T term = w.template apply<kMulMask, Q>(face_diff<Q>(a[Q], b[Q]));        \
         /* accumulate form: the term added once to the existing rhs */                 \
         if (FVF_IN(ro + (Off)(i0 + Q) * rplane, rall))                                  \
             r[(Off)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;             \
