@@ -26,9 +26,12 @@
 //          blocks as fit on the SMs at once, each taking an equal band of
 //          rows.
 //   scalar (any size or alignment): one thread per cell.
-//   cluster (small grids, nsteps >= 2): all steps in one launch, the grid in
-//          the shared memory of an 8-block thread-block cluster.  The
-//          cluster, blocked and march kernels are described below.
+//   blocked (FP32, nsteps >= 3): up to 8 steps per launch in shared memory.
+//   cluster (grids of up to 32K cells, nsteps >= 2): all steps in one
+//          launch, the grid in the shared memory of a 16-block (8 where the
+//          device or the grid does not allow 16) thread-block cluster.
+// FP64 takes the cluster kernel or one march (or scalar) launch per step.
+// The cluster, blocked and march kernels are described below.
 #include <cooperative_groups.h>
 
 // The FP64 update reads bit patterns word by word (fp64_emu.cuh): 6% faster
@@ -454,7 +457,7 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
 //
 // For grids of up to a few tens of thousands of cells the time goes to
 // launch latency and, for FP64, to arithmetic that one SM would do alone.  A
-// cluster of kClusterSize blocks (one per SM) splits the rows into bands:
+// cluster of 8 or 16 blocks (one per SM) splits the rows into bands:
 // each block keeps both ping-pong states of its band in its own shared
 // memory, reads the row just above and just below its band from the
 // neighbouring blocks' shared memory (distributed shared memory), and the
@@ -463,12 +466,24 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
 // as in the other kernels, so the same bits.  At the end every block writes
 // its band of the last state to the result array and of the state before it
 // to the other array.
-constexpr int kClusterSize = 8;
+#ifndef FVF_CLUSTER_MAX
+#define FVF_CLUSTER_MAX 16
+#endif
 constexpr int kClusterThreads = 512;
 constexpr int64_t kClusterMaxBytes = 200 * 1024;   // per block: both states of a band
+// Largest grid the cluster kernel takes.  Measured on GB300 (16-block
+// cluster against the per-step march kernel for FP64 and the blocked kernel
+// for FP32): 128^2 x 100 steps 237 vs 425 us (FP64) and 89 vs 151 us (FP32);
+// 200^2 x 50 steps 243 vs 220 us and 85 vs 87 us; larger grids favour the
+// others.
+constexpr int64_t kClusterMaxCells = 32 * 1024;
 
-template <typename T>
-__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kClusterThreads)
+// CS blocks per cluster, launched with the cluster dimension as a launch
+// attribute.  A thread's cells (c = tid, tid + blockDim.x, ...) are the same
+// at every step; their (row, column) are stepped by a fixed increment rather
+// than divided out per cell and step.
+template <typename T, int CS>
+__global__ void __launch_bounds__(kClusterThreads)
 diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restrict__ v, int nx,
                        int ny, int band, int64_t nsteps, T alpha) {
     extern __shared__ unsigned char smem_raw[];
@@ -479,7 +494,10 @@ diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restric
     const int r0 = rank * band;
     const int rows = max(0, min(band, ny - r0));
     const int cells = rows * nx;
-    for (int c = threadIdx.x; c < cells; c += kClusterThreads)
+    const int nt = (int)blockDim.x;
+    const int step_r = nt / nx, step_i = nt - step_r * nx;
+    const int lr0 = (int)threadIdx.x / nx, i0 = (int)threadIdx.x - lr0 * nx;
+    for (int c = threadIdx.x; c < cells; c += nt)
         if (FVF_IN((int64_t)r0 * nx + c, (int64_t)nx * ny)) st0[c] = u0[(int64_t)r0 * nx + c];
     cluster.sync();
     for (int64_t s = 1; s <= nsteps; ++s) {
@@ -487,9 +505,9 @@ diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restric
         T *out = (s & 1) ? st1 : st0;
         // the neighbours' copies of the same state (rows r0-1 and r0+rows)
         const T *above = rank > 0 ? cluster.map_shared_rank(in, rank - 1) : nullptr;
-        const T *below = rank + 1 < kClusterSize ? cluster.map_shared_rank(in, rank + 1) : nullptr;
-        for (int c = threadIdx.x; c < cells; c += kClusterThreads) {
-            const int lr = c / nx, i = c - lr * nx;
+        const T *below = rank + 1 < CS ? cluster.map_shared_rank(in, rank + 1) : nullptr;
+        int lr = lr0, i = i0;
+        for (int c = threadIdx.x; c < cells; c += nt) {
             const int j = r0 + lr;
             if (i == 0 || i == nx - 1 || j == 0 || j == ny - 1) {
                 out[c] = T(0);
@@ -498,58 +516,115 @@ diffuse_cluster_kernel(const T *__restrict__ u0, T *__restrict__ u, T *__restric
                 const T nv = lr + 1 < rows ? in[c + nx] : below[i];
                 out[c] = update<T>(in[c], in[c - 1], in[c + 1], sv, nv, alpha);
             }
+            lr += step_r;
+            i += step_i;
+            if (i >= nx) {
+                i -= nx;
+                ++lr;
+            }
         }
         cluster.sync();
     }
     // state n is in st[n & 1]; it belongs in v for odd n and in u for even n
     const T *last = (nsteps & 1) ? st1 : st0, *prev = (nsteps & 1) ? st0 : st1;
     T *res = (nsteps & 1) ? v : u, *oth = (nsteps & 1) ? u : v;
-    for (int c = threadIdx.x; c < cells; c += kClusterThreads) {
+    for (int c = threadIdx.x; c < cells; c += nt) {
         if (!FVF_IN((int64_t)r0 * nx + c, (int64_t)nx * ny)) continue;
         res[(int64_t)r0 * nx + c] = last[c];
         oth[(int64_t)r0 * nx + c] = prev[c];
     }
 }
 
-// Band height and whether the cluster kernel applies (nsteps >= 2: step n-1
-// must exist for the other buffer).
+// Band height for a cluster of cs blocks, 0 when the cluster kernel does not
+// apply (nsteps >= 2: step n-1 must exist for the other buffer).
 template <typename T>
-int cluster_band(int64_t nx, int64_t ny, int64_t nsteps) {
-    if (nsteps < 2 || nx > 65536 || ny > 65536) return 0;
-    const int64_t band = (ny + kClusterSize - 1) / kClusterSize;
+int cluster_band(int64_t nx, int64_t ny, int64_t nsteps, int cs) {
+    if (nsteps < 2 || nx > 65536 || ny > 65536 || nx * ny > kClusterMaxCells) return 0;
+    const int64_t band = (ny + cs - 1) / cs;
     if (band * nx * 2 * (int64_t)sizeof(T) > kClusterMaxBytes) return 0;
     return (int)band;
 }
 
-// The dynamic shared-memory attribute, set once per device.
+// Per device, once: the dynamic shared-memory attribute of both kernels, and
+// whether a 16-block (non-portable) cluster of the largest band can be
+// resident.  Returns the widest usable cluster: 16, 8, or 0 for none.
 template <typename T>
-cudaError_t cluster_prepare() {
-    static cudaError_t status[64] = {};
+int cluster_prepare() {
+    static int width[64] = {};
     static bool done[64] = {};
     const int d = device_slot();
     if (!done[d]) {
-        status[d] = cudaFuncSetAttribute(diffuse_cluster_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kClusterMaxBytes);
-        if (status[d] != cudaSuccess) cudaGetLastError();
         done[d] = true;
+        int w = 0;
+        if (cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kClusterMaxBytes) == cudaSuccess)
+            w = 8;
+        if (w && FVF_CLUSTER_MAX >= 16 &&
+            cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kClusterMaxBytes) == cudaSuccess &&
+            cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 16;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(16);
+            cfg.blockDim = dim3(kClusterThreads);
+            cfg.dynamicSmemBytes = (size_t)kClusterMaxBytes;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, diffuse_cluster_kernel<T, 16>, &cfg) ==
+                    cudaSuccess &&
+                clusters > 0)
+                w = 16;
+        }
+        cudaGetLastError();
+        width[d] = w;
     }
-    return status[d];
+    return width[d];
+}
+
+template <typename T, int CS>
+cudaError_t launch_cluster(T *u, T *v, int nx, int ny, int band, int64_t nsteps, T alpha,
+                           cudaStream_t stream) {
+    // threads: the band's cells rounded up to a warp, at most kClusterThreads
+    const int cells = band * nx;
+    const int threads = cells >= kClusterThreads ? kClusterThreads : ((cells + 31) / 32) * 32;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CS);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = (size_t)(2 * cells) * sizeof(T);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // u is both the input and an output: every block reads its band before
+    // the first cluster barrier and writes after the last.
+    return cudaLaunchKernelEx(&cfg, diffuse_cluster_kernel<T, CS>, (const T *)u, u, v, nx, ny,
+                              band, nsteps, alpha);
 }
 
 constexpr size_t tblock_smem_bytes(size_t elem) { return 2 * (size_t)kTbW * kTbH * elem; }
 
-// Whether to run blocks of steps in shared memory: FP32 is HBM-bound, so
-// blocking cuts its traffic about sixfold; FP64 is arithmetic-bound on large
-// grids (the halo's recomputation would only cost), so it is blocked only on
-// grids small enough that launches, not arithmetic, dominate.
+// Whether to run blocks of steps in shared memory (FP32 only): FP32 is
+// HBM-bound, so blocking cuts its traffic about sixfold.  FP64 is bound by
+// its arithmetic, and a block of steps puts a tile's whole multi-step work on
+// one SM: measured 3x slower than a launch per step even at 1024^2 (778 vs
+// 258 us for 20 steps) and far slower on grids of fewer tiles than SMs.
 template <typename T>
 bool use_tblock(int64_t nx, int64_t ny, int64_t nsteps) {
-    if (nsteps < 3) return false;
+    if (sizeof(T) != 4 || nsteps < 3) return false;
     const int64_t tiles_y = (ny + kTbY - 1) / kTbY;
-    if (tiles_y > 65535 || (nx + kTbX - 1) / kTbX > 0x7fffffff) return false;
-    if (sizeof(T) == 4) return true;
-    return nx * ny <= (int64_t)1024 * 1024;
+    return tiles_y <= 65535 && (nx + kTbX - 1) / kTbX <= 0x7fffffff;
 }
 
 template <typename T>
@@ -609,46 +684,56 @@ template <typename T>
 cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
                 cudaStream_t stream, uint64_t *launches) {
     cudaError_t e;
-    if (const int band = cluster_band<T>(nx, ny, nsteps)) {
-        if (cluster_prepare<T>() == cudaSuccess) {
-            // u is both the input and an output: every block reads its band
-            // before the first cluster barrier and writes after the last.
-            const size_t smem = (size_t)(2 * band * nx) * sizeof(T);
-            diffuse_cluster_kernel<T><<<kClusterSize, kClusterThreads, smem, stream>>>(
-                u, u, v, (int)nx, (int)ny, band, nsteps, alpha);
-            ++*launches;
-            return cudaGetLastError();
+    // small grids (both states of an eighth of the grid fit one block's
+    // shared memory): all steps in one cluster launch, of 16 blocks where the
+    // device allows a cluster that wide and the grid has two rows per block
+    const int width =
+        FVF_CLUSTER_MAX >= 8 && cluster_band<T>(nx, ny, nsteps, 8) ? cluster_prepare<T>() : 0;
+    if (width) {
+        if (width == 16 && ny >= 32) {
+            const int band = cluster_band<T>(nx, ny, nsteps, 16);
+            e = launch_cluster<T, 16>(u, v, (int)nx, (int)ny, band, nsteps, alpha, stream);
+        } else {
+            const int band = cluster_band<T>(nx, ny, nsteps, 8);
+            e = launch_cluster<T, 8>(u, v, (int)nx, (int)ny, band, nsteps, alpha, stream);
         }
+        if (e != cudaSuccess) return e;
+        ++*launches;
+        return cudaGetLastError();
     }
     SingleStep<T> one;
     e = one.setup(u, v, nx, ny);
     if (e != cudaSuccess) return e;
-    if (use_tblock<T>(nx, ny, nsteps) && tblock_prepare<T>() == cudaSuccess) {
-        // Steps 1..n-1 in B blocked launches, step n as one single-step
-        // launch, so the other buffer ends holding step n-1.  Launch k reads
-        // u (k even) or v (k odd); step n-1 must end in u when n is odd (the
-        // last step writes v) and in v when n is even, i.e. B must have the
-        // parity of n+1.  B = n-1 (one step per launch) always has it, so
-        // raising B by one when needed keeps B <= n-1.
-        const int64_t n1 = nsteps - 1;
-        int64_t nb = (n1 + kTbSteps - 1) / kTbSteps;
-        if ((nb & 1) != ((nsteps + 1) & 1)) ++nb;
-        const dim3 grid((unsigned)((nx + kTbX - 1) / kTbX), (unsigned)((ny + kTbY - 1) / kTbY));
-        const size_t smem = tblock_smem_bytes(sizeof(T));
-        for (int64_t k = 0; k < nb; ++k) {
-            const int steps = (int)(n1 / nb + (k < n1 % nb ? 1 : 0));
-            const T *src = (k & 1) ? v : u;
-            T *dst = (k & 1) ? u : v;
-            diffuse_tblock_kernel<T><<<grid, kTbThreads, smem, stream>>>(src, dst, nx, ny, steps,
-                                                                          alpha);
+    // FP32 only: FP64 takes one launch per step (see use_tblock)
+    if constexpr (sizeof(T) == 4) {
+        if (use_tblock<T>(nx, ny, nsteps) && tblock_prepare<T>() == cudaSuccess) {
+            // Steps 1..n-1 in B blocked launches, step n as one single-step
+            // launch, so the other buffer ends holding step n-1.  Launch k reads
+            // u (k even) or v (k odd); step n-1 must end in u when n is odd (the
+            // last step writes v) and in v when n is even, i.e. B must have the
+            // parity of n+1.  B = n-1 (one step per launch) always has it, so
+            // raising B by one when needed keeps B <= n-1.
+            const int64_t n1 = nsteps - 1;
+            int64_t nb = (n1 + kTbSteps - 1) / kTbSteps;
+            if ((nb & 1) != ((nsteps + 1) & 1)) ++nb;
+            const dim3 grid((unsigned)((nx + kTbX - 1) / kTbX),
+                            (unsigned)((ny + kTbY - 1) / kTbY));
+            const size_t smem = tblock_smem_bytes(sizeof(T));
+            for (int64_t k = 0; k < nb; ++k) {
+                const int steps = (int)(n1 / nb + (k < n1 % nb ? 1 : 0));
+                const T *src = (k & 1) ? v : u;
+                T *dst = (k & 1) ? u : v;
+                diffuse_tblock_kernel<T><<<grid, kTbThreads, smem, stream>>>(src, dst, nx, ny,
+                                                                              steps, alpha);
+                ++*launches;
+                if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            }
+            const T *src = (nsteps & 1) ? u : v;
+            T *dst = (nsteps & 1) ? v : u;
+            one.launch(src, dst, nx, ny, alpha, stream);
             ++*launches;
-            if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            return cudaGetLastError();
         }
-        const T *src = (nsteps & 1) ? u : v;
-        T *dst = (nsteps & 1) ? v : u;
-        one.launch(src, dst, nx, ny, alpha, stream);
-        ++*launches;
-        return cudaGetLastError();
     }
     for (int64_t s = 1; s <= nsteps; ++s) {
         const T *src = (s & 1) ? u : v;

@@ -1,6 +1,6 @@
 """Every entry point through the index-checking debug build (libfvf_check.so,
 built with FVF_BOUNDS_CHECK): on small grids that exercise every kernel (the
-scalar, march, blocked and cluster 2D diffusion kernels, both 3D kernels, the
+scalar, march, blocked and both cluster 2D diffusion kernels, both 3D kernels, the
 x and transposing packs with and without the copy, the flux difference, the
 stage update), the results must still match the oracle bit for bit and no
 kernel may have met an index outside its arrays (fvf_device_error bit 2)."""
@@ -35,8 +35,9 @@ def _no_flags():
 
 @pytest.mark.parametrize("dt", [np.float64, np.float32])
 @pytest.mark.parametrize("nx,ny,steps", [
-    (31, 27, 7), (64, 64, 32), (3, 5, 2),   # cluster kernel (all steps in one launch)
-    (2048, 200, 9),                          # blocked kernel, then one single step
+    (31, 27, 7), (3, 5, 2),                 # 8-block cluster kernel (all steps in one launch)
+    (64, 64, 32), (33, 65, 5),               # 16-block cluster kernel
+    (2048, 200, 9),                          # FP32: blocked kernel, then one single step
     (2048, 200, 1),                          # vector march kernel
     (2047, 100, 1),                          # scalar kernel (rows not 16-byte aligned)
 ])

@@ -179,13 +179,16 @@ def test_full_size_8192_200_steps(dt):
 
 
 @pytest.mark.parametrize("dt", [np.float32, np.float64])
-@pytest.mark.parametrize("nx,ny", [(300, 250), (113, 65), (224, 128), (1000, 7), (9, 600)])
+@pytest.mark.parametrize("nx,ny", [(300, 250), (1130, 65), (224, 160), (4000, 11), (9, 6000),
+                                   (113, 65), (224, 128), (1000, 7), (9, 600)])
 @pytest.mark.parametrize("steps", [3, 4, 9, 16, 17, 24])
 def test_blocked_steps_multi_tile(dt, nx, ny, steps):
-    """Step counts that take the shared-memory blocked path (up to 8 steps
-    per launch, the last step on its own): several tiles, ragged tile edges,
-    random values everywhere including the edges; both buffers bit-exact
-    (the other buffer must hold step n-1)."""
+    """Step counts that take the shared-memory blocked path in FP32 (up to 8
+    steps per launch, the last step on its own) on grids above the cluster
+    kernel's 32K cells, and the 16- or 8-block cluster kernel on smaller
+    ones; FP64 takes one launch per step above 32K cells.  Several tiles,
+    ragged tile edges, random values everywhere including the edges; both
+    buffers bit-exact (the other buffer must hold step n-1)."""
     torch = torch_cuda()
     n = nx * ny
     u0 = (inputs.uniform_f32(11, nx + ny, n) if dt == np.float32
