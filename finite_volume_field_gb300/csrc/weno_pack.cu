@@ -12,16 +12,25 @@
 // output cell, the variable loop sequential inside the thread, the index
 // arithmetic done once per cell and reused for every variable.  x keeps the
 // contiguous index on the lanes for both the load and the store.  y and z are
-// transposes: a block stages a 32 x 32 tile of each variable in shared memory
-// so that both the global load (along j) and the global store (along the
-// swept axis) are coalesced.
+// transposes: a block of 128 threads stages a 32 x 32 tile of each variable
+// in shared memory so that both the global load (along j) and the global
+// store (along the swept axis) are coalesced.
 #include "fvf_internal.cuh"
 
 namespace fvf {
 namespace {
 
 constexpr int kTile = 32;
-constexpr int kRows = 8;  // threads along the second tile axis
+// threads along the second tile axis of the transposing kernel (each thread
+// then moves kTile / rows elements of a variable's tile).  4 rows (8 elements
+// per thread, 128-thread blocks) measured 3-5% faster on GB300 than 8 rows,
+// and 16 rows 12-25% slower; 2 rows equal in FP32, slower in FP64.
+#ifndef FVF_PACK_ROWS_F64
+#define FVF_PACK_ROWS_F64 4
+#endif
+#ifndef FVF_PACK_ROWS_F32
+#define FVF_PACK_ROWS_F32 4
+#endif
 
 // x: out(a, b, c, i) = f_i(a, b+g2, c+g3); (M1, M2, M3) = (N1, n2, n3).
 // T is double or float: the pack is a copy of 8- or 4-byte elements.  The
@@ -79,15 +88,14 @@ pack_x_kernel(FieldTable t, int nv, int64_t N1, int64_t N2, int64_t n2, int64_t 
 //   z: a = l, jt = j, q = k; packed extents (N3, n2, n1)
 // The tile is double-buffered across variables: the loads of variable i+1
 // are in flight while variable i is stored, with one barrier per variable.
-constexpr int kPer = kTile / kRows;
 
 struct TransposeGeom {
     int64_t na, nj, nq, jo, qo, pj, pq, pnj, pnq, sa, sq, da, dq, plane, tiles_a, tiles_j;
     int64_t stored;  // elements of one field's stored box (index checks)
 };
 
-template <typename T, bool COPY, typename Idx>
-__global__ void __launch_bounds__(kTile * kRows)
+template <typename T, bool COPY, typename Idx, int R>
+__global__ void __launch_bounds__(kTile * R)
 pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                       T *__restrict__ out) {
     // geometry in the index type of this instantiation: 32-bit when every
@@ -98,7 +106,8 @@ pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
     const Idx plane = (Idx)G.plane, tiles_a = (Idx)G.tiles_a, tiles_j = (Idx)G.tiles_j;
     const Idx stored = (Idx)G.stored;
     constexpr int TA = kTile;            // tile extent along a
-    constexpr int LP = kPer;             // loads per thread and variable
+    constexpr int LP = kTile / R;        // loads per thread and variable
+    constexpr int kRows = R, kPer = LP;
     __shared__ T tile[2][TA][kTile + 1];
     Idx blk = (Idx)blockIdx.x;
     const Idx ta = blk % tiles_a;
@@ -312,14 +321,15 @@ static cudaError_t launch_transpose(const FieldTable &fields, const CopyTable &c
     // 8 x 207^3) while every index a block forms, including those of the rows
     // and columns past the box edge that it computes but does not use, fits
     const int64_t lim = (int64_t)1 << 31;
-    const bool narrow = G.stored + 8 * G.sa + G.sq + 64 < lim &&
+    const bool narrow = G.stored + 32 * G.sa + G.sq + 64 < lim &&
                         G.plane * nv + 40 * G.da + G.dq + 64 < lim && blocks < lim;
+    constexpr int R = sizeof(T) == 4 ? FVF_PACK_ROWS_F32 : FVF_PACK_ROWS_F64;
     if (narrow)
-        pack_transpose_kernel<T, COPY, int32_t><<<(unsigned)blocks, dim3(kTile, kRows), 0,
-                                                  stream>>>(fields, copies, nv, G, out);
+        pack_transpose_kernel<T, COPY, int32_t, R><<<(unsigned)blocks, dim3(kTile, R), 0,
+                                                     stream>>>(fields, copies, nv, G, out);
     else
-        pack_transpose_kernel<T, COPY, int64_t><<<(unsigned)blocks, dim3(kTile, kRows), 0,
-                                                  stream>>>(fields, copies, nv, G, out);
+        pack_transpose_kernel<T, COPY, int64_t, R><<<(unsigned)blocks, dim3(kTile, R), 0,
+                                                     stream>>>(fields, copies, nv, G, out);
     return cudaSuccess;
 }
 
