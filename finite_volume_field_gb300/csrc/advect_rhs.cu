@@ -40,16 +40,21 @@
 #ifndef FVF_RHS_F32_GROUP
 #define FVF_RHS_F32_GROUP 8
 #endif
-// FP32 form: at least this many blocks per SM (a register cap that keeps
-// more loads in flight for 4-byte elements; measured 20% faster on GB300).
-// The FP64 form takes no minimum (0): a minimum of 1 already changed the
-// compiler's register allocation and measured slower.
-#ifndef FVF_RHS_F32_MINB
-#define FVF_RHS_F32_MINB 4
-#endif
 
 namespace fvf {
 namespace {
+
+// Minimum resident blocks per SM, per form (a register cap; 0 = none), as
+// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7: the FP32 form at 4
+// (20% faster: more loads in flight for 4-byte elements), the assigning FP64
+// y form at 6 (5-7% faster despite a few spilled registers) and the
+// accumulating one at 5 (7%).  The other FP64 forms take none: a cap there
+// measured 5-13% slower, and even a minimum of 1 changes the compiler's
+// register allocation (48 -> 64-84 registers, 9-43% slower).
+template <int DIR, bool ACC, typename T>
+constexpr int min_blocks() {
+    return sizeof(T) == 4 ? 4 : (DIR == 1 ? (ACC ? 5 : 6) : 0);
+}
 
 constexpr int kThreads = 256;
 // variables per load batch: 4 FP64 or 8 FP32, 64 bytes of face loads each
@@ -102,7 +107,7 @@ __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, 
 // has a cell whatever n1 is: the kernel is bound by the FP64 unit, which
 // charges idle lanes.
 template <int DIR, bool ACC, typename Idx, typename Off, typename T>
-__global__ void __launch_bounds__(kThreads, sizeof(T) == 4 ? FVF_RHS_F32_MINB : 0)
+__global__ void __launch_bounds__(kThreads, min_blocks<DIR, ACC, T>())
 advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int nv,
                   int64_t n1_, int64_t n2_, int64_t n3_, T *__restrict__ rhs) {
     const Idx n1 = (Idx)n1_, n2 = (Idx)n2_;
