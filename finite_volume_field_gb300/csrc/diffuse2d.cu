@@ -231,8 +231,14 @@ __device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int
     return r;
 }
 
+// FP64: at least 12 blocks of 128 threads per SM (a 40-register cap, one
+// 8-byte spill): 2% faster per 8192^2 step on GB300 than the 48-register
+// default (10 blocks).
+#ifndef FVF_MARCH_F64_MINB
+#define FVF_MARCH_F64_MINB 12
+#endif
 template <typename T>
-__global__ void __launch_bounds__(kMarchThreads)
+__global__ void __launch_bounds__(kMarchThreads, sizeof(T) == 8 ? FVF_MARCH_F64_MINB : 0)
 diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                      int64_t rows_per_block, T alpha) {
     constexpr int V = Vec16<T>::n;
