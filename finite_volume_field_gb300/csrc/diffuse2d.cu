@@ -472,7 +472,6 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
 // as in the other kernels, so the same bits.  At the end every block writes
 // its band of the last state to the result array and of the state before it
 // to the other array.
-// widest cluster tried (16, or 8 to stay within the portable size)
 #ifndef FVF_CLUSTER_MAX
 #define FVF_CLUSTER_MAX 16
 #endif
