@@ -137,6 +137,51 @@ def test_rhs_special_values_and_alias():
     torch.cuda.synchronize()
 
 
+def _tie_faces(seed, nv, extents, direction):
+    """Face fluxes whose differences are exact values with a set last
+    significand bit (every other face zero), so that their products with a
+    spacing of few significand bits (1.5, 0.75, 1.25) land exactly halfway
+    between two doubles, or one unit either side: round-to-even territory."""
+    fl = inputs.face_fluxes(seed, nv, extents, direction)
+    bits = fl.view(np.uint64) | np.uint64(1)                    # odd significands
+    bits ^= (inputs.random_bits(seed, 900, fl.size) & np.uint64(2))  # and next-to-last bits
+    fl = bits.view(np.float64).copy()
+    fe = oracle.flux_extents(extents, direction)
+    f4 = fl.reshape(nv, fe[2], fe[1], fe[0])
+    idx = [np.arange(m) for m in fe]
+    mask = (idx[direction] % 2 == 1)
+    if direction == 0:
+        f4[:, :, :, mask] = 0.0
+    elif direction == 1:
+        f4[:, :, mask, :] = 0.0
+    else:
+        f4[:, mask, :, :] = 0.0
+    return f4.reshape(-1)
+
+
+@pytest.mark.parametrize("direction", [0, 1, 2])
+@pytest.mark.parametrize("nv", [4, 8])
+def test_rhs_products_at_rounding_ties(direction, nv):
+    """Spacings 1.5, 0.75 and 1.25 times differences with odd significands:
+    the exact products sit on or beside rounding ties, where the integer-pipe
+    product's sticky bit and ties-to-even decide the last bit.  Assigning and
+    accumulating forms, every variable slot of a load batch."""
+    torch = torch_cuda()
+    extents = (37, 9, 6)
+    flux = _tie_faces(21, nv, extents, direction)
+    n_dir = extents[direction]
+    inv_d = np.resize(np.array([1.5, 0.75, 1.25, -1.5, 3.0 * 2.0 ** -900]), n_dir).astype(np.float64)
+    got = _gpu_rhs(torch, flux, inv_d, nv, extents, direction)
+    want = oracle.advect_rhs(flux, inv_d, nv, extents, direction)
+    assert_bits_equal(got, want, what=f"assign dir {direction}")
+    old = inputs.normal_f64(22, direction, got.size)
+    rhs = to_dev(old)
+    api.advect_rhs_add(to_dev(flux), to_dev(inv_d), nv, extents, direction, rhs)
+    torch.cuda.synchronize()
+    assert_bits_equal(to_host(rhs), oracle.advect_rhs_add(flux, inv_d, nv, extents, direction, old),
+                      what=f"accumulate dir {direction}")
+
+
 # ---------------------------------------------------------------------------
 # Full-size workloads, in the launch configuration the benchmark uses
 # ---------------------------------------------------------------------------
