@@ -1,9 +1,12 @@
-"""The integer-pipe binary64 addition used by the FP64 kernels
-(finite_volume_field_gb300/csrc/fp64_emu.cuh) is bit-identical to IEEE 754
-round-to-nearest-even addition: the same header, compiled for the host, is
-checked against the host CPU's own addition on about ten million operand
-pairs (random bit patterns, every exponent difference up to 70,
-cancellations, ties, the ends of the exponent range and special values)."""
+"""The integer-pipe binary64 addition and multiplication used by the FP64
+kernels (finite_volume_field_gb300/csrc/fp64_emu.cuh) are bit-identical to
+IEEE 754 round-to-nearest-even arithmetic: the same header, compiled for the
+host, is checked against the host CPU's own addition and multiplication on
+about 21 million operand pairs (random bit patterns, every exponent
+difference up to 70, cancellations, ties, products from deep underflow to
+overflow, exact and halfway products, subnormal operands, the ends of the
+exponent range and special values; the complete algorithms and the fast
+paths, including the fixed-factor product with either operand fixed)."""
 from __future__ import annotations
 
 import shutil
@@ -15,7 +18,7 @@ import pytest
 HERE = Path(__file__).resolve().parent
 
 
-def test_emulated_add_matches_ieee(tmp_path):
+def test_emulated_add_and_mul_match_ieee(tmp_path):
     cxx = shutil.which("g++") or shutil.which("c++")
     if cxx is None:
         pytest.skip("no host C++ compiler")
