@@ -32,6 +32,8 @@
 //          device or the grid does not allow 16) thread-block cluster.
 // FP64 takes the cluster kernel or one march (or scalar) launch per step.
 // The cluster, blocked and march kernels are described below.
+#include <atomic>
+
 #include <cooperative_groups.h>
 
 // The FP64 update reads bit patterns word by word (fp64_emu.cuh): 6% faster
@@ -277,19 +279,20 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
 
 template <typename T>
 int march_blocks_per_sm() {
-    static int cached[64] = {0};  // per device; a repeated fill writes the same value
+    // per device; concurrent first calls compute and store the same value
+    static std::atomic<int> cached[64];
     const int d = device_slot();
-    if (cached[d] == 0) {
-        int n = 0;
+    int n = cached[d].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, diffuse_march_kernel<T>,
                                                           kMarchThreads, 0) != cudaSuccess ||
             n <= 0) {
             cudaGetLastError();
             n = 8;
         }
-        cached[d] = n;
+        cached[d].store(n, std::memory_order_relaxed);
     }
-    return cached[d];
+    return n;
 }
 
 // ---------------------------------------------------------------------------
@@ -556,43 +559,41 @@ int cluster_band(int64_t nx, int64_t ny, int64_t nsteps, int cs) {
 // resident.  Returns the widest usable cluster: 16, 8, or 0 for none.
 template <typename T>
 int cluster_prepare() {
-    static int width[64] = {};
-    static bool done[64] = {};
+    static std::atomic<int> width1[64];   // width + 1 once known (0: not yet)
     const int d = device_slot();
-    if (!done[d]) {
-        done[d] = true;
-        int w = 0;
-        if (cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kClusterMaxBytes) == cudaSuccess)
-            w = 8;
-        if (w && FVF_CLUSTER_MAX >= 16 &&
-            cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kClusterMaxBytes) == cudaSuccess &&
-            cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 16;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(16);
-            cfg.blockDim = dim3(kClusterThreads);
-            cfg.dynamicSmemBytes = (size_t)kClusterMaxBytes;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, diffuse_cluster_kernel<T, 16>, &cfg) ==
-                    cudaSuccess &&
-                clusters > 0)
-                w = 16;
-        }
-        cudaGetLastError();
-        width[d] = w;
+    const int known = width1[d].load(std::memory_order_relaxed);
+    if (known) return known - 1;
+    int w = 0;
+    if (cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kClusterMaxBytes) == cudaSuccess)
+        w = 8;
+    if (w && FVF_CLUSTER_MAX >= 16 &&
+        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kClusterMaxBytes) == cudaSuccess &&
+        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 16;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(16);
+        cfg.blockDim = dim3(kClusterThreads);
+        cfg.dynamicSmemBytes = (size_t)kClusterMaxBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, diffuse_cluster_kernel<T, 16>, &cfg) ==
+                cudaSuccess &&
+            clusters > 0)
+            w = 16;
     }
-    return width[d];
+    cudaGetLastError();
+    width1[d].store(w + 1, std::memory_order_relaxed);
+    return w;
 }
 
 template <typename T, int CS>
@@ -635,17 +636,16 @@ bool use_tblock(int64_t nx, int64_t ny, int64_t nsteps) {
 
 template <typename T>
 cudaError_t tblock_prepare() {
-    static cudaError_t status[64] = {};
-    static bool done[64] = {};
+    static std::atomic<int> status1[64];  // status + 1 once known (0: not yet)
     const int d = device_slot();
-    if (!done[d]) {
-        status[d] = cudaFuncSetAttribute(diffuse_tblock_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tblock_smem_bytes(sizeof(T)));
-        if (status[d] != cudaSuccess) cudaGetLastError();
-        done[d] = true;
-    }
-    return status[d];
+    const int known = status1[d].load(std::memory_order_relaxed);
+    if (known) return (cudaError_t)(known - 1);
+    const cudaError_t st = cudaFuncSetAttribute(diffuse_tblock_kernel<T>,
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                (int)tblock_smem_bytes(sizeof(T)));
+    if (st != cudaSuccess) cudaGetLastError();
+    status1[d].store((int)st + 1, std::memory_order_relaxed);
+    return st;
 }
 
 // One-step launches (march or scalar kernel), configured once per call.

@@ -37,6 +37,7 @@
 //          planes into runs so that about 8 blocks per SM are in flight.
 #include <cuda.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "fp64_emu.cuh"
@@ -84,7 +85,8 @@ template <int BIT>
 __device__ __forceinline__ float mulk_rn(float k, float x) { return __fmul_rn(k, x); }
 template <int BIT>
 __device__ __forceinline__ double mulk_rn(double k, double x) {
-    if (FVF_3D_EMU_MUL & BIT) return emu::from_bits(emu::mul_const_bits(emu::bits(x), emu::mul_const(k)));
+    if (FVF_3D_EMU_MUL & BIT)
+        return emu::from_bits(emu::mul_const_bits(emu::bits(x), emu::mul_const(k)));
     return __dmul_rn(k, x);
 }
 
@@ -484,8 +486,11 @@ cudaError_t launch_bulk(const CUtensorMap &src_map, T *dst, int64_t nx, int64_t 
                         T alpha, cudaStream_t stream) {
     constexpr int TX = 32 * (16 / sizeof(T));
     constexpr size_t smem = bulk_smem_bytes<T>();
-    static int per_sm_dev[64] = {0};  // per device: the attribute and occupancy
-    int &per_sm = per_sm_dev[device_slot()];
+    // per device, the attribute and occupancy; concurrent first calls compute
+    // and store the same value
+    static std::atomic<int> per_sm_dev[64];
+    const int d = device_slot();
+    int per_sm = per_sm_dev[d].load(std::memory_order_relaxed);
     if (per_sm == 0) {
         if (smem > 48 * 1024 &&
             cudaFuncSetAttribute(diffuse3d_bulk_kernel<T>,
@@ -500,6 +505,7 @@ cudaError_t launch_bulk(const CUtensorMap &src_map, T *dst, int64_t nx, int64_t 
             n = 1;
         }
         per_sm = n;
+        per_sm_dev[d].store(n, std::memory_order_relaxed);
     }
     const int64_t tiles_x = (nx + TX - 1) / TX, tiles_y = (ny + kBulkRows - 1) / kBulkRows;
     const int64_t kz_len = FVF_3D_KZ;  // planes per item

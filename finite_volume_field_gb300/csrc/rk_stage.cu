@@ -154,9 +154,11 @@ rk_stage_kernel(RkStageArgs A) {
                     if (FUSED) {
                         rr = mul_rn<1>(wx, mx, sub_rn<16>(xl[q], xh[q], v), v);
                         if (FY)
-                            rr = add_rn<1>(rr, mul_rn<2>(wy, my, sub_rn<32>(yl[q], yh[q], v), v), v);
+                            rr = add_rn<1>(
+                                rr, mul_rn<2>(wy, my, sub_rn<32>(yl[q], yh[q], v), v), v);
                         if (FZ)
-                            rr = add_rn<2>(rr, mul_rn<4>(wz, mz, sub_rn<64>(zl[q], zh[q], v), v), v);
+                            rr = add_rn<2>(
+                                rr, mul_rn<4>(wz, mz, sub_rn<64>(zl[q], zh[q], v), v), v);
                     } else {
                         rr = r[q];
                     }
