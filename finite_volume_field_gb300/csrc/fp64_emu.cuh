@@ -235,7 +235,9 @@ FVF_HD double add(double a, double b) { return from_bits(add_bits(bits(a), bits(
 // normalisation, a sticky bit for the low 64 bits, and the rounding and
 // packing of the addition above.  The 64 x 64-bit product is formed from
 // four 32 x 32 -> 64-bit products, integer multiply-adds that issue on the
-// FMA pipe rather than the ALU pipe the additions load.
+// FMA pipe; measured on GB300, a product costs about 31 ALU-pipe and 15
+// FMA-pipe instructions, against about 46 ALU-pipe instructions for a
+// same-sign addition.
 // ---------------------------------------------------------------------------
 
 // hi:lo = a * b exactly.  Every partial sum stays below 2^64.
@@ -298,9 +300,9 @@ FVF_HD uint64_t mul_full_int(uint64_t A, uint64_t B) {
     return sgn | (((uint64_t)(e - 1) << 52) + mant);
 }
 
-// One factor fixed for a whole sweep (the diffusion coefficient): its
-// significand placed at the top of a 64-bit word and its exponent, prepared
-// once.  `fast` is 0 when the factor is zero, subnormal, infinite or NaN;
+// A factor shared by many products (a diffusion or stage coefficient for a
+// whole sweep, an inverse spacing for a cell's variables): its significand
+// placed at the top of a 64-bit word and its exponent, prepared once.  `fast` is 0 when the factor is zero, subnormal, infinite or NaN;
 // every product then takes the complete algorithm.
 struct MulConst {
     uint64_t bits;   // the factor's bit pattern
