@@ -984,7 +984,8 @@ def run_ncu_case():
     on the same fields (at most about 1.7 GB), flux difference x/y/z on
     8 x 201^3, the SSPRK3 stage fused with the x/y/z flux difference on
     8 x 201^3 (about 3.1 GB), one 3D 7-point diffusion step on 512^3 in FP32
-    then FP64 (at most 2.1 GB).  FP64 runs 2 single steps, FP32 17 steps (two
+    then FP64 (at most 2.1 GB), and the 64 x 64 FP64 centre impulse for 32
+    steps (one cluster launch).  FP64 runs 2 single steps, FP32 17 steps (two
     8-step shared-memory launches, then one single step).  Device-generated values (the
     kernels' timing does not depend on them)."""
     import torch
@@ -1041,6 +1042,12 @@ def run_ncu_case():
         api.diffuse3d_step(u, v, 512, 512, 512, 0.1, 1, code)
         del u, v
         free()
+    # the small-grid case: 64 x 64 FP64 centre impulse, 32 steps, one cluster launch
+    u = torch.zeros(64 * 64, dtype=torch.float64, device="cuda")
+    u[31 * 64 + 31] = 1.0
+    v = torch.zeros_like(u)
+    api.diffuse2d_step(u, v, 64, 64, 0.1, 32, api.FVF_FP64)
+    free()
     print("ncu case done", flush=True)
     return 0
 
