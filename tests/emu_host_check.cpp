@@ -51,6 +51,7 @@ static void check_mul(uint64_t A, uint64_t B) {
     const uint64_t want = bits(native_mul(a, b));
     ++cases;
     report("mul full", A, B, mul_full_int(A, B), want);
+    report("mul", A, B, bits(mul(a, b)), want);
     report("mul const", A, B, mul_const_bits(A, mul_const(b)), want);
     report("mul const swapped", B, A, mul_const_bits(B, mul_const(a)), want);
     uint64_t fast;
