@@ -46,7 +46,7 @@ WORKLOAD = ("2D 5-point diffusion 8192x8192, alpha 0.1, 200 steps, FP32 and FP64
             "(plus one pass of each other hot-path sweep: WENO pack x/y/z nv=8 207^3, "
             "flux difference x/y/z nv=8 201^3, 4800x1200 nv=7 pack+flux sequence x100)")
 FALLBACK_HBM_GBS = 6800.0
-FP64_NOMINAL_TFLOPS = 1.25   # FP64 rate of the part (FMA counted as 2 flops)
+FP64_NOMINAL_TFLOPS = 1.25   # nominal FP64 rate of the part (FMA = 2 flops): context only
 # Algorithmic FP64 flops per output element of the FP64 arithmetic sweeps.
 FP64_FLOPS = {"diffuse_fp64": 7, "rhs_x": 2, "rhs_y": 2, "rhs_z": 2}
 # FP64-unit instructions per element as built: the diffusion update has 6
@@ -573,7 +573,8 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
                "frac_hbm": round(nbytes / (t * 1e-3) / 1e9 / hbm, 4)}
         if flops:
             tf = flops * units / (t * 1e-3) / 1e12
-            rec.update(fp64_tflops=round(tf, 4), frac_fp64=round(tf / FP64_NOMINAL_TFLOPS, 4))
+            rec.update(fp64_tflops=round(tf, 4),
+                       frac_fp64_nominal=round(tf / FP64_NOMINAL_TFLOPS, 4))
         out[name] = rec
 
     scratch = torch.empty_like(sw.rhs_flux[1])
@@ -712,11 +713,34 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     return out
 
 
-def load_ablation():
-    """libfvf_ablation.so (built by buildlib.build_ablation) through ctypes."""
-    import ctypes
+ABLATION_SRCS = [ROOT / "ablation" / "collapse4.cu", ROOT / "ablation" / "peaks.cu"]
+ABLATION_LIB = ROOT / "ablation" / "libfvf_ablation.so"
+
+
+def build_ablation(force: bool = False) -> Path:
+    """Compile ablation/libfvf_ablation.so: the benchmark-only kernels -- the
+    one-thread-per-(cell, variable) mapping that libfvf's kernels replace,
+    and the arithmetic issue-rate probes.  Not part of libfvf and not used
+    by it; built with the library's nvcc flags."""
     from finite_volume_field_gb300 import buildlib
-    lib = ctypes.CDLL(str(buildlib.build_ablation()))
+    newest = max([p.stat().st_mtime for p in ABLATION_SRCS]
+                 + [Path(buildlib.__file__).stat().st_mtime])
+    if not force and ABLATION_LIB.exists() and ABLATION_LIB.stat().st_mtime >= newest:
+        return ABLATION_LIB
+    tmp = ABLATION_LIB.with_suffix(f".so.tmp{os.getpid()}")
+    cmd = [buildlib.nvcc(), *buildlib.NVCC_FLAGS, "-shared", "-cudart", "static",
+           *map(str, ABLATION_SRCS), "-o", str(tmp)]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on the ablation library:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, ABLATION_LIB)
+    return ABLATION_LIB
+
+
+def load_ablation():
+    """ablation/libfvf_ablation.so (built by build_ablation) through ctypes."""
+    import ctypes
+    lib = ctypes.CDLL(str(build_ablation()))
     vp, i64, cint = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.ablation_pack_x_collapse4.argtypes = [ctypes.POINTER(vp), cint, ctypes.POINTER(i64), cint,
                                               vp, vp]
@@ -783,6 +807,55 @@ def aggregate(per_rank, world):
     e2e_ms = max(r["e2e_ms_per_step"] for r in per_rank)
     launches = sum(r["launches"] for r in per_rank)
     return ms, e2e_ms, launches
+
+
+def roofline(r, name, sw, hbm, peak_kind, rates):
+    """The roofline object of the dominant kernel: algorithmic bytes of one
+    launch over its CUDA-event launch time, against the measured HBM copy
+    rate.  For an FP64 sweep, the same launch against this GPU's measured FP64
+    issue rate (the FP64-unit instructions the kernel issues per element as
+    built) sits beside it in ``fp64``; ``binding`` names the larger of the
+    two fractions."""
+    launch_ms = sw["ms"] / r["launches"]
+    achieved = r["per_launch_bytes"] / (launch_ms * 1e-3) / 1e9
+    roof = {"kernel": name, "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+            "unit": "GB/s", "frac": round(achieved / hbm, 4),
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+            "traffic": ncu_traffic(name), "launch_ms": round(launch_ms, 5),
+            "algorithmic_bytes_per_launch": r["per_launch_bytes"], "binding": "hbm"}
+    if name in FP64_FLOPS:
+        cells = r["per_launch_cells"]
+        tf = FP64_FLOPS[name] * cells / (launch_ms * 1e-3) / 1e12
+        fp = {"flops_per_element": FP64_FLOPS[name], "tflops": round(tf, 4),
+              "instructions_per_element": FP64_INSTR[name]}
+        peak_ops = rates.get("fp64_fma")
+        if peak_ops:
+            ops = FP64_INSTR[name] * cells / (launch_ms * 1e-3) / 1e12
+            fp.update(achieved=round(ops, 4), peak=peak_ops, unit="T FP64 instructions/s",
+                      frac=round(ops / peak_ops, 4),
+                      peak_source="measured: FP64 FMA issue-rate probe, this run")
+            if fp["frac"] > roof["frac"]:
+                roof["binding"] = "fp64"
+        roof["fp64"] = fp
+    return roof
+
+
+def blocked_traffic(ms, hbm):
+    """DRAM bytes that the blocked FP32 diffusion moves for the 8192^2 x 200
+    workload, from its tiling (each 8-step launch reads every 128 x 80 staged
+    region and writes every 112 x 64 tile; the last step is one plain launch
+    that reads and writes the grid), and that traffic's fraction of the HBM
+    copy rate: beside the row's effective fraction, which counts the one-pass
+    bytes of every step."""
+    tiles = -(-DIFF_N // 112) * -(-DIFF_N // 64)
+    n1 = DIFF_STEPS - 1
+    nb = -(-n1 // 8)
+    if nb % 2 != (DIFF_STEPS + 1) % 2:
+        nb += 1
+    b = nb * tiles * (128 * 80 + 112 * 64) * 4 + 2 * DIFF_N * DIFF_N * 4
+    return {"dram_bytes_model": b, "dram_gbs_model": round(b / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm_dram_model": round(b / (ms * 1e-3) / 1e9 / hbm, 4),
+            "note": "frac_hbm counts 8 one-pass steps per blocked launch (effective)"}
 
 
 def run_gpu(args):
@@ -905,40 +978,13 @@ def run_gpu(args):
             if name in FP64_FLOPS:
                 tf = FP64_FLOPS[name] * r["cellvars"] / (t * 1e-3) / 1e12
                 sweeps[name]["fp64_tflops"] = round(tf, 4)
-                sweeps[name]["frac_fp64"] = round(tf / FP64_NOMINAL_TFLOPS, 4)
+                if rates.get("fp64_fma"):
+                    ops = FP64_INSTR[name] * r["cellvars"] / (t * 1e-3) / 1e12
+                    sweeps[name]["frac_fp64_issue"] = round(ops / rates["fp64_fma"], 4)
         dom = max((n for n in R if n != "seq2d"), key=lambda n: sweeps[n]["ms"])
-        r = R[dom]
-        launch_ms = sweeps[dom]["ms"] / r["launches"]
-        roof = {"kernel": dom, "bound": "hbm",
-                "achieved": round(r["per_launch_bytes"] / (launch_ms * 1e-3) / 1e9, 1),
-                "peak": hbm, "unit": "GB/s", "peak_source": f"{peak_kind} hbm_gbs",
-                "traffic": ncu_traffic(dom), "launch_ms": round(launch_ms, 5),
-                "algorithmic_bytes_per_launch": r["per_launch_bytes"]}
-        roof["frac"] = round(roof["achieved"] / hbm, 4)
-        if dom in FP64_FLOPS:
-            # FP64 arithmetic bound: the algorithmic FP64 flops of one launch
-            # (7 per cell for the update: 3 neighbour adds, 4c, s - 4c,
-            # alpha*t, c + ...; 2 per element for the flux difference) over
-            # the launch time, against the part's nominal FP64 rate.
-            tf = FP64_FLOPS[dom] * r["per_launch_cells"] / (launch_ms * 1e-3) / 1e12
-            roof["fp64"] = {"achieved": round(tf, 4), "peak": FP64_NOMINAL_TFLOPS,
-                            "unit": "TFLOP/s", "frac": round(tf / FP64_NOMINAL_TFLOPS, 4),
-                            "flops_per_element": FP64_FLOPS[dom],
-                            "peak_source": "nominal FP64 rate of the part (recipe unit table)"}
-            if roof["fp64"]["frac"] > roof["frac"]:
-                roof.update(bound="alu", achieved=roof["fp64"]["achieved"],
-                            peak=FP64_NOMINAL_TFLOPS, unit="TFLOP/s", frac=roof["fp64"]["frac"],
-                            peak_source="nominal FP64 rate of the part (recipe unit table)")
-            # the same launch against this GPU's measured FP64 issue rate:
-            # the FP64-unit instructions the kernel issues per element as
-            # built (FP64_INSTR), over the launch time
-            peak_ops = rates.get("fp64_fma")
-            if peak_ops:
-                ops = FP64_INSTR[dom] * r["per_launch_cells"] / (launch_ms * 1e-3) / 1e12
-                roof["fp64_issue"] = {"achieved_tops": round(ops, 4),
-                                      "measured_peak_tops": peak_ops,
-                                      "frac": round(ops / peak_ops, 4),
-                                      "instructions_per_element": FP64_INSTR[dom]}
+        roof = roofline(R[dom], dom, sweeps[dom], hbm, peak_kind, rates)
+        if "diffuse_fp32" in sweeps:
+            sweeps["diffuse_fp32"].update(blocked_traffic(sweeps["diffuse_fp32"]["ms"], hbm))
         line = {
             "impl": "gb300", "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -951,7 +997,6 @@ def run_gpu(args):
                        "hbm_peak_source": peak_kind,
                        "seq2d": "one CUDA graph of its 400 launches per step" if not args.no_graph
                                 else "400 launches per step"},
-            "sweeps": sweeps,
             "roofline": roof,
             "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -968,6 +1013,8 @@ def run_gpu(args):
                                     "sample": ORACLE_SAMPLE_DESC,
                                     "gcell_var_per_s": round(cv / sec / 1e9, 4),
                                     "seconds": round(sec, 2)}
+        # the per-sweep table last: a reader of the end of the line sees it
+        line["sweeps"] = sweeps
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -97,28 +97,6 @@ def build(force: bool = False, verbose: bool = False, bounds_check: bool = False
     return lib
 
 
-ABLATION_SRCS = [PKG / "ablation" / "collapse4.cu", PKG / "ablation" / "peaks.cu"]
-ABLATION_LIB = PKG / "libfvf_ablation.so"
-
-
-def build_ablation(force: bool = False) -> Path:
-    """Compile libfvf_ablation.so: the benchmark-only kernels -- the
-    one-thread-per-(cell, variable) mapping that libfvf's kernels replace,
-    and the arithmetic issue-rate probes.  Not part of libfvf and not used
-    by it."""
-    newest = max([p.stat().st_mtime for p in ABLATION_SRCS] + [Path(__file__).stat().st_mtime])
-    if not force and ABLATION_LIB.exists() and ABLATION_LIB.stat().st_mtime >= newest:
-        return ABLATION_LIB
-    tmp = ABLATION_LIB.with_suffix(f".so.tmp{os.getpid()}")
-    cmd = [nvcc(), *NVCC_FLAGS, "-shared", "-cudart", "static", *map(str, ABLATION_SRCS), "-o",
-           str(tmp)]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on the ablation library:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, ABLATION_LIB)
-    return ABLATION_LIB
-
-
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
     print(LIB)
