@@ -537,7 +537,8 @@ def run_reference(args):
 
 def time_extra_sweeps(torch, sw, stream, reps=5):
     """Rows beyond the benchmark step, each timed on its own with CUDA events
-    on the launching stream (median of several calls after one warm-up call):
+    on the launching stream (median of several timings after one warm-up
+    call; calls under a millisecond are timed 8 back to back per timing):
     the accumulating flux difference and the directional flux copy back to
     the physical frame on the 8 x 201^3 flux workload's buffers, the
     conservative-variable copy alone and fused with the pack on the 8 x 207^3
@@ -555,15 +556,26 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
     out = {}
 
     def timed(fn):
+        # A call shorter than a millisecond is repeated back to back between
+        # the events (the time per call is the total over the calls): timed
+        # alone, the host-side argument checks and launch of a single call
+        # would show up as idle device time inside the interval.
         fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        inner = 1 if e0.elapsed_time(e1) >= 1.0 else 8
         times = []
         for _ in range(reps):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            fn()
+            for _ in range(inner):
+                fn()
             e1.record(stream)
             e1.synchronize()
-            times.append(e0.elapsed_time(e1))
+            times.append(e0.elapsed_time(e1) / inner)
         return statistics.median(times)
 
     def record(name, fn, nbytes, units, flops=0):

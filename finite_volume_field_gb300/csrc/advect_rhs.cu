@@ -10,13 +10,12 @@
 // Two FP64 operations per element would keep this kernel on GB300's FP64
 // unit, well below the HBM roof.  The multiplication by inv_d runs on the
 // integer pipes instead (fp64_emu.cuh: an exact binary64 product, the factor
-// prepared once per cell) for three of every four variables
-// (FVF_RHS_EMU_MUL = 7, one bit per slot of a load batch); on GB300 this
-// measured 20-26% faster than all-FP64 and than emulating all four (the
-// integer pipes saturate then).  The accumulating form takes all four
-// (FVF_RHS_EMU_MUL_ACC).  Moving the subtraction instead measured
-// slower: the exact addition costs about twice the integer instructions of
-// the product.
+// prepared once per cell) for three of every four variables (kMulMask = 7,
+// one bit per slot of a load batch); on GB300 this measured 20-26% faster
+// than all-FP64 and than emulating all four (the integer pipes saturate
+// then).  The accumulating form takes all four (kMulMaskAcc).  Moving the
+// subtraction instead measured slower: the exact addition costs about twice
+// the integer instructions of the product.
 //
 // Mapping ("Why this is faster" on the same page): one thread per spatial
 // cell; the inverse spacing is loaded once per cell, outside the variable
@@ -26,49 +25,37 @@
 #include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
 
-#ifndef FVF_RHS_EMU
-#define FVF_RHS_EMU 0
-#endif
-#ifndef FVF_RHS_EMU_MUL
-#define FVF_RHS_EMU_MUL 7
-#endif
-// the same for the accumulating form, whose extra read and add change the
-// balance: all four slots measured 2-7% faster there
-#ifndef FVF_RHS_EMU_MUL_ACC
-#define FVF_RHS_EMU_MUL_ACC 15
-#endif
-#ifndef FVF_RHS_F32_GROUP
-#define FVF_RHS_F32_GROUP 8
-#endif
-
 namespace fvf {
 namespace {
 
+// Variable slots of a load batch whose product runs on the integer pipes
+// (bit q: slot q): three of four for the assigning form; all four for the
+// accumulating form, whose extra read and add change the balance (2-7%
+// faster there).
+constexpr int kMulMask = 7;
+constexpr int kMulMaskAcc = 15;
+
 // Minimum resident blocks per SM, per form (a register cap; 0 = none), as
-// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7: the FP32 form at 4
-// (20% faster: more loads in flight for 4-byte elements), the assigning FP64
-// y form at 6 (5-7% faster despite a few spilled registers) and the
-// accumulating one at 5 (7%).  The other FP64 forms take none: a cap there
+// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7: the FP32 form at 6
+// (more loads in flight for 4-byte elements: 0.099 ms at 4 blocks, 0.093 ms
+// at 6, 0.146 ms at 8, timed back to back), the assigning FP64 y form at 6
+// (5-7% faster despite a few spilled registers) and the accumulating one at
+// 5 (7%).  The other FP64 forms take none: a cap there
 // measured 5-13% slower, and even a minimum of 1 changes the compiler's
 // register allocation (48 -> 64-84 registers, 9-43% slower).
 template <int DIR, bool ACC, typename T>
 constexpr int min_blocks() {
-    return sizeof(T) == 4 ? 4 : (DIR == 1 ? (ACC ? 5 : 6) : 0);
+    return sizeof(T) == 4 ? 6 : (DIR == 1 ? (ACC ? 5 : 6) : 0);
 }
 
 constexpr int kThreads = 256;
 // variables per load batch: 4 FP64 or 8 FP32, 64 bytes of face loads each
 template <typename T>
-__host__ __device__ constexpr int group_of() { return sizeof(T) == 4 ? FVF_RHS_F32_GROUP : 4; }
+__host__ __device__ constexpr int group_of() { return sizeof(T) == 4 ? 8 : 4; }
 
-// Face difference F(c-1) - F(c) of variable slot q of a batch: on the FP64
-// unit, or as an exact integer-pipe addition of -F(c) when bit q of
-// FVF_RHS_EMU is set.
+// Face difference F(c-1) - F(c) on the FP64 unit.
 template <int Q>
-__device__ __forceinline__ double face_diff(double lo, double hi) {
-    if ((FVF_RHS_EMU >> Q) & 1) return emu::add(lo, emu::from_bits(emu::bits(hi) ^ emu::kSign));
-    return __dsub_rn(lo, hi);
-}
+__device__ __forceinline__ double face_diff(double lo, double hi) { return __dsub_rn(lo, hi); }
 
 // FP32 form: binary32 operations, each rounded to nearest even.
 template <int Q>
@@ -136,7 +123,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
         const T *f = flux + lo;
         T *r = rhs + ro;
         constexpr int kGroup = group_of<T>();
-        constexpr int kMulMask = ACC ? FVF_RHS_EMU_MUL_ACC : FVF_RHS_EMU_MUL;
+        constexpr int kMask = ACC ? kMulMaskAcc : kMulMask;
         for (int i0 = 0; i0 < nv; i0 += kGroup) {
             T a[kGroup], b[kGroup], old[kGroup];
 #pragma unroll
@@ -152,7 +139,7 @@ advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int n
             }
 #define FVF_RHS_Q(Q)                                                                    \
     if (Q < kGroup && i0 + Q < nv) {                                                    \
-        const T term = w.template apply<kMulMask, Q>(face_diff<Q>(a[Q], b[Q]));        \
+        const T term = w.template apply<kMask, Q>(face_diff<Q>(a[Q], b[Q]));        \
         /* accumulate form: the term added once to the existing rhs */                 \
         if (FVF_IN(ro + (Off)(i0 + Q) * rplane, rall))                                  \
             r[(Off)(i0 + Q) * rplane] = ACC ? add_rn(old[Q], term) : term;             \

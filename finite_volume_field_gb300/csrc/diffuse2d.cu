@@ -44,27 +44,6 @@
 
 namespace cg = cooperative_groups;
 
-// How the FP64 update splits its additions between the FP64 unit and the
-// integer pipes (fp64_emu.cuh).  Every split gives bit-identical results; the
-// best one balances the two kinds of pipe.
-//   FVF_FP64_EMU_SUMS: how many of the three neighbour sums (W+E, +S, +N, in
-//                      that order) run on the integer pipes (0..3);
-//   FVF_FP64_EMU_T:    1 to also compute s - 4c on the integer pipes.
-//   FVF_FP64_EMU_MUL:  1 to compute alpha * (s - 4c) on the integer pipes.
-//   FVF_FP64_EMU_LAST: 1 to compute the final c + alpha * (s - 4c) there.
-#ifndef FVF_FP64_EMU_SUMS
-#define FVF_FP64_EMU_SUMS 2
-#endif
-#ifndef FVF_FP64_EMU_T
-#define FVF_FP64_EMU_T 0
-#endif
-#ifndef FVF_FP64_EMU_MUL
-#define FVF_FP64_EMU_MUL 0
-#endif
-#ifndef FVF_FP64_EMU_LAST
-#define FVF_FP64_EMU_LAST 0
-#endif
-
 namespace fvf {
 namespace {
 
@@ -113,37 +92,19 @@ __device__ __forceinline__ T update(T c, T w, T e, T s, T n, T alpha) {
     return update_hw<T>(c, w, e, s, n, alpha);
 }
 
-// FP64 update with part of the additions on the integer pipes; the same
+// FP64 update with the first two neighbour sums (W + E, then + S) on the
+// integer pipes (fp64_emu.cuh) and the rest on the FP64 unit: the same
 // operations in the same order, each correctly rounded, so the same bits.
+// This split balances the two kinds of pipe on GB300 (8192^2 step: 0.557 ms,
+// against 0.652 ms with all three sums emulated, 0.664 ms with one, 0.787 ms
+// with none; moving alpha * t or the last addition too measured slower).
 template <>
 __device__ __forceinline__ double update<double>(double c, double w, double e, double s,
                                                  double n, double alpha) {
-    double sum = FVF_FP64_EMU_SUMS >= 1 ? emu::add_same_sign(w, e) : __dadd_rn(w, e);
-    sum = FVF_FP64_EMU_SUMS >= 2 ? emu::add_same_sign(sum, s) : __dadd_rn(sum, s);
-    sum = FVF_FP64_EMU_SUMS >= 3 ? emu::add_same_sign(sum, n) : __dadd_rn(sum, n);
-    double t;
-#if FVF_FP64_EMU_T
-    // -4c is c with the exponent raised by two and the sign flipped, exactly,
-    // when c is normal and 4c stays normal (biased exponent 1..2044).
-    const uint64_t cb = emu::bits(c);
-    const uint32_t ec = (uint32_t)(cb >> 52) & 0x7FFu;
-    if (ec - 1u < 2044u)
-        t = emu::add(sum, emu::from_bits((cb + (2ull << 52)) ^ emu::kSign));
-    else
-        t = Rn<double>::sub4(sum, c);
-#else
-    t = Rn<double>::sub4(sum, c);
-#endif
-#if FVF_FP64_EMU_MUL
-    const double p = emu::from_bits(emu::mul_const_bits(emu::bits(t), emu::mul_const(alpha)));
-#else
-    const double p = __dmul_rn(alpha, t);
-#endif
-#if FVF_FP64_EMU_LAST
-    return emu::add(c, p);
-#else
-    return __dadd_rn(c, p);
-#endif
+    double sum = emu::add_same_sign(w, e);
+    sum = emu::add_same_sign(sum, s);
+    sum = __dadd_rn(sum, n);
+    return __dadd_rn(c, __dmul_rn(alpha, Rn<double>::sub4(sum, c)));
 }
 
 // ---------------------------------------------------------------------------
@@ -242,11 +203,9 @@ __device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int
 // FP64: at least 12 blocks of 128 threads per SM (a 40-register cap, one
 // 8-byte spill): 2% faster per 8192^2 step on GB300 than the 48-register
 // default (10 blocks).
-#ifndef FVF_MARCH_F64_MINB
-#define FVF_MARCH_F64_MINB 12
-#endif
+constexpr int kMarchF64MinBlocks = 12;
 template <typename T>
-__global__ void __launch_bounds__(kMarchThreads, sizeof(T) == 8 ? FVF_MARCH_F64_MINB : 0)
+__global__ void __launch_bounds__(kMarchThreads, sizeof(T) == 8 ? kMarchF64MinBlocks : 0)
 diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                      int64_t rows_per_block, T alpha) {
     constexpr int V = Vec16<T>::n;
@@ -481,9 +440,6 @@ diffuse_tblock_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx
 // as in the other kernels, so the same bits.  At the end every block writes
 // its band of the last state to the result array and of the state before it
 // to the other array.
-#ifndef FVF_CLUSTER_MAX
-#define FVF_CLUSTER_MAX 16
-#endif
 constexpr int kClusterThreads = 512;
 constexpr int64_t kClusterMaxBytes = 200 * 1024;   // per block: both states of a band
 // Largest grid the cluster kernel takes.  Measured on GB300 (16-block
@@ -584,7 +540,7 @@ int cluster_prepare() {
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kClusterMaxBytes) == cudaSuccess)
         w = 8;
-    if (w && FVF_CLUSTER_MAX >= 16 &&
+    if (w &&
         cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kClusterMaxBytes) == cudaSuccess &&
@@ -718,7 +674,7 @@ cudaError_t run(T *u, T *v, int64_t nx, int64_t ny, T alpha, int64_t nsteps,
     // shared memory): all steps in one cluster launch, of 16 blocks where the
     // device allows a cluster that wide and the grid has two rows per block
     const int width =
-        FVF_CLUSTER_MAX >= 8 && cluster_band<T>(nx, ny, nsteps, 8) ? cluster_prepare<T>() : 0;
+        cluster_band<T>(nx, ny, nsteps, 8) ? cluster_prepare<T>() : 0;
     if (width) {
         if (width == 16 && ny >= 32) {
             const int band = cluster_band<T>(nx, ny, nsteps, 16);

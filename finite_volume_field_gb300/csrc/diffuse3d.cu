@@ -45,23 +45,13 @@
 #include "mbarrier.cuh"
 
 // How the FP64 update splits its work between the FP64 unit and the integer
-// pipes (fp64_emu.cuh); every choice gives the same bits.  FVF_3D_EMU_SUMS:
-// how many of the five neighbour sums (W+E, +S, +N, +B, +T, in that order)
-// run on the integer pipes; FVF_3D_EMU_MUL: bit 1 the product alpha * (...),
-// bit 2 the product 6c.  Two sums and both products measured fastest on
-// GB300 (6% below three sums and no product).
-#ifndef FVF_3D_EMU_SUMS
-#define FVF_3D_EMU_SUMS 2
-#endif
-#ifndef FVF_3D_EMU_MUL
-#define FVF_3D_EMU_MUL 3
-#endif
-// 1: aligned FP32 grids take the bulk-copy kernel; 0: the register march
-// kernel.  FP64 always takes the march kernel, which measured faster there
-// (FP64 arithmetic, not memory, bounds the FP64 update).
-#ifndef FVF_3D_BULK
-#define FVF_3D_BULK 1
-#endif
+// pipes (fp64_emu.cuh): the first two of the five neighbour sums (W+E, +S,
+// +N, +B, +T, in that order) and both products (alpha * (...) and 6c) run on
+// the integer pipes.  This measured fastest on GB300 (6% below three sums
+// and no product); every split gives the same bits.  Aligned FP32 grids take
+// the bulk-copy kernel; FP64 takes the register march kernel, which measured
+// faster there (FP64 arithmetic, not memory, bounds the FP64 update).
+constexpr int kEmuSums3d = 2;
 
 namespace fvf {
 namespace {
@@ -77,17 +67,15 @@ template <int I>
 __device__ __forceinline__ float sum_rn(float a, float b) { return __fadd_rn(a, b); }
 template <int I>
 __device__ __forceinline__ double sum_rn(double a, double b) {
-    return I < FVF_3D_EMU_SUMS ? emu::add_same_sign(a, b) : __dadd_rn(a, b);
+    return I < kEmuSums3d ? emu::add_same_sign(a, b) : __dadd_rn(a, b);
 }
 
-// k * x with the factor k fixed for the sweep
+// k * x with the factor k fixed for the sweep (FP64: on the integer pipes)
 template <int BIT>
 __device__ __forceinline__ float mulk_rn(float k, float x) { return __fmul_rn(k, x); }
 template <int BIT>
 __device__ __forceinline__ double mulk_rn(double k, double x) {
-    if (FVF_3D_EMU_MUL & BIT)
-        return emu::from_bits(emu::mul_const_bits(emu::bits(x), emu::mul_const(k)));
-    return __dmul_rn(k, x);
+    return emu::from_bits(emu::mul_const_bits(emu::bits(x), emu::mul_const(k)));
 }
 
 template <typename T>
@@ -260,19 +248,11 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
 // Bulk-copy kernel
 // ---------------------------------------------------------------------------
 
-#ifndef FVF_3D_RING
-#define FVF_3D_RING 5
-#endif
-#ifndef FVF_3D_KZ
-#define FVF_3D_KZ 64
-#endif
 // Ring of 5 slots, 2 rows per warp and runs of 64 planes measured best at
 // 512^3 (0.216 ms per step, against 0.240 for 6 slots, 1 row, 32 planes).
-constexpr int kRing = FVF_3D_RING;           // slots: planes k-1, k, k+1 and kRing-3 ahead
-#ifndef FVF_3D_RPW
-#define FVF_3D_RPW 2
-#endif
-constexpr int kRPW = FVF_3D_RPW;             // rows per warp in the bulk kernel
+constexpr int kRing = 5;                     // slots: planes k-1, k, k+1 and kRing-3 ahead
+constexpr int kRPW = 2;                      // rows per warp in the bulk kernel
+constexpr int64_t kRunPlanes = 64;           // planes per work item of the bulk kernel
 constexpr int kBulkRows = kTY * kRPW;        // tile rows of a bulk block
 constexpr int kRows = kBulkRows + 2;         // tile rows plus one halo row each side
 
@@ -508,7 +488,7 @@ cudaError_t launch_bulk(const CUtensorMap &src_map, T *dst, int64_t nx, int64_t 
         per_sm_dev[d].store(n, std::memory_order_relaxed);
     }
     const int64_t tiles_x = (nx + TX - 1) / TX, tiles_y = (ny + kBulkRows - 1) / kBulkRows;
-    const int64_t kz_len = FVF_3D_KZ;  // planes per item
+    const int64_t kz_len = kRunPlanes;  // planes per item
     const int64_t runs = (nz + kz_len - 1) / kz_len;
     const int64_t items = tiles_x * tiles_y * runs;
     const int64_t maxgrid = (int64_t)per_sm * sm_count();
@@ -545,7 +525,7 @@ cudaError_t launch_steps(T *u, T *v, int64_t nx, int64_t ny, int64_t nz, T alpha
     const bool vec = nx % VW == 0 && (uintptr_t)u % 16 == 0 && (uintptr_t)v % 16 == 0;
     // tensor maps of both buffers (each is the source of every other step)
     CUtensorMap map_u, map_v;
-    const bool bulk = FVF_3D_BULK && sizeof(T) == 4 && vec &&
+    const bool bulk = sizeof(T) == 4 && vec &&
                       encode_field_map<T>(&map_u, u, nx, ny, nz) &&
                       encode_field_map<T>(&map_v, v, nx, ny, nz);
     for (int64_t s = 1; s <= nsteps; ++s) {

@@ -26,73 +26,34 @@
 // FP64 throughput.  The fused 3D update is 13 FP64 operations per element
 // against 48 bytes of HBM traffic, far above GB300's FP64-to-bandwidth
 // ratio.  Its six multiplications run on the integer pipes instead, as exact
-// binary64 products by factors prepared once (fp64_emu.cuh), leaving the
-// seven additions on the FP64 unit: FVF_RK_EMU_MUL selects them (1/2/4 the
-// x/y/z inverse spacings, 8 dt, 16 a, 32 b), and all six with one variable
-// per load batch (FVF_RK_CHUNK = 1) measured fastest on GB300, 36% below the
-// all-FP64 kernel (the update alone, FVF_RK_CHUNK_AXPBY = 1, measured
-// fastest with one variable per batch as well).  FVF_RK_EMU selects
-// additions that run as exact integer-pipe additions as well: bit 1 the y
-// term, 2 the z term, 4 u + dt*rhs, 8 the final sum, 16/32/64 the x/y/z face
-// differences.  An addition costs about twice the integer instructions of a
-// product, and every choice of them measured slower, so the default is 0.
+// binary64 products by factors prepared once (fp64_emu.cuh: the x/y/z
+// inverse spacings, dt, a and b), leaving the seven additions on the FP64
+// unit.  With one variable per load batch this measured fastest on GB300, 36%
+// below the all-FP64 kernel (the update alone measured fastest with one
+// variable per batch as well).  Additions on the integer pipes as well (the
+// y and z terms, u + dt*rhs, the final sum, the face differences, any
+// choice of them) measured slower: an exact addition costs about twice the
+// integer instructions of a product.
 #include "fp64_emu.cuh"
 #include "fvf_internal.cuh"
-
-#ifndef FVF_RK_EMU
-#define FVF_RK_EMU 0
-#endif
-#ifndef FVF_RK_EMU_Q
-#define FVF_RK_EMU_Q 0xFF
-#endif
-#ifndef FVF_RK_EMU_MUL
-#define FVF_RK_EMU_MUL 63
-#endif
-#ifndef FVF_RK_EMU_MUL_Q
-#define FVF_RK_EMU_MUL_Q 0xFF
-#endif
-#ifndef FVF_RK_CHUNK
-#define FVF_RK_CHUNK 1
-#endif
-#ifndef FVF_RK_CHUNK_AXPBY
-#define FVF_RK_CHUNK_AXPBY 1
-#endif
 
 namespace fvf {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kChunk = 1;   // variables per load batch
 
-// v is the variable's index: FVF_RK_EMU_Q selects, by v mod 8, the variables
-// whose additions are emulated (a warp-uniform choice: every lane of a warp
-// works on the same variable).
-template <int BIT>
-__device__ __forceinline__ double add_rn(double x, double y, int v) {
-    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> (v & 7)) & 1)) return emu::add(x, y);
-    return __dadd_rn(x, y);
-}
+__device__ __forceinline__ double add_rn(double x, double y) { return __dadd_rn(x, y); }
+__device__ __forceinline__ double sub_rn(double x, double y) { return __dsub_rn(x, y); }
 
-template <int BIT>
-__device__ __forceinline__ double sub_rn(double x, double y, int v) {
-    if ((FVF_RK_EMU & BIT) && ((FVF_RK_EMU_Q >> (v & 7)) & 1))
-        return emu::add(x, emu::from_bits(emu::bits(y) ^ emu::kSign));
-    return __dsub_rn(x, y);
-}
-
-// w * x on the FP64 unit, or on the integer pipes with the factor w prepared
-// in m (fp64_emu.cuh) when BIT is set in FVF_RK_EMU_MUL (1/2/4 the x/y/z
-// inverse spacings, 8 dt, 16 a, 32 b) and bit v mod 8 in FVF_RK_EMU_MUL_Q.
-template <int BIT>
-__device__ __forceinline__ double mul_rn(double w, const emu::MulConst &m, double x, int v) {
-    if ((FVF_RK_EMU_MUL & BIT) && ((FVF_RK_EMU_MUL_Q >> (v & 7)) & 1))
-        return emu::from_bits(emu::mul_const_bits(emu::bits(x), m));
-    return __dmul_rn(w, x);
+// w * x on the integer pipes, the factor w prepared in m (fp64_emu.cuh)
+__device__ __forceinline__ double mul_rn(const emu::MulConst &m, double x) {
+    return emu::from_bits(emu::mul_const_bits(emu::bits(x), m));
 }
 
 template <bool FUSED, bool FY, bool FZ, typename Idx>
 __global__ void __launch_bounds__(kThreads)
 rk_stage_kernel(RkStageArgs A) {
-    constexpr int kChunk = FUSED ? FVF_RK_CHUNK : FVF_RK_CHUNK_AXPBY;
     const Idx n1 = (Idx)A.n[0], n2 = (Idx)A.n[1];
     const Idx plane_jk = n1 * n2;
     const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
@@ -152,20 +113,16 @@ rk_stage_kernel(RkStageArgs A) {
                     const int v = i0 + q;
                     double rr;
                     if (FUSED) {
-                        rr = mul_rn<1>(wx, mx, sub_rn<16>(xl[q], xh[q], v), v);
-                        if (FY)
-                            rr = add_rn<1>(
-                                rr, mul_rn<2>(wy, my, sub_rn<32>(yl[q], yh[q], v), v), v);
-                        if (FZ)
-                            rr = add_rn<2>(
-                                rr, mul_rn<4>(wz, mz, sub_rn<64>(zl[q], zh[q], v), v), v);
+                        rr = mul_rn(mx, sub_rn(xl[q], xh[q]));
+                        if (FY) rr = add_rn(rr, mul_rn(my, sub_rn(yl[q], yh[q])));
+                        if (FZ) rr = add_rn(rr, mul_rn(mz, sub_rn(zl[q], zh[q])));
                     } else {
                         rr = r[q];
                     }
-                    const double t = add_rn<4>(uv[q], mul_rn<8>(A.dt, mdt, rr, v), v);
+                    const double t = add_rn(uv[q], mul_rn(mdt, rr));
                     if (FVF_IN(c + (int64_t)v * cplane, call))
-                        A.out[c + (int64_t)v * cplane] = add_rn<8>(
-                            mul_rn<16>(A.a, ma, u0v[q], v), mul_rn<32>(A.b, mb, t, v), v);
+                        A.out[c + (int64_t)v * cplane] =
+                            add_rn(mul_rn(ma, u0v[q]), mul_rn(mb, t));
                 }
             }
         }

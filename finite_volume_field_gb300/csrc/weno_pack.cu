@@ -21,16 +21,18 @@ namespace fvf {
 namespace {
 
 constexpr int kTile = 32;
-// threads along the second tile axis of the transposing kernel (each thread
+// Threads along the second tile axis of the transposing kernel (each thread
 // then moves kTile / rows elements of a variable's tile).  4 rows (8 elements
 // per thread, 128-thread blocks) measured 3-5% faster on GB300 than 8 rows,
 // and 16 rows 12-25% slower; 2 rows equal in FP32, slower in FP64.
-#ifndef FVF_PACK_ROWS_F64
-#define FVF_PACK_ROWS_F64 4
-#endif
-#ifndef FVF_PACK_ROWS_F32
-#define FVF_PACK_ROWS_F32 4
-#endif
+constexpr int kPackRows = 4;
+// Minimum resident blocks per SM of the transposing kernel: FP32 at 12 (a
+// 40-register cap, 12 blocks of 128 threads) keeps enough 4-byte loads in
+// flight per SM for HBM (8 x 207^3, y: 0.113 -> 0.107 ms, z: 0.123 -> 0.115 ms
+// on GB300); FP64 moves twice the bytes per thread and measured slower with
+// the cap (spills), so it takes none.
+template <typename T>
+constexpr int pack_min_blocks() { return sizeof(T) == 4 ? 12 : 0; }
 
 // x: out(a, b, c, i) = f_i(a, b+g2, c+g3); (M1, M2, M3) = (N1, n2, n3).
 // T is double or float: the pack is a copy of 8- or 4-byte elements.  The
@@ -95,7 +97,7 @@ struct TransposeGeom {
 };
 
 template <typename T, bool COPY, typename Idx, int R>
-__global__ void __launch_bounds__(kTile * R)
+__global__ void __launch_bounds__(kTile * R, pack_min_blocks<T>())
 pack_transpose_kernel(FieldTable t, CopyTable cp, int nv, TransposeGeom G,
                       T *__restrict__ out) {
     // geometry in the index type of this instantiation: 32-bit when every
@@ -323,7 +325,7 @@ static cudaError_t launch_transpose(const FieldTable &fields, const CopyTable &c
     const int64_t lim = (int64_t)1 << 31;
     const bool narrow = G.stored + 32 * G.sa + G.sq + 64 < lim &&
                         G.plane * nv + 40 * G.da + G.dq + 64 < lim && blocks < lim;
-    constexpr int R = sizeof(T) == 4 ? FVF_PACK_ROWS_F32 : FVF_PACK_ROWS_F64;
+    constexpr int R = kPackRows;
     if (narrow)
         pack_transpose_kernel<T, COPY, int32_t, R><<<(unsigned)blocks, dim3(kTile, R), 0,
                                                      stream>>>(fields, copies, nv, G, out);
