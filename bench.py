@@ -704,6 +704,23 @@ def time_extra_sweeps(torch, sw, stream, reps=5):
                                                    "single_step_ms": round(t_one, 3),
                                                    "speedup": round(t_one / t_blk, 3)}
     del whole_u, whole_v
+    # FP64 diffusion of a field with mixed signs: the 8192^2 grid with
+    # interior N(0,1) values, 20 steps per call, beside the same 20 steps of
+    # the uniform [0,1) field the step times (the integer-pipe additions take
+    # their general form on rows where signs differ)
+    nrm = torch.from_numpy(inputs.diffusion_field(DIFF_N, DIFF_N, np.float64,
+                                                  seed=inputs.config_seed(2), stream=2,
+                                                  values="normal")).to(sw.dev)
+    nrm_v = torch.zeros_like(nrm)
+    uni = sw.u64.clone()
+    cells2 = (DIFF_N - 2) ** 2
+    for name, fld in (("diffuse_fp64_normal_20steps", nrm), ("diffuse_fp64_uniform_20steps", uni)):
+        record(name, lambda fld=fld: api.diffuse2d_step(fld, nrm_v, DIFF_N, DIFF_N, 0.1, 20,
+                                                         api.FVF_FP64, stream),
+               20 * 2 * DIFF_N * DIFF_N * 8, 20 * cells2, FP64_FLOPS["diffuse_fp64"])
+    out["diffuse_fp64_normal_20steps"]["vs_uniform"] = round(
+        out["diffuse_fp64_normal_20steps"]["ms"] / out["diffuse_fp64_uniform_20steps"]["ms"], 4)
+    del nrm, nrm_v, uni
     # the 64 x 64 FP64 centre-impulse case, 32 steps: a latency measurement
     # (both states live in shared memory), reported per call and per step
     u = torch.zeros(64 * 64, dtype=torch.float64, device=sw.dev)

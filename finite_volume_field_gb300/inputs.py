@@ -111,12 +111,15 @@ def stored_extents(extents, ghost):
     return tuple(int(n) + 2 * int(ghost) if int(n) > 1 else 1 for n in extents)
 
 
-def diffusion_field(nx: int, ny: int, dtype, seed: int | None = None, stream: int = 0):
+def diffusion_field(nx: int, ny: int, dtype, seed: int | None = None, stream: int = 0,
+                    values: str = "uniform"):
     """Initial 2D field of shape (ny, nx) (element [j, i] is u(i, j)).
 
     With ``seed`` None: the centre impulse (all zero except the 1-based cell
-    ((nx+1)/2, (ny+1)/2) = 1).  Otherwise: interior uniform [0, 1) drawn in
-    the requested precision, edges zero.
+    ((nx+1)/2, (ny+1)/2) = 1).  Otherwise: interior values drawn from the
+    seed, edges zero: uniform [0, 1) in the requested precision, or with
+    ``values="normal"`` N(0,1) (FP64 draws, rounded to the precision), a
+    field of mixed signs.
     """
     dt = np.dtype(dtype)
     u = np.zeros((ny, nx), dtype=dt)
@@ -124,7 +127,12 @@ def diffusion_field(nx: int, ny: int, dtype, seed: int | None = None, stream: in
         u[(ny + 1) // 2 - 1, (nx + 1) // 2 - 1] = 1
         return u
     n = (nx - 2) * (ny - 2)
-    vals = uniform_f32(seed, stream, n) if dt == np.float32 else uniform_f64(seed, stream, n)
+    if values == "normal":
+        vals = normal_f64(seed, stream, n).astype(dt)
+    elif values == "uniform":
+        vals = uniform_f32(seed, stream, n) if dt == np.float32 else uniform_f64(seed, stream, n)
+    else:
+        raise ValueError(f"values must be 'uniform' or 'normal', not {values!r}")
     u[1:-1, 1:-1] = vals.reshape(ny - 2, nx - 2)
     return u
 

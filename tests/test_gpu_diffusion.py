@@ -178,6 +178,44 @@ def test_full_size_8192_200_steps(dt):
     assert oracle.physical_check(got)["min"] >= 0
 
 
+@pytest.mark.parametrize("nx,ny", [(512, 256), (1130, 65), (258, 300), (4000, 11)])
+def test_mixed_sign_fields(nx, ny):
+    """FP64 fields of mixed signs on grids the row-marching kernel takes
+    (above 32K cells, rows 16-byte aligned): N(0,1) values in the upper rows,
+    their magnitudes in the lower rows (rows of a warp then take either form
+    of the integer-pipe additions), a block of zeros and a band of negative
+    magnitudes; several step counts, both buffers bit-exact."""
+    torch = torch_cuda()
+    n = nx * ny
+    u0 = inputs.normal_f64(21, nx + ny, n).reshape(ny, nx)
+    u0[ny // 2:, :] = np.abs(u0[ny // 2:, :])
+    u0[ny // 4: ny // 4 + 9, nx // 3: nx // 3 + 40] = 0.0
+    u0[3 * ny // 4: 3 * ny // 4 + 3, :] *= -1.0
+    for steps in (1, 2, 5):
+        gu, gv = _run_gpu(torch, u0, steps)
+        ou, ov, _ = oracle.diffuse2d(u0, steps, return_both=True)
+        assert_bits_equal(gu, ou, what=f"u {nx}x{ny} {steps}")
+        assert_bits_equal(gv, ov, what=f"v {nx}x{ny} {steps}")
+
+
+def test_full_size_normal_field():
+    """The 8192 x 8192 FP64 grid with interior N(0,1) values (mixed signs),
+    20 steps, in the launch configuration the benchmark times, cell by cell
+    against the multithreaded oracle."""
+    torch = torch_cuda()
+    nx = ny = 8192
+    u0 = inputs.diffusion_field(nx, ny, np.float64, seed=inputs.config_seed(2), stream=2,
+                                values="normal")
+    u = to_dev(u0)
+    v = torch.zeros_like(u)
+    api.diffuse2d_step(u, v, nx, ny, 0.1, 20, api.FVF_FP64)
+    torch.cuda.synchronize()
+    got = to_host(u)
+    del u, v
+    want = oracle.diffuse2d(u0, 20, nthreads=oracle.max_threads())
+    assert_bits_equal(got, want, what="8192^2 N(0,1) FP64")
+
+
 @pytest.mark.parametrize("dt", [np.float32, np.float64])
 @pytest.mark.parametrize("nx,ny", [(300, 250), (1130, 65), (224, 160), (4000, 11), (9, 6000),
                                    (113, 65), (224, 128), (1000, 7), (9, 600)])
