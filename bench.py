@@ -1061,9 +1061,10 @@ def run_ncu_case():
     8 x 201^3, the SSPRK3 stage fused with the x/y/z flux difference on
     8 x 201^3 (about 3.1 GB), one 3D 7-point diffusion step on 512^3 in FP32
     then FP64 (at most 2.1 GB), and the 64 x 64 FP64 centre impulse for 32
-    steps (one cluster launch).  FP64 runs 2 single steps, FP32 17 steps (two
-    8-step shared-memory launches, then one single step).  Device-generated values (the
-    kernels' timing does not depend on them)."""
+    steps (one cluster launch); then the FP32 pack y/z and the FP32 flux
+    difference x.  FP64 runs 2 single steps, FP32 17 steps (two 8-step
+    shared-memory launches, then one single step).  Device-generated values
+    (the kernels' timing does not depend on them)."""
     import torch
     from finite_volume_field_gb300 import api, buildlib
     if not api.LIB_PATH.exists():
@@ -1118,6 +1119,23 @@ def run_ncu_case():
         api.diffuse3d_step(u, v, 512, 512, 512, 0.1, 1, code)
         del u, v
         free()
+    # FP32 pack y/z on 8 fields of 207^3 and the FP32 flux difference x on
+    # 8 x 201^3 (at most about 0.55 GB)
+    fields = [torch.randn(N, dtype=torch.float32, device="cuda") for _ in range(PACK_NV)]
+    out = torch.empty(_prod(pack_extents(PACK_EXT, PACK_G, 0)) * PACK_NV, dtype=torch.float32,
+                      device="cuda")
+    for d in (1, 2):
+        api.weno_pack_f32(fields, PACK_NV, PACK_EXT, PACK_G, d, out)
+    del fields, out
+    free()
+    fe = list(RHS_EXT)
+    fe[0] += 1
+    F = torch.randn(_prod(fe) * RHS_NV, dtype=torch.float32, device="cuda")
+    w = torch.rand(RHS_EXT[0], dtype=torch.float32, device="cuda") + 0.5
+    r = torch.empty(_prod(RHS_EXT) * RHS_NV, dtype=torch.float32, device="cuda")
+    api.advect_rhs_f32(F, w, RHS_NV, RHS_EXT, 0, r)
+    del F, w, r
+    free()
     # the small-grid case: 64 x 64 FP64 centre impulse, 32 steps, one cluster launch
     u = torch.zeros(64 * 64, dtype=torch.float64, device="cuda")
     u[31 * 64 + 31] = 1.0
