@@ -1184,6 +1184,92 @@ def run_ncu_ablation():
     return 0
 
 
+def run_slab(args):
+    """The diffusion rows of the step (8192^2, 200 steps, FP64 then FP32) on
+    a grid split into j-slabs (finite_volume_field_gb300/slab.py): one slab
+    per rank under torchrun, halos exchanged with torch.distributed point to
+    point (NCCL); with one process, ``--slab P`` slabs on the one device,
+    halos copied between them.  FP64 takes 4-row halos (an exchange every 4
+    steps), FP32 8-row halos (one exchange per 8-step blocked launch).  The
+    whole grid is the work for any number of ranks: strong scaling."""
+    import torch
+    from finite_volume_field_gb300 import api, buildlib, slab
+    world, rank, local = dist_env()
+    if not api.LIB_PATH.exists():
+        buildlib.build()
+    api.load()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    parts = world if world > 1 else max(1, args.slab)
+    host = host_inputs()
+    stream = torch.cuda.Stream(device)
+    runs = []
+    for key, code, halo in (("u64", api.FVF_FP64, 4), ("u32", api.FVF_FP32, 8)):
+        u0 = host[key]
+        mine = [rank] if world > 1 else list(range(parts))
+        slabs = []
+        for p in mine:
+            rows = slab.slab_rows(DIFF_N, parts, p, halo)
+            u = torch.from_numpy(u0[rows.l0:rows.l1].reshape(-1).copy()).to(device)
+            slabs.append(slab.SlabDiffusion2D(u, torch.zeros_like(u), DIFF_N, DIFF_N, rows, halo,
+                                              0.1, code, stream=stream))
+        if world > 1:
+            ex = slab.dist_exchanger(dist, rank, world, sync=stream.synchronize)
+            advance = lambda n, s=slabs[0], ex=ex: s.advance(n, ex)  # noqa: E731
+        else:
+            lx = slab.LocalExchange(slabs)
+            advance = lx.advance
+        runs.append((key, advance))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(device)
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            for _, advance in runs:
+                advance(DIFF_STEPS)
+    for _ in range(max(1, args.warmup)):
+        one_step()
+    barrier()
+    t0 = time.perf_counter()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        one_step()
+    end.record(stream)
+    barrier()
+    ms = start.elapsed_time(end) / args.steps
+    wall_ms = 1e3 * (time.perf_counter() - t0) / args.steps
+    if dist is not None:
+        both = [None] * world
+        dist.all_gather_object(both, (ms, wall_ms))
+        ms = max(b[0] for b in both)
+        wall_ms = max(b[1] for b in both)
+    if rank == 0:
+        step_bytes = DIFF_STEPS * 2 * DIFF_N * DIFF_N * (8 + 4)
+        line = {"impl": "gb300", "metric": METRIC, "value": round(step_bytes / (ms * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms, 4), "wall_ms_per_step": round(wall_ms, 4),
+                "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+                "dtype": "f32+f64", "data": "synthetic",
+                "config": {"workload": "2D 5-point diffusion 8192x8192, alpha 0.1, 200 steps, "
+                                       "FP64 then FP32, in j-slabs with halo exchange",
+                           "slabs": parts, "halo_rows": {"fp64": 4, "fp32": 8},
+                           "exchange": "torch.distributed point to point" if world > 1
+                                       else "device copies between slabs on one GPU"}}
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1198,7 +1284,12 @@ def main(argv=None):
                     help="run the collapse-3 / collapse-4 kernel pairs once each (for ncu)")
     ap.add_argument("--ncu-case", action="store_true",
                     help="launch each sweep kernel once at benchmark size (for ncu), no timing")
+    ap.add_argument("--slab", type=int, default=0,
+                    help="the diffusion rows only, decomposed into j-slabs: one per rank under "
+                         "torchrun, or this many on the one GPU (strong scaling)")
     args = ap.parse_args(argv)
+    if args.slab and args.impl == "gb300":
+        return run_slab(args)
     if args.ncu_case:
         return run_ncu_case()
     if args.ncu_ablation:

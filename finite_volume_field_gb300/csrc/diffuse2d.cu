@@ -314,12 +314,10 @@ int march_blocks_per_sm() {
     const int d = device_slot();
     int n = cached[d].load(std::memory_order_relaxed);
     if (n == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, diffuse_march_kernel<T>,
-                                                          kMarchThreads, 0) != cudaSuccess ||
-            n <= 0) {
-            cudaGetLastError();
-            n = 8;
-        }
+        const cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, diffuse_march_kernel<T>, kMarchThreads, 0);
+        if (st != cudaSuccess) cudaGetLastError();   // this query's own error only
+        if (st != cudaSuccess || n <= 0) n = 8;
         cached[d].store(n, std::memory_order_relaxed);
     }
     return n;
@@ -520,8 +518,10 @@ constexpr int64_t kClusterMaxCells = 32 * 1024;
 // than divided out per cell and step.  HW: the FP64 update entirely on the
 // FP64 unit, for bands of at most kClusterHwCells cells, where a step is
 // bound by the latency of one cell's update rather than by throughput (the
-// integer-pipe additions lengthen that chain): 64^2 x 32 steps measured 43
-// against 48 us on GB300, 128^2 x 100 steps 246 against 238 us.
+// integer-pipe additions lengthen that chain).  In one A/B on GB300 (the
+// same box, call by call): 64^2 x 32 steps 43 us with this form against
+// 48 us with the split, and 128^2 x 100 steps 246 against 238 us (the split
+// wins there).
 constexpr int kClusterHwCells = 512;
 
 template <typename T, int CS, bool HW>
@@ -597,25 +597,33 @@ int cluster_prepare() {
     const int d = device_slot();
     const int known = width1[d].load(std::memory_order_relaxed);
     if (known) return known - 1;
+    // An attribute or occupancy query that fails leaves its error as the
+    // thread's last error; it is cleared here (so that the launch checks that
+    // follow do not report it) only when one of these calls failed.
+    bool failed = false;
+    auto ok = [&failed](cudaError_t e) {
+        if (e != cudaSuccess) failed = true;
+        return e == cudaSuccess;
+    };
     int w = 0;
-    if (cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kClusterMaxBytes) == cudaSuccess &&
-        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kClusterMaxBytes) == cudaSuccess)
+    if (ok(cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kClusterMaxBytes)) &&
+        ok(cudaFuncSetAttribute(diffuse_cluster_kernel<T, 8, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kClusterMaxBytes)))
         w = 8;
     if (w &&
-        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kClusterMaxBytes) == cudaSuccess &&
-        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kClusterMaxBytes) == cudaSuccess &&
-        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, false>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, true>,
-                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        ok(cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, false>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kClusterMaxBytes)) &&
+        ok(cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kClusterMaxBytes)) &&
+        ok(cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, false>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) &&
+        ok(cudaFuncSetAttribute(diffuse_cluster_kernel<T, 16, true>,
+                                cudaFuncAttributeNonPortableClusterSizeAllowed, 1))) {
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -627,13 +635,15 @@ int cluster_prepare() {
         cfg.dynamicSmemBytes = (size_t)kClusterMaxBytes;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, diffuse_cluster_kernel<T, 16, false>, &cfg) ==
-                cudaSuccess &&
-            clusters > 0)
+        // both instantiations a 16-block launch may take (all-FP64 update for
+        // bands of up to kClusterHwCells cells, the split one above that)
+        int c0 = 0, c1 = 0;
+        if (ok(cudaOccupancyMaxActiveClusters(&c0, diffuse_cluster_kernel<T, 16, false>, &cfg)) &&
+            ok(cudaOccupancyMaxActiveClusters(&c1, diffuse_cluster_kernel<T, 16, true>, &cfg)) &&
+            c0 > 0 && c1 > 0)
             w = 16;
     }
-    cudaGetLastError();
+    if (failed) cudaGetLastError();
     width1[d].store(w + 1, std::memory_order_relaxed);
     return w;
 }

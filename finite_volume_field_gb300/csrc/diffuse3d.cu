@@ -256,7 +256,7 @@ constexpr int64_t kRunPlanes = 64;           // planes per work item of the bulk
 constexpr int kBulkRows = kTY * kRPW;        // tile rows of a bulk block
 constexpr int kRows = kBulkRows + 2;         // tile rows plus one halo row each side
 
-__device__ int g_device_error;               // nonzero: a bounded wait expired
+__device__ int g_device_error;   // bit 1: a bounded wait expired; bit 2: a drain wait too
 
 using mbar::smem_addr;
 
@@ -358,11 +358,15 @@ diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict
             if (k + 1 <= pl1) ok = mbar::wait(smem_addr(&bars[st]), pt) && ok;
             if (__syncthreads_or(!ok)) {
                 // a copy did not land in time: record it, let the copies in
-                // flight finish (bounded) and leave
+                // flight finish (bounded) and leave.  If a drain wait expires
+                // too, bit 2 records that the block may have exited with a
+                // copy into its shared memory still pending.  (Not exercised
+                // by a test: making a tensor copy fail to land would need a
+                // fault of the copy engine.)
                 if (producer) {
-                    atomicExch(&g_device_error, 1);
+                    atomicOr(&g_device_error, 1);
                     for (int64_t p = k > pl0 ? k - 1 : pl0; p <= issued; ++p)
-                        (void)wait_t(tbase + (uint32_t)(p - pl0));
+                        if (!wait_t(tbase + (uint32_t)(p - pl0))) atomicOr(&g_device_error, 2);
                 }
                 return;
             }
@@ -478,12 +482,10 @@ cudaError_t launch_bulk(const CUtensorMap &src_map, T *dst, int64_t nx, int64_t 
                                  (int)smem) != cudaSuccess)
             return cudaGetLastError();
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, diffuse3d_bulk_kernel<T>,
-                                                          32 * kTY, smem) != cudaSuccess ||
-            n < 1) {
-            cudaGetLastError();
-            n = 1;
-        }
+        const cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, diffuse3d_bulk_kernel<T>, 32 * kTY, smem);
+        if (st != cudaSuccess) cudaGetLastError();   // this query's own error only
+        if (st != cudaSuccess || n < 1) n = 1;
         per_sm = n;
         per_sm_dev[d].store(n, std::memory_order_relaxed);
     }

@@ -561,7 +561,7 @@ FVF_API int fvf_device_error(int *flag) {
         bounds |= b;
     }
     if (e != cudaSuccess) return cuda_status(e);
-    *flag = (waits ? 1 : 0) | (bounds ? 2 : 0);
+    *flag = ((waits & 1) ? 1 : 0) | (bounds ? 2 : 0) | ((waits & 2) ? 4 : 0);
     return FVF_OK;
 }
 

@@ -312,7 +312,10 @@ int fvf_last_cuda_error(void);
  *      finish (also bounded) and returned without completing its work: the
  *      results of that launch are invalid;
  *   2  (index-checking debug builds only, libfvf_check.so) a kernel met a
- *      global index outside its array and skipped that access.
+ *      global index outside its array and skipped that access;
+ *   4  (with 1) one of the waits for the copies still in flight expired as
+ *      well: a block may have returned while a copy into its shared memory
+ *      was pending.
  * Synchronises the device.  Returns FVF_OK, FVF_ERR_NULL or FVF_ERR_CUDA.
  */
 int fvf_device_error(int *flag);

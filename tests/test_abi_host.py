@@ -262,3 +262,35 @@ def test_fp32_pack_and_flux_validation(lib):
         assert f(4096, 8192, 0, ext, 0, None, None) == C["FVF_OK"]
         assert f(4098, 8192, 2, ext, 0, 65536, None) == C["FVF_ERR_ALIGN"]
         assert f(4100, 8196, 2, ext, 0, 65540, None) == C["FVF_ERR_NOT_DEVICE"]
+
+
+def test_degenerate_sizes_are_valid_calls(lib):
+    """The boundary accepts, as valid calls, sizes a narrower contract could
+    reject: empty grids, nv = 0 and zero extents return FVF_OK without
+    touching memory (NULL pointers are fine then, and nothing is launched);
+    grids with no interior (nx or ny <= 2) and a swept axis of extent 1 are
+    ordinary calls, which proceed to the pointer checks (FVF_ERR_NULL here,
+    not FVF_ERR_SIZE).  Their results are pinned on the GPU
+    (test_gpu_degenerate.py)."""
+    before = lib.fvf_launch_count()
+    d2, d3 = lib.diffuse2d_step, lib.diffuse3d_step
+    for dt in (0, 1):
+        assert d2(None, None, 0, 9, 0.1, 3, dt, None) == C["FVF_OK"]
+        assert d2(None, None, 9, 0, 0.1, 3, dt, None) == C["FVF_OK"]
+        assert d3(None, None, 9, 0, 9, 0.1, 3, dt, None) == C["FVF_OK"]
+        for nx, ny in ((1, 1), (2, 2), (2, 9), (9, 1)):
+            assert d2(None, None, nx, ny, 0.1, 1, dt, None) == C["FVF_ERR_NULL"]
+    ext0 = E3(0, 5, 5)
+    ext1 = E3(5, 5, 1)
+    tab = (ctypes.c_void_p * 1)(None)
+    assert lib.weno_pack(tab, 0, E3(5, 5, 5), 2, 0, None, None) == C["FVF_OK"]
+    assert lib.weno_pack(tab, 1, ext0, 2, 0, None, None) == C["FVF_OK"]
+    assert lib.weno_pack(tab, 1, ext1, 2, 2, None, None) == C["FVF_ERR_NULL"]
+    for name in ("advect_rhs", "advect_rhs_add"):
+        f = getattr(lib, name)
+        assert f(None, None, 0, E3(5, 5, 5), 0, None, None) == C["FVF_OK"]
+        assert f(None, None, 2, ext0, 1, None, None) == C["FVF_OK"]
+        assert f(None, None, 2, ext1, 2, None, None) == C["FVF_ERR_NULL"]
+    assert lib.flux_unpack(None, 0, E3(5, 5, 5), 1, None, None) == C["FVF_OK"]
+    assert lib.fields_copy(tab, 0, E3(5, 5, 5), 1, tab, None) == C["FVF_OK"]
+    assert lib.fvf_launch_count() == before
