@@ -22,9 +22,9 @@
 //          read from HBM once per step (plus one row per strip boundary).
 //          The W/E neighbours across vectors come from the adjacent lanes by
 //          warp shuffle; the two warp-edge lanes load their outside
-//          neighbour together with the row.  The grid is one wave: as many
-//          blocks as fit on the SMs at once, each taking an equal band of
-//          rows.
+//          neighbour together with the row.  FP32: the grid is one wave, as
+//          many blocks as fit on the SMs at once, each taking an equal band
+//          of rows; FP64: bands of 12 rows (many waves, see kMarchF64Rows).
 //   scalar (any size or alignment): one thread per cell.
 //   blocked (FP32, nsteps >= 3): up to 8 steps per launch in shared memory.
 //   cluster (grids of up to 32K cells, nsteps >= 2): all steps in one
@@ -95,9 +95,12 @@ __device__ __forceinline__ T update(T c, T w, T e, T s, T n, T alpha) {
 // FP64 update with the first two neighbour sums (W + E, then + S) on the
 // integer pipes (fp64_emu.cuh) and the rest on the FP64 unit: the same
 // operations in the same order, each correctly rounded, so the same bits.
-// This split balances the two kinds of pipe on GB300 (8192^2 step: 0.557 ms,
-// against 0.652 ms with all three sums emulated, 0.664 ms with one, 0.787 ms
-// with none; moving alpha * t or the last addition too measured slower).
+// This split balances the two kinds of pipe on GB300 (8192^2 step with the
+// march kernel: 0.557 ms, against 0.652 ms with all three sums emulated one
+// by one, 0.664 ms with one, 0.787 ms with none; moving alpha * t or the last
+// addition too measured slower).  The march kernel now takes the frame form
+// below for its same-sign rows; this one serves the kernels whose lanes may
+// diverge around the update (scalar, cluster).
 template <>
 __device__ __forceinline__ double update<double>(double c, double w, double e, double s,
                                                  double n, double alpha) {
@@ -105,6 +108,41 @@ __device__ __forceinline__ double update<double>(double c, double w, double e, d
     sum = emu::add_same_sign(sum, s);
     sum = __dadd_rn(sum, n);
     return __dadd_rn(c, __dmul_rn(alpha, Rn<double>::sub4(sum, c)));
+}
+
+// The same update with the whole neighbour sum ((W + E) + S) + N taken in
+// one 64-bit fixed-point frame on the integer pipes
+// (emu::sum4_one_sign_fast: one alignment and one packing for the three
+// additions, each still rounded as binary64 rounds it, the operands
+// accumulated with integer multiply-adds) and s - 4c, alpha * t and c + ...
+// on the FP64 unit.  The caller guarantees that W, E, S and N have one sign.
+// Lanes whose operands the frame declines (a spread of more than 9 binades,
+// zeros, subnormals, values at or above 2^1021) take the three additions on
+// the FP64 unit in an out-of-line function on bit patterns: a call is not
+// if-converted, so lanes that succeed issue no FP64 instruction for the sum
+// (written inline, the compiler evaluated the fallback's three additions for
+// every cell, 0.78 ms per 8192^2 step).  Measured on GB300 per 8192^2 step,
+// with the 12-row bands of the march grid: 0.413 ms, against 0.524 ms with
+// update<double> on the same grid.
+static __device__ __noinline__ uint64_t sum4_fp64_unit(uint64_t w, uint64_t e, uint64_t s,
+                                                       uint64_t n) {
+    return emu::bits(__dadd_rn(__dadd_rn(__dadd_rn(emu::from_bits(w), emu::from_bits(e)),
+                                         emu::from_bits(s)),
+                               emu::from_bits(n)));
+}
+
+template <typename T>
+__device__ __forceinline__ T update_frame(T c, T w, T e, T s, T n, T alpha) {
+    return update<T>(c, w, e, s, n, alpha);
+}
+
+template <>
+__device__ __forceinline__ double update_frame<double>(double c, double w, double e, double s,
+                                                       double n, double alpha) {
+    uint64_t sum;
+    if (!emu::sum4_one_sign_fast(emu::bits(w), emu::bits(e), emu::bits(s), emu::bits(n), &sum))
+        sum = sum4_fp64_unit(emu::bits(w), emu::bits(e), emu::bits(s), emu::bits(n));
+    return __dadd_rn(c, __dmul_rn(alpha, Rn<double>::sub4(emu::from_bits(sum), c)));
 }
 
 // The same update for rows where some lane's operands differ in sign.  The
@@ -139,13 +177,13 @@ __device__ __forceinline__ double update_any_sign<double>(double c, double w, do
     return __dadd_rn(c, __dmul_rn(alpha, Rn<double>::sub4(sum, c)));
 }
 
-// Whether the operands of the integer-pipe additions, W + E and then + S,
-// have one sign (FP64; FP32 has no such additions).
+// Whether the four neighbours have one sign, the precondition of the
+// fixed-point sum (FP64; FP32 has no integer-pipe additions).
 template <typename T>
-__device__ __forceinline__ bool same_sign3(T w, T e, T s) {
+__device__ __forceinline__ bool same_sign4(T w, T e, T s, T n) {
     if constexpr (sizeof(T) == 8) {
         const int hw = __double2hiint(w);
-        return ((hw ^ __double2hiint(e)) | (hw ^ __double2hiint(s))) >= 0;
+        return ((hw ^ __double2hiint(e)) | (hw ^ __double2hiint(s)) | (hw ^ __double2hiint(n))) >= 0;
     } else {
         return true;
     }
@@ -244,12 +282,19 @@ __device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int
     return r;
 }
 
-// FP64: at least 12 blocks of 128 threads per SM (a 40-register cap, one
-// 8-byte spill): 2% faster per 8192^2 step on GB300 than the 48-register
-// default (10 blocks).
-constexpr int kMarchF64MinBlocks = 12;
+// FP64 rows per block.  The FP64 grid is many short bands rather than one
+// wave of long ones: warps whose lanes often take the FP64 fallback (the
+// columns next to the zero edges, every row) run slower than the rest, and
+// with one wave of long bands the SMs idled while those finished (warps
+// active 51% of the SM's capacity against 75% possible).  Short bands let
+// the block scheduler even the load out; the extra halo rows (2 per band)
+// come from L2 and the kernel is not bound by HBM.  Per 8192^2 step on
+// GB300: one wave 0.498 ms; bands of 32, 16, 12, 8 and 6 rows 0.424, 0.414,
+// 0.413, 0.415 and 0.419 ms (no register cap; a 40-register cap for 12
+// blocks per SM measured 0.416 ms at 12 rows).
+constexpr int kMarchF64Rows = 12;
 template <typename T>
-__global__ void __launch_bounds__(kMarchThreads, sizeof(T) == 8 ? kMarchF64MinBlocks : 0)
+__global__ void __launch_bounds__(kMarchThreads)
 diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                      int64_t rows_per_block, T alpha) {
     constexpr int V = Vec16<T>::n;
@@ -271,14 +316,14 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
         if (lane == 31) e_in = rc.e_out;
         Vec16<T> out;
         const bool edge_row = (j == 0) || (j == ny - 1);
-        // FP64: one vote per row picks the same-sign integer additions when
-        // every lane's operands allow them (every lane takes part: the loop
-        // over rows is uniform in the block)
+        // FP64: one vote per row picks the fixed-point neighbour sum when
+        // W, E, S and N have one sign in every lane (every lane takes part:
+        // the loop over rows is uniform in the block)
         bool same = true;
 #pragma unroll
         for (int k = 0; k < V; ++k)
-            same &= same_sign3<T>(k > 0 ? rc.c.v[k - 1] : w_in, k < V - 1 ? rc.c.v[k + 1] : e_in,
-                                  rs.c.v[k]);
+            same &= same_sign4<T>(k > 0 ? rc.c.v[k - 1] : w_in, k < V - 1 ? rc.c.v[k + 1] : e_in,
+                                  rs.c.v[k], rn.c.v[k]);
         if (sizeof(T) == 4 || __all_sync(0xffffffffu, same)) {
 #pragma unroll
             for (int k = 0; k < V; ++k) {
@@ -286,7 +331,7 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
                 const T e = k < V - 1 ? rc.c.v[k + 1] : e_in;
                 const int64_t i = col + k;
                 const bool edge = edge_row || i == 0 || i == nx - 1;
-                out.v[k] = edge ? T(0) : update<T>(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha);
+                out.v[k] = edge ? T(0) : update_frame<T>(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha);
             }
         } else {
 #pragma unroll
@@ -716,11 +761,20 @@ struct SingleStep {
                  nx >= 2 * V;
         if (vec_ok) {
             const int64_t bx = (nx / V + kMarchThreads - 1) / kMarchThreads;
-            const int64_t resident = (int64_t)march_blocks_per_sm<T>() * sm_count();
-            int64_t by = resident / bx;
-            if (by < 1) by = 1;
-            if (by > ny) by = ny;
-            rows = (ny + by - 1) / by;
+            int64_t by;
+            if (sizeof(T) == 8) {
+                // bands of kMarchF64Rows rows (more where the grid's y
+                // dimension would exceed its limit)
+                rows = kMarchF64Rows;
+                if ((ny + rows - 1) / rows > 65535) rows = (ny + 65534) / 65535;
+            } else {
+                // FP32: one wave of equal bands
+                const int64_t resident = (int64_t)march_blocks_per_sm<T>() * sm_count();
+                by = resident / bx;
+                if (by < 1) by = 1;
+                if (by > ny) by = ny;
+                rows = (ny + by - 1) / by;
+            }
             by = (ny + rows - 1) / rows;
             if (bx > 0x7fffffff || by > 65535) return cudaErrorInvalidValue;
             grid = dim3((unsigned)bx, (unsigned)by);

@@ -229,6 +229,92 @@ FVF_HD uint64_t add_same_sign_bits(uint64_t A, uint64_t B) {
 FVF_HD double add(double a, double b) { return from_bits(add_bits(bits(a), bits(b))); }
 
 // ---------------------------------------------------------------------------
+// ((a + b) + c) + d, each addition correctly rounded, for four normal
+// operands of one sign whose exponents span at most 9 binades.  The three
+// additions share one 64-bit fixed-point frame instead of aligning,
+// normalising and packing three times:
+//   * with E the largest biased exponent of the four, an operand of
+//     exponent e enters as its 53-bit significand times 2^s,
+//     s = 9 - (E - e) in [0, 9], so every operand bit is a frame bit and the
+//     frame's unit is 2^(E - 9 - 1075);
+//   * the operands are accumulated with integer multiply-adds by 2^s (the
+//     low word as a 32 x 32 -> 64-bit product added to the frame, the high
+//     word's 21 significand bits times 2^s added to the frame's high word),
+//     which issue on the FMA pipe instead of loading the ALU pipe with
+//     64-bit shifts and additions;
+//   * each partial sum is exact in the frame (operands < 2^62, the rounded
+//     partial sums stay below 2^64 - 2^11: the largest case rounds
+//     2^64 - 2560 to 2^64 - 2048, so no step carries out of the frame) and
+//     is then rounded to its 53 leading bits, ties to even, exactly as the
+//     binary64 addition rounds it; the leading one is at bit 61 or above,
+//     so the p = 11 - clz(high word) bits below those 53 number 1 to 11;
+//   * rounding adds 2^(p-1) - 1 + (the kept part's last bit) and clears the
+//     p low bits (round half to even: a remainder of exactly 2^(p-1) moves
+//     up only when the kept part is odd); the carry of a round-up stays in
+//     the frame;
+//   * the packed exponent is E + 2 - clz(high word of the sum): the leading
+//     one at bit 63 - z is worth 2^(63 - z + E - 1084).
+// The operands' sign bit rides along in the high words: with one sign it
+// cancels in the exponent differences and lands back in the sign of the
+// result, and the high words order the magnitudes.  PRECONDITION: the four
+// operands have one sign (zeros included: +0 with positive operands); the
+// caller checks it.  Returns false (and an unspecified value) for a zero or
+// subnormal operand, a largest exponent below 2^-1013 or at or above 2^1021
+// (so the sum cannot overflow), or a spread of more than 9 binades: with
+// E >= 10, every s in [0, 9] implies every operand is normal, and a wider
+// spread makes some s wrap below zero.
+
+// a * b + c, 32 x 32 -> 64 bits, as one integer multiply-add
+FVF_HD uint64_t mad_wide(uint32_t a, uint32_t b, uint64_t c) {
+#if defined(__CUDA_ARCH__)
+    uint64_t d;
+    asm("mad.wide.u32 %0, %1, %2, %3;" : "=l"(d) : "r"(a), "r"(b), "l"(c));
+    return d;
+#else
+    return (uint64_t)a * b + c;
+#endif
+}
+
+// frame + significand(hi, lo) * pw, pw = 2^s; the caller's bound keeps the
+// true sum below 2^64, so neither part carries out
+FVF_HD uint64_t frame_add(uint64_t frame, uint32_t hi, uint32_t lo, uint32_t pw) {
+    frame = mad_wide(lo, pw, frame);
+    const uint32_t sig_hi = (hi & 0xFFFFFu) | 0x100000u;
+    const uint32_t h = sig_hi * pw + (uint32_t)(frame >> 32);
+    return ((uint64_t)h << 32) | (uint32_t)frame;
+}
+
+FVF_HD uint64_t round53_frame(uint64_t S) {
+    const uint32_t p = 11u - (uint32_t)clz32((uint32_t)(S >> 32));  // 1..11
+    const uint32_t unit = 1u << p;
+    const uint32_t lsb = ((uint32_t)S >> p) & 1u;
+    // p <= 11, so the cleared bits lie in the low word: a 32-bit mask (a
+    // 64-bit one built from a variable shift cost about 9% of the 2D FP64
+    // step on GB300)
+    return (S + ((unit >> 1) - 1u + lsb)) & ~(uint64_t)(unit - 1u);
+}
+
+FVF_HD bool sum4_one_sign_fast(uint64_t A, uint64_t B, uint64_t C, uint64_t D, uint64_t *out) {
+    const uint32_t ah = (uint32_t)(A >> 32), bh = (uint32_t)(B >> 32);
+    const uint32_t ch = (uint32_t)(C >> 32), dh = (uint32_t)(D >> 32);
+    const uint32_t m1 = ah > bh ? ah : bh, m2 = ch > dh ? ch : dh, hmax = m1 > m2 ? m1 : m2;
+    const uint32_t top = hmax >> 20;                 // sign and largest exponent
+    const uint32_t sa = (ah >> 20) - top + 9u, sb = (bh >> 20) - top + 9u;
+    const uint32_t sc = (ch >> 20) - top + 9u, sd = (dh >> 20) - top + 9u;
+    const bool ok = (sa | sb | sc | sd) < 16u &&
+                    (hmax & 0x7FFFFFFFu) - 0x00A00000u < 0x7FC00000u - 0x00A00000u;
+    uint64_t s = frame_add(frame_add(0, ah, (uint32_t)A, 1u << (sa & 15u)), bh, (uint32_t)B,
+                           1u << (sb & 15u));
+    s = round53_frame(s);
+    s = round53_frame(frame_add(s, ch, (uint32_t)C, 1u << (sc & 15u)));
+    s = round53_frame(frame_add(s, dh, (uint32_t)D, 1u << (sd & 15u)));
+    const uint32_t z = (uint32_t)clz32((uint32_t)(s >> 32));
+    // the implicit one at bit 52 adds the last 1 to the exponent field
+    *out = ((uint64_t)(top + 1u - z) << 52) + (s >> (11u - z));
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
 // Multiplication.  The same textbook method (Muller et al., chapter 7): the
 // product of the two 53-bit significands, both placed at the top of a 64-bit
 // word, is a 128-bit value with its leading one in bit 127 or 126; a one-bit

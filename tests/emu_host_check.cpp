@@ -1,7 +1,9 @@
 // Host check of the integer-pipe binary64 addition and multiplication
 // (fp64_emu.cuh): every sum and product must be bit-identical to the host
-// CPU's IEEE 754 operation (round to nearest even).  Built with -O2
-// -ffp-contract=off; prints "mismatches N cases M".
+// CPU's IEEE 754 operation (round to nearest even), and so must the
+// fixed-point sum of four operands, ((a + b) + c) + d, wherever its fast
+// form accepts the operands.  Built with -O2 -ffp-contract=off; prints
+// "mismatches N cases M sum4_taken T".
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -56,6 +58,27 @@ static void check_mul(uint64_t A, uint64_t B) {
     report("mul const swapped", B, A, mul_const_bits(B, mul_const(a)), want);
     uint64_t fast;
     if (mul_const_fast_int(A, mul_const(b), &fast)) report("mul fast", A, B, fast, want);
+}
+
+static uint64_t sum4_taken = 0;
+
+// ((A + B) + C) + D: the fixed-point form where it accepts the operands
+// (operands of one sign: its precondition).
+static void check_sum4(uint64_t A, uint64_t B, uint64_t C, uint64_t D) {
+    uint64_t got;
+    if (((A ^ B) | (A ^ C) | (A ^ D)) & kSign) return;
+    if (!sum4_one_sign_fast(A, B, C, D, &got)) return;
+    ++sum4_taken;
+    ++cases;
+    const double want = native_add(native_add(native_add(from_bits(A), from_bits(B)), from_bits(C)),
+                                   from_bits(D));
+    if (got != bits(want)) {
+        if (mismatches < 10)
+            std::printf("sum4 %016llx %016llx %016llx %016llx: got %016llx want %016llx\n",
+                        (unsigned long long)A, (unsigned long long)B, (unsigned long long)C,
+                        (unsigned long long)D, (unsigned long long)got, (unsigned long long)bits(want));
+        ++mismatches;
+    }
 }
 
 static void check(uint64_t A, uint64_t B) {
@@ -187,7 +210,53 @@ int main(int argc, char **argv) {
         for (int j = 0; j < ns; ++j) check_mul(specials[i], specials[j]);
     for (long i = 0; i < n / 10; ++i)
         for (int j = 0; j < ns; ++j) check_mul(specials[j], next_u64());
-    std::printf("mismatches %llu cases %llu\n", (unsigned long long)mismatches,
-                (unsigned long long)cases);
+    // four-operand sums: one sign, exponents within 10 of a random centre
+    // (spreads of 9 and 10 binades, zeros and subnormals near the bottom,
+    // results near overflow at the top); significands with few bits (ties
+    // in every partial sum); all-ones significands at spreads 0..9 (the
+    // largest frame values); the diffusion's own values (uniform [0, 1),
+    // products of [0.25, 0.75) and their negatives)
+    for (long i = 0; i < n; ++i) {
+        const uint64_t sg = next_u64() & 1, e0 = 1 + next_u64() % 2046;
+        auto g = [&]() {
+            int64_t e = (int64_t)e0 + (int64_t)(next_u64() % 21) - 10;
+            e = e < 0 ? 0 : (e > 2047 ? 2047 : e);
+            return make(sg, (uint64_t)e, next_u64());
+        };
+        const uint64_t a = g(), b = g(), c = g(), d = g();
+        check_sum4(a, b, c, d);
+    }
+    for (long i = 0; i < n; ++i) {
+        const uint64_t sg = next_u64() & 1, e0 = 1 + next_u64() % 2046;
+        auto g = [&]() {
+            int64_t e = (int64_t)e0 + (int64_t)(next_u64() % 3) - 1;
+            e = e < 0 ? 0 : (e > 2047 ? 2047 : e);
+            const uint64_t f = (next_u64() & 1) ? next_u64() : next_u64() & ~((1ull << (next_u64() % 53)) - 1);
+            return make(sg, (uint64_t)e, f);
+        };
+        const uint64_t a = g(), b = g(), c = g(), d = g();
+        check_sum4(a, b, c, d);
+    }
+    for (long i = 0; i < n; ++i) {
+        const uint64_t sg = next_u64() & 1, e0 = 1 + next_u64() % 2040;
+        auto g = [&]() {
+            const uint64_t f = (next_u64() & 1) ? kFrac : (next_u64() & 0xFFF0000000000ull);
+            return make(sg, e0 + next_u64() % 10, f);
+        };
+        const uint64_t a = g(), b = g(), c = g(), d = g();
+        check_sum4(a, b, c, d);
+        const uint64_t top = make(sg, 2030 + next_u64() % 18, kFrac - next_u64() % 8);
+        check_sum4(top, top, top, top);
+    }
+    for (long i = 0; i < n; ++i) {
+        auto u = [&]() { return bits((double)(next_u64() >> 11) * 0x1p-53); };
+        const uint64_t a = u(), b = u(), c = u(), d = u();
+        check_sum4(a, b, c, d);
+        auto v = [&]() { return bits(-(0.25 + 0.5 * (double)(next_u64() >> 11) * 0x1p-53)); };
+        const uint64_t e = v(), f = v(), g = v(), h = v();
+        check_sum4(e, f, g, h);
+    }
+    std::printf("mismatches %llu cases %llu sum4_taken %llu\n", (unsigned long long)mismatches,
+                (unsigned long long)cases, (unsigned long long)sum4_taken);
     return mismatches != 0;
 }

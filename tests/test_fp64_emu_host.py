@@ -6,9 +6,14 @@ about 21 million operand pairs (random bit patterns, every exponent
 difference up to 70, cancellations, ties, products from deep underflow to
 overflow, exact and halfway products, subnormal operands, the ends of the
 exponent range and special values; the complete algorithms and the fast
-paths, including the fixed-factor product with either operand fixed)."""
+paths, including the fixed-factor product with either operand fixed), and
+the fixed-point sum of four same-sign operands, ((a + b) + c) + d, on every
+case its fast form accepts (about 5 million: spreads up to the 9-binade
+limit, ties in each partial sum, all-ones significands, sums near
+overflow, the diffusion's own value ranges)."""
 from __future__ import annotations
 
+import re
 import shutil
 import subprocess
 from pathlib import Path
@@ -28,3 +33,5 @@ def test_emulated_add_and_mul_match_ieee(tmp_path):
     r = subprocess.run([str(exe), "1000000"], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "mismatches 0 " in r.stdout, r.stdout
+    taken = int(re.search(r"sum4_taken (\d+)", r.stdout).group(1))
+    assert taken > 4_000_000, r.stdout
