@@ -45,13 +45,16 @@
 #include "mbarrier.cuh"
 
 // How the FP64 update splits its work between the FP64 unit and the integer
-// pipes (fp64_emu.cuh): the first two of the five neighbour sums (W+E, +S,
-// +N, +B, +T, in that order) and both products (alpha * (...) and 6c) run on
-// the integer pipes.  This measured fastest on GB300 (6% below three sums
-// and no product); every split gives the same bits.  Aligned FP32 grids take
-// the bulk-copy kernel; FP64 takes the register march kernel, which measured
-// faster there (FP64 arithmetic, not memory, bounds the FP64 update).
-constexpr int kEmuSums3d = 2;
+// pipes (fp64_emu.cuh): the five neighbour sums (W+E, +S, +N, +B, +T, in that
+// order) run in one fixed-point frame on the integer pipes where the six
+// operands have one sign and span at most 8 binades (emu::sum_one_sign_fast);
+// 6c, the subtraction, alpha * (...) and the last addition run on the FP64
+// unit (4 instructions per cell).  Per 512^3 step on GB300: 1.56 ms, against
+// 1.85 ms with two sums and both products on the integer pipes (1.68 ms with
+// the frame and both products there: the ALU pipe saturates).  Every split
+// gives the same bits.  Aligned FP32 grids take the bulk-copy kernel; FP64
+// takes the register march kernel, which measured faster there (FP64
+// arithmetic, not memory, bounds the FP64 update).
 
 namespace fvf {
 namespace {
@@ -63,29 +66,46 @@ __device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(
 __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
 __device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
 
-template <int I>
-__device__ __forceinline__ float sum_rn(float a, float b) { return __fadd_rn(a, b); }
-template <int I>
-__device__ __forceinline__ double sum_rn(double a, double b) {
-    return I < kEmuSums3d ? emu::add_same_sign(a, b) : __dadd_rn(a, b);
-}
-
-// k * x with the factor k fixed for the sweep (FP64: on the integer pipes)
-template <int BIT>
-__device__ __forceinline__ float mulk_rn(float k, float x) { return __fmul_rn(k, x); }
-template <int BIT>
-__device__ __forceinline__ double mulk_rn(double k, double x) {
-    return emu::from_bits(emu::mul_const_bits(emu::bits(x), emu::mul_const(k)));
-}
+__device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
 
 template <typename T>
 __device__ __forceinline__ T update3(T c, T w, T e, T s, T n, T b, T t, T alpha) {
-    T x = sum_rn<0>(w, e);
-    x = sum_rn<1>(x, s);
-    x = sum_rn<2>(x, n);
-    x = sum_rn<3>(x, b);
-    x = sum_rn<4>(x, t);
-    return add_rn(c, mulk_rn<1>(alpha, sub_rn(x, mulk_rn<2>(T(6), c))));
+    T x = add_rn(w, e);
+    x = add_rn(x, s);
+    x = add_rn(x, n);
+    x = add_rn(x, b);
+    x = add_rn(x, t);
+    return add_rn(c, mul_rn(alpha, sub_rn(x, mul_rn(T(6), c))));
+}
+
+// The five neighbour sums on the FP64 unit, for the lanes whose operands the
+// fixed-point frame declines (zeros such as the boundary neighbours, signs
+// that differ, spreads over 8 binades, subnormals, values from 2^1021 up).
+// Out of line on bit patterns: a call is not if-converted, so lanes that
+// take the frame issue no FP64 instruction for the sum.
+static __device__ __noinline__ uint64_t sum6_fp64_unit(uint64_t w, uint64_t e, uint64_t s,
+                                                       uint64_t n, uint64_t b, uint64_t t) {
+    double x = __dadd_rn(emu::from_bits(w), emu::from_bits(e));
+    x = __dadd_rn(x, emu::from_bits(s));
+    x = __dadd_rn(x, emu::from_bits(n));
+    x = __dadd_rn(x, emu::from_bits(b));
+    return emu::bits(__dadd_rn(x, emu::from_bits(t)));
+}
+
+template <>
+__device__ __forceinline__ double update3<double>(double c, double w, double e, double s,
+                                                  double n, double b, double t, double alpha) {
+    const uint64_t X[6] = {emu::bits(w), emu::bits(e), emu::bits(s),
+                           emu::bits(n), emu::bits(b), emu::bits(t)};
+    const int hw = __double2hiint(w);
+    const bool one_sign = ((hw ^ __double2hiint(e)) | (hw ^ __double2hiint(s)) |
+                           (hw ^ __double2hiint(n)) | (hw ^ __double2hiint(b)) |
+                           (hw ^ __double2hiint(t))) >= 0;
+    uint64_t sum;
+    const bool ok = emu::sum_one_sign_fast<6>(X, &sum);
+    if (!(ok && one_sign)) sum = sum6_fp64_unit(X[0], X[1], X[2], X[3], X[4], X[5]);
+    return __dadd_rn(c, __dmul_rn(alpha, __dsub_rn(emu::from_bits(sum), __dmul_rn(6.0, c))));
 }
 
 template <typename T, int V>
@@ -148,8 +168,10 @@ __device__ __forceinline__ void store_vec(T *p, const Vec<T, V> &x) {
     }
 }
 
+// FP64: at most 64 registers, 4 blocks of 256 threads per SM (1.56 against
+// 1.67 ms per 512^3 step at 74 registers and 3 blocks; 5 blocks spill).
 template <typename T, int V>
-__global__ void __launch_bounds__(32 * kTY)
+__global__ void __launch_bounds__(32 * kTY, sizeof(T) == 8 ? 4 : 0)
 diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                  int64_t nz, T alpha, int64_t kz_len) {
     __shared__ T rows[2][kTY + 2][32 * V];
@@ -507,12 +529,23 @@ cudaError_t launch_typed(const T *src, T *dst, int64_t nx, int64_t ny, int64_t n
     const int64_t gx = (nx + 32 * V - 1) / (32 * V);
     const int64_t gy = (ny + kTY - 1) / kTY;
     if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
-    // split the planes into runs so that about 8 blocks per SM are in flight
-    const int64_t want = (int64_t)sm_count() * 8;
-    int64_t runs = (want + gx * gy - 1) / (gx * gy);
-    if (runs < 1) runs = 1;
-    int64_t kz_len = (nz + runs - 1) / runs;
-    if (kz_len < 8) kz_len = nz < 8 ? nz : 8;
+    int64_t kz_len;
+    if (sizeof(T) == 8) {
+        // FP64: runs of 16 planes, many waves of blocks: with about one wave
+        // of long runs the blocks whose rows meet the zero faces (their
+        // lanes take the FP64 fallback) finished last while SMs idled (512^3
+        // step: runs of 171, 64, 32, 16, 8 planes 1.85, 1.72, 1.70, 1.70,
+        // 1.71 ms with the earlier update)
+        kz_len = nz < 16 ? nz : 16;
+        if ((nz + kz_len - 1) / kz_len > 65535) kz_len = (nz + 65534) / 65535;
+    } else {
+        // split the planes into runs so that about 8 blocks per SM are in flight
+        const int64_t want = (int64_t)sm_count() * 8;
+        int64_t runs = (want + gx * gy - 1) / (gx * gy);
+        if (runs < 1) runs = 1;
+        kz_len = (nz + runs - 1) / runs;
+        if (kz_len < 8) kz_len = nz < 8 ? nz : 8;
+    }
     const int64_t gz = (nz + kz_len - 1) / kz_len;
     if (gz > 65535) return cudaErrorInvalidValue;
     diffuse3d_kernel<T, V><<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), dim3(32, kTY), 0,

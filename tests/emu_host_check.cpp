@@ -67,7 +67,20 @@ static uint64_t sum4_taken = 0;
 static void check_sum4(uint64_t A, uint64_t B, uint64_t C, uint64_t D) {
     uint64_t got;
     if (((A ^ B) | (A ^ C) | (A ^ D)) & kSign) return;
-    if (!sum4_one_sign_fast(A, B, C, D, &got)) return;
+    const uint64_t X[4] = {A, B, C, D};
+    uint64_t tgot;
+    const bool tok = sum_one_sign_fast<4>(X, &tgot);
+    if (!sum4_one_sign_fast(A, B, C, D, &got)) {
+        if (tok) {                               // the two forms must agree
+            if (mismatches < 10) std::printf("sum4 forms disagree on acceptance\n");
+            ++mismatches;
+        }
+        return;
+    }
+    if (!tok || tgot != got) {
+        if (mismatches < 10) std::printf("sum4 forms disagree\n");
+        ++mismatches;
+    }
     ++sum4_taken;
     ++cases;
     const double want = native_add(native_add(native_add(from_bits(A), from_bits(B)), from_bits(C)),
@@ -77,6 +90,27 @@ static void check_sum4(uint64_t A, uint64_t B, uint64_t C, uint64_t D) {
             std::printf("sum4 %016llx %016llx %016llx %016llx: got %016llx want %016llx\n",
                         (unsigned long long)A, (unsigned long long)B, (unsigned long long)C,
                         (unsigned long long)D, (unsigned long long)got, (unsigned long long)bits(want));
+        ++mismatches;
+    }
+}
+
+static uint64_t sum6_taken = 0;
+
+// (((((X0 + X1) + X2) + X3) + X4) + X5): the six-operand frame where it
+// accepts the operands (one sign: its precondition).
+static void check_sum6(const uint64_t (&X)[6]) {
+    for (int q = 1; q < 6; ++q)
+        if ((X[q] ^ X[0]) & kSign) return;
+    uint64_t got;
+    if (!sum_one_sign_fast<6>(X, &got)) return;
+    ++sum6_taken;
+    ++cases;
+    double want = from_bits(X[0]);
+    for (int q = 1; q < 6; ++q) want = native_add(want, from_bits(X[q]));
+    if (got != bits(want)) {
+        if (mismatches < 10)
+            std::printf("sum6 %016llx ... %016llx: got %016llx want %016llx\n", (unsigned long long)X[0],
+                        (unsigned long long)X[5], (unsigned long long)got, (unsigned long long)bits(want));
         ++mismatches;
     }
 }
@@ -256,7 +290,39 @@ int main(int argc, char **argv) {
         const uint64_t e = v(), f = v(), g = v(), h = v();
         check_sum4(e, f, g, h);
     }
-    std::printf("mismatches %llu cases %llu sum4_taken %llu\n", (unsigned long long)mismatches,
-                (unsigned long long)cases, (unsigned long long)sum4_taken);
+    // six-operand sums (the 3D update's neighbours): the same kinds of cases
+    // with the 8-binade limit of the six-operand frame
+    for (long i = 0; i < n; ++i) {
+        const uint64_t sg = next_u64() & 1, e0 = 1 + next_u64() % 2046;
+        uint64_t X[6];
+        for (auto &x : X) {
+            int64_t e = (int64_t)e0 + (int64_t)(next_u64() % 19) - 9;
+            e = e < 0 ? 0 : (e > 2047 ? 2047 : e);
+            x = make(sg, (uint64_t)e, next_u64());
+        }
+        check_sum6(X);
+        for (auto &x : X) {
+            int64_t e = (int64_t)e0 + (int64_t)(next_u64() % 3) - 1;
+            e = e < 0 ? 0 : (e > 2047 ? 2047 : e);
+            const uint64_t f = (next_u64() & 1) ? next_u64() : next_u64() & ~((1ull << (next_u64() % 53)) - 1);
+            x = make(sg, (uint64_t)e, f);
+        }
+        check_sum6(X);
+        const uint64_t e1 = 1 + next_u64() % 2040;
+        for (auto &x : X) x = make(sg, e1 + next_u64() % 9, (next_u64() & 1) ? kFrac : (next_u64() & 0xFFF0000000000ull));
+        check_sum6(X);
+        const uint64_t t = make(sg, 2030 + next_u64() % 18, kFrac - next_u64() % 8);
+        for (auto &x : X) x = t;
+        check_sum6(X);
+        for (auto &x : X) x = bits((double)(next_u64() >> 11) * 0x1p-53);
+        check_sum6(X);
+        for (auto &x : X) {
+            const uint64_t r = next_u64() % 4;
+            x = r == 0 ? make(sg, 0, 0) : r == 1 ? make(sg, 0, next_u64()) : make(sg, next_u64() % 12, next_u64());
+        }
+        check_sum6(X);
+    }
+    std::printf("mismatches %llu cases %llu sum4_taken %llu sum6_taken %llu\n", (unsigned long long)mismatches,
+                (unsigned long long)cases, (unsigned long long)sum4_taken, (unsigned long long)sum6_taken);
     return mismatches != 0;
 }

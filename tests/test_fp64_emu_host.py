@@ -10,7 +10,9 @@ paths, including the fixed-factor product with either operand fixed), and
 the fixed-point sum of four same-sign operands, ((a + b) + c) + d, on every
 case its fast form accepts (about 5 million: spreads up to the 9-binade
 limit, ties in each partial sum, all-ones significands, sums near
-overflow, the diffusion's own value ranges)."""
+overflow, the diffusion's own value ranges; the written-out form and the
+N-operand template must agree), and the six-operand frame of the 3D update
+on about 3.8 million accepted sets."""
 from __future__ import annotations
 
 import re
@@ -35,3 +37,5 @@ def test_emulated_add_and_mul_match_ieee(tmp_path):
     assert "mismatches 0 " in r.stdout, r.stdout
     taken = int(re.search(r"sum4_taken (\d+)", r.stdout).group(1))
     assert taken > 4_000_000, r.stdout
+    taken6 = int(re.search(r"sum6_taken (\d+)", r.stdout).group(1))
+    assert taken6 > 3_000_000, r.stdout
