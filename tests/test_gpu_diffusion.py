@@ -198,6 +198,72 @@ def test_mixed_sign_fields(nx, ny):
         assert_bits_equal(gv, ov, what=f"v {nx}x{ny} {steps}")
 
 
+def _binade_field(nx, ny, seed):
+    """FP64 field in bands of 8 rows, each band built from sign, exponent and
+    fraction bits so that the four neighbours of a cell meet one boundary of
+    the march kernel's fixed-point neighbour sum: exponents spread over at
+    most 9 binades (accepted) or 10 (declined), significands of at most four
+    bits (rounding ties in the partial sums), all-ones significands, largest
+    exponents on both sides of the 2^1020 bound (sums that overflow
+    included) and of the 2^-1013 bound, zeros and subnormals, negative bands,
+    and rows of mixed signs."""
+    n = nx * ny
+    b = inputs.random_bits(seed, 1, 3 * n).reshape(3, ny, nx)
+    frac = b[0] & np.uint64((1 << 52) - 1)
+    u8 = (b[1] & np.uint64(0xFF)).astype(np.int64)
+    mode = (np.arange(ny) // 8) % 10
+    u0 = np.zeros((ny, nx), dtype=np.float64)
+    for m in range(10):
+        rows = mode == m
+        fr, r = frac[rows], u8[rows]
+        if m == 0:       # spread <= 9 binades about 2^0
+            e = 1023 - r % 10
+        elif m == 1:     # spread up to 10 binades
+            e = 1023 - r % 11
+        elif m == 2:     # four-bit significands, spread 3: ties
+            e = 1023 - r % 4
+            fr = fr & np.uint64(0xF << 48)
+        elif m == 3:     # all-ones significands, spread 9
+            e = 1023 - r % 10
+            fr = np.full_like(fr, (1 << 52) - 1)
+        elif m == 4:     # largest exponents about 2^1020: both sides of the range bound
+            e = 2045 - r % 6
+        elif m == 5:     # largest exponents about 2^-1013: both sides of the lower bound
+            e = 12 - r % 6
+        elif m == 6:     # zeros and subnormals among normal values
+            e = np.where(r % 5 == 0, 0, 1023 - r % 4)
+            fr = np.where(r % 10 == 0, np.uint64(0), fr)
+        elif m == 7:     # negative band, spread <= 9
+            e = 1023 - r % 10
+        elif m == 8:     # mixed signs in every row
+            e = 1023 - r % 3
+        else:            # spread exactly 9 and 10 in alternating columns
+            e = np.where((np.arange(nx)[None, :] % 2) == 0, 1023, 1014 - (r % 2))
+            e = np.broadcast_to(e, fr.shape)
+        sign = np.uint64(1 << 63) if m == 7 else (
+            ((b[2][rows] & np.uint64(1)) << np.uint64(63)) if m == 8 else np.uint64(0))
+        bits = sign | (np.asarray(e, dtype=np.uint64) << np.uint64(52)) | fr
+        u0[rows] = bits.view(np.float64)
+    u0[0, :] = u0[-1, :] = 0.0
+    u0[:, 0] = u0[:, -1] = 0.0
+    return u0
+
+
+@pytest.mark.parametrize("nx,ny", [(1024, 160), (2050, 88)])
+def test_fixed_point_sum_boundaries(nx, ny):
+    """FP64 on grids the march kernel takes: every boundary of the
+    fixed-point neighbour sum (spread, range, ties, zeros, subnormals, signs),
+    1 and 2 steps, both buffers bit-exact up to NaN payloads (the bands near
+    2^1021 overflow to infinities and NaNs)."""
+    torch = torch_cuda()
+    u0 = _binade_field(nx, ny, 31)
+    for steps in (1, 2):
+        gu, gv = _run_gpu(torch, u0, steps)
+        ou, ov, _ = oracle.diffuse2d(u0, steps, return_both=True)
+        assert_bits_equal(gu, ou, nan_payloads=False, what=f"u {nx}x{ny} {steps}")
+        assert_bits_equal(gv, ov, nan_payloads=False, what=f"v {nx}x{ny} {steps}")
+
+
 def test_full_size_normal_field():
     """The 8192 x 8192 FP64 grid with interior N(0,1) values (mixed signs),
     20 steps, in the launch configuration the benchmark times, cell by cell

@@ -60,6 +60,54 @@ def test_small_grids(dt, shape, steps):
     assert_bits_equal(gv, ov, what=f"v {shape} {steps}")
 
 
+def _binade_field_3d(shape, seed):
+    """FP64 3D field in slabs of 4 planes, each built from sign, exponent and
+    fraction bits so that a cell's six neighbours meet one boundary of the
+    six-operand fixed-point sum: spreads of at most 8 binades (accepted) or 9
+    (declined), significands of at most four bits (ties), all-ones
+    significands, exponents about 2^1020 and 2^-1014, zeros and subnormals,
+    a negative slab and mixed signs."""
+    nz, ny, nx = shape
+    n = nz * ny * nx
+    b = inputs.random_bits(seed, 2, 3 * n).reshape(3, nz, ny, nx)
+    frac = b[0] & np.uint64((1 << 52) - 1)
+    r = (b[1] & np.uint64(0xFF)).astype(np.int64)
+    u0 = np.zeros(shape, dtype=np.float64)
+    for k in range(nz):
+        m = (k // 4) % 8
+        fr, rk = frac[k], r[k]
+        e = {0: 1023 - rk % 9, 1: 1023 - rk % 10, 2: 1023 - rk % 3, 3: 1023 - rk % 9,
+             4: 2045 - rk % 6, 5: 11 - rk % 6, 6: np.where(rk % 5 == 0, 0, 1023 - rk % 4),
+             7: 1023 - rk % 3}[m]
+        if m == 2:
+            fr = fr & np.uint64(0xF << 48)
+        if m == 3:
+            fr = np.full_like(fr, (1 << 52) - 1)
+        if m == 6:
+            fr = np.where(rk % 10 == 0, np.uint64(0), fr)
+        sign = np.uint64(1 << 63) if m == 3 else (
+            ((b[2][k] & np.uint64(1)) << np.uint64(63)) if m == 7 else np.uint64(0))
+        u0[k] = (sign | (np.asarray(e, dtype=np.uint64) << np.uint64(52)) | fr).view(np.float64)
+    u0[0], u0[-1] = 0, 0
+    u0[:, 0], u0[:, -1] = 0, 0
+    u0[:, :, 0], u0[:, :, -1] = 0, 0
+    return u0
+
+
+@pytest.mark.parametrize("shape", [(34, 20, 130), (40, 9, 64)])
+def test_fixed_point_sum_boundaries(shape):
+    """FP64 march kernel on fields that meet every boundary of the
+    six-operand fixed-point sum, 1 and 2 steps, both buffers bit-exact up to
+    NaN payloads (the slabs near 2^1021 overflow)."""
+    torch = torch_cuda()
+    u0 = _binade_field_3d(shape, 41)
+    for steps in (1, 2):
+        gu, gv = _run(torch, u0, steps)
+        ou, ov, _ = oracle.diffuse3d(u0, steps, 0.1, return_both=True)
+        assert_bits_equal(gu, ou, nan_payloads=False, what=f"u {shape} {steps}")
+        assert_bits_equal(gv, ov, nan_payloads=False, what=f"v {shape} {steps}")
+
+
 @pytest.mark.parametrize("dt", [np.float64, np.float32])
 def test_impulse_and_special_values(dt):
     """A centre impulse (exact one-step values at alpha = 1/8), then a field
