@@ -1062,9 +1062,9 @@ def run_ncu_case():
     on the same fields (at most about 1.7 GB), flux difference x/y/z on
     8 x 201^3, the SSPRK3 stage fused with the x/y/z flux difference on
     8 x 201^3 (about 3.1 GB), one 3D 7-point diffusion step on 512^3 in FP32
-    then FP64 (at most 2.1 GB), and the 64 x 64 FP64 centre impulse for 32
-    steps (one cluster launch); then the FP32 pack y/z and the FP32 flux
-    difference x.  FP64 runs 2 single steps, FP32 17 steps (two 8-step
+    then FP64 (at most 2.1 GB), the FP32 pack y, z, x and the FP32 flux
+    difference x, and last the 64 x 64 FP64 centre impulse for 32 steps (one
+    cluster launch).  The 2D FP32 diffusion runs 17 steps (two 8-step
     shared-memory launches, then one single step).  Device-generated values:
     the timing of the sweeps does not depend on them, except the FP64
     diffusion's, whose field is U[0,1) with zero edges (the benchmark's
@@ -1130,12 +1130,12 @@ def run_ncu_case():
         api.diffuse3d_step(u, v, 512, 512, 512, 0.1, 1, code)
         del u, v
         free()
-    # FP32 pack y/z on 8 fields of 207^3 and the FP32 flux difference x on
+    # FP32 pack y, z, x on 8 fields of 207^3 and the FP32 flux difference x on
     # 8 x 201^3 (at most about 0.55 GB)
     fields = [torch.randn(N, dtype=torch.float32, device="cuda") for _ in range(PACK_NV)]
     out = torch.empty(_prod(pack_extents(PACK_EXT, PACK_G, 0)) * PACK_NV, dtype=torch.float32,
                       device="cuda")
-    for d in (1, 2):
+    for d in (1, 2, 0):
         api.weno_pack_f32(fields, PACK_NV, PACK_EXT, PACK_G, d, out)
     del fields, out
     free()
