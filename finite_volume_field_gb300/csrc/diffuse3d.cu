@@ -62,12 +62,9 @@ namespace {
 constexpr int kTY = 8;  // warps (rows along j) per block
 
 __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
-__device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
 __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
-__device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
 
 __device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
-__device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
 
 template <typename T>
 __device__ __forceinline__ T update3(T c, T w, T e, T s, T n, T b, T t, T alpha) {
@@ -77,6 +74,43 @@ __device__ __forceinline__ T update3(T c, T w, T e, T s, T n, T b, T t, T alpha)
     x = add_rn(x, b);
     x = add_rn(x, t);
     return add_rn(c, mul_rn(alpha, sub_rn(x, mul_rn(T(6), c))));
+}
+
+// FP32 update of two cells at once for the bulk kernel: the additions as
+// packed two-lane FP32 instructions (add.rn.f32x2, each lane an IEEE
+// round-to-nearest addition), the products 6c and alpha * (...) as scalar
+// multiplications.  A packed product whose only use is a packed addition is
+// contracted into one packed fused multiply-add by the compiler, even with
+// explicit .rn and --fmad=false (measured on GB300: the fused result in 100%
+// of cases); scalar products feeding a packed addition are not.  11
+// instructions for two cells instead of 18: 0.212 -> 0.197 ms per 512^3
+// step, bit-identical.  (In the 2D blocked kernel the same form measured
+// slower: building the lane pairs costs more there.)
+__device__ __forceinline__ unsigned long long pack2(float x, float y) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 unpack2(unsigned long long r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+__device__ __forceinline__ unsigned long long add2_rn(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float2 update3x2(float2 c, float2 w, float2 e, float2 s, float2 n,
+                                           float2 b, float2 t, float alpha) {
+    unsigned long long x = add2_rn(pack2(w.x, w.y), pack2(e.x, e.y));
+    x = add2_rn(x, pack2(s.x, s.y));
+    x = add2_rn(x, pack2(n.x, n.y));
+    x = add2_rn(x, pack2(b.x, b.y));
+    x = add2_rn(x, pack2(t.x, t.y));
+    // x - 6c as x + (-6c): the same rounded result
+    const float2 d = unpack2(add2_rn(x, pack2(__fmul_rn(-6.0f, c.x), __fmul_rn(-6.0f, c.y))));
+    return unpack2(add2_rn(pack2(c.x, c.y), pack2(__fmul_rn(alpha, d.x), __fmul_rn(alpha, d.y))));
 }
 
 // The five neighbour sums on the FP64 unit, for the lanes whose operands the
@@ -421,14 +455,34 @@ diffuse3d_bulk_kernel(const __grid_constant__ CUtensorMap src_map, T *__restrict
                     const T er = __shfl_down_sync(0xffffffffu, c.v[0], 1);
                     const T wfirst = lane == 0 ? rc[-1] : wl;      // margin cell x0-1
                     const T elast = lane == 31 ? rc[V] : er;       // margin cell x0+32V
+                    T res[V];
+                    if constexpr (sizeof(T) == 4) {
+                        // two cells per update3x2: (v, v+1) with W (v-1, v), E (v+1, v+2)
+#pragma unroll
+                        for (int v = 0; v < V; v += 2) {
+                            const T w0 = v == 0 ? wfirst : c.v[(v + V - 1) % V];
+                            const T e1 = v + 2 < V ? c.v[(v + 2) % V] : elast;
+                            const float2 r2 = update3x2(
+                                make_float2(c.v[v], c.v[v + 1]), make_float2(w0, c.v[v]),
+                                make_float2(c.v[v + 1], e1), make_float2(so.v[v], so.v[v + 1]),
+                                make_float2(no.v[v], no.v[v + 1]), make_float2(bo.v[v], bo.v[v + 1]),
+                                make_float2(to.v[v], to.v[v + 1]), alpha);
+                            res[v] = r2.x;
+                            res[v + 1] = r2.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < V; ++v) {
+                            const T we = v == 0 ? wfirst : c.v[v - 1];
+                            const T ea = v == V - 1 ? elast : c.v[v + 1];
+                            res[v] = update3<T>(c.v[v], we, ea, so.v[v], no.v[v], bo.v[v],
+                                                to.v[v], alpha);
+                        }
+                    }
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        const T we = v == 0 ? wfirst : c.v[v - 1];
-                        const T ea = v == V - 1 ? elast : c.v[v + 1];
-                        const T res = update3<T>(c.v[v], we, ea, so.v[v], no.v[v], bo.v[v],
-                                                 to.v[v], alpha);
                         const int64_t i = xi + v;
-                        out.v[v] = (lane_inner || (i != 0 && i < nx - 1)) ? res : T(0);
+                        out.v[v] = (lane_inner || (i != 0 && i < nx - 1)) ? res[v] : T(0);
                     }
                 }
                 T *drw = drow + kTY * r * nx;
