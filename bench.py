@@ -25,6 +25,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import re
 import statistics
 import subprocess
@@ -482,6 +483,50 @@ def oracle_sample(host, diffusion_steps=160, passes=10):
         tot_b += r["bytes"] / SEQ_REPS
         tot_cv += r["cellvars"] / SEQ_REPS
     return tot_b, tot_cv, tot_s, threads
+
+
+def oracle_single_thread(host, steps=2):
+    """The oracle's FP64 diffusion on the full 8192^2 grid on one host thread
+    (the same loops and operation order as the all-threads run), for the
+    single-core figure beside the all-cores one."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.diffuse2d(host["u64"], steps, nthreads=1)
+    sec = time.perf_counter() - t0
+    b = steps * 2 * DIFF_N * DIFF_N * 8
+    return {"value": round(b / sec / 1e9, 3), "unit": "GB/s", "cores": 1,
+            "gcell_per_s": round(steps * (DIFF_N - 2) ** 2 / sec / 1e9, 4),
+            "sample": f"{steps} FP64 diffusion steps on 8192^2, one thread",
+            "seconds": round(sec, 2)}
+
+
+def cpu_model():
+    """The host CPU's model as the kernel reports it (x86 model name, or the
+    Arm implementer and part numbers), with the logical CPU count."""
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "CPU part"):
+            for line in info.splitlines():
+                if line.startswith(key):
+                    name = line.split(":", 1)[1].strip()
+                    break
+            if name:
+                if key == "CPU part":
+                    impl = [l.split(":", 1)[1].strip() for l in info.splitlines()
+                            if l.startswith("CPU implementer")]
+                    name = f"implementer {impl[0] if impl else '?'} part {name}"
+                break
+    except OSError:
+        pass
+    return {"model": name or platform.processor() or platform.machine(),
+            "machine": platform.machine(), "logical_cpus": os.cpu_count()}
+
+
+def oracle_build_flags():
+    import oracle
+    return " ".join(getattr(oracle, "_CFLAGS", [])) + " (+ -fopenmp where available)"
 
 
 ORACLE_SAMPLE_DESC = ("160 diffusion steps per precision on 8192^2 (OpenMP over rows, all host "
@@ -1002,6 +1047,8 @@ def run_gpu(args):
             t = statistics.median(per_row[name])
             sweeps[name] = {
                 "ms": round(t, 4), "launches": r["launches"],
+                # median over the timed steps, and the fastest and slowest step
+                "spread_ms": [round(min(per_row[name]), 4), round(max(per_row[name]), 4)],
                 "gbs": round(r["bytes"] / (t * 1e-3) / 1e9, 1),
                 "gcell_var_per_s": round(r["cellvars"] / (t * 1e-3) / 1e9, 2),
                 "frac_hbm": round(r["bytes"] / (t * 1e-3) / 1e9 / hbm, 4),
@@ -1043,7 +1090,10 @@ def run_gpu(args):
                                     "cores": threads, "kind": "oracle",
                                     "sample": ORACLE_SAMPLE_DESC,
                                     "gcell_var_per_s": round(cv / sec / 1e9, 4),
-                                    "seconds": round(sec, 2)}
+                                    "seconds": round(sec, 2),
+                                    "single_thread": oracle_single_thread(host),
+                                    "cpu_model": cpu_model(),
+                                    "oracle_build": oracle_build_flags()}
         # the per-sweep table last: a reader of the end of the line sees it
         line["sweeps"] = sweeps
         print(json.dumps(line), flush=True)
