@@ -246,8 +246,10 @@ FVF_HD double add(double a, double b) { return from_bits(add_bits(bits(a), bits(
 //     partial sums stay below 2^64 - 2^11: the largest case rounds
 //     2^64 - 2560 to 2^64 - 2048, so no step carries out of the frame) and
 //     is then rounded to its 53 leading bits, ties to even, exactly as the
-//     binary64 addition rounds it; the leading one is at bit 61 or above,
-//     so the p = 11 - clz(high word) bits below those 53 number 1 to 11;
+//     binary64 addition rounds it; a partial sum of two or more operands
+//     (each at least 2^52 in the frame) has its leading one at bit 53 or
+//     above, so the p = 11 - clz(high word) bits below those 53 number 1
+//     to 11;
 //   * rounding adds 2^(p-1) - 1 + (the kept part's last bit) and clears the
 //     p low bits (round half to even: a remainder of exactly 2^(p-1) moves
 //     up only when the kept part is odd); the carry of a round-up stays in
