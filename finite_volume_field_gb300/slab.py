@@ -7,8 +7,8 @@ advances ``k <= halo`` steps at a time with the library's own
 ``diffuse2d_step`` on its stored rows (FP32 then takes the shared-memory
 blocked kernel for k > 2), then exchanges halos: it sends its first and last
 ``halo`` owned rows to its neighbours and receives theirs into its halo
-rows.  One exchange per ``k`` steps (the decomposition of SURVEY-style
-temporal blocking; with k = 1, one row per step).
+rows.  One exchange per ``k`` steps (halos as deep as the block of steps,
+as in temporal blocking; with k = 1, one row per step).
 
 Why this reproduces the single-grid result bit for bit: the library treats
 the first and last stored rows as edges and writes zeros there each step.
