@@ -33,8 +33,9 @@
 //   march  (FP64, and FP32 rows that are not 16-byte aligned; V cells per
 //          lane, 1 when unaligned): each lane keeps planes k-1, k, k+1 of its
 //          cells in registers and prefetches k+2; W/E by warp shuffle, S/N
-//          from the tile's rows staged in shared memory.  The grid splits the
-//          planes into runs so that about 8 blocks per SM are in flight.
+//          from the tile's rows staged in shared memory.  FP64: runs of 16
+//          planes (many waves of blocks); FP32: the planes split into runs so
+//          that about 8 blocks per SM are in flight.
 #include <cuda.h>
 
 #include <atomic>
