@@ -264,6 +264,23 @@ def test_fixed_point_sum_boundaries(nx, ny):
         assert_bits_equal(gv, ov, nan_payloads=False, what=f"v {nx}x{ny} {steps}")
 
 
+@pytest.mark.parametrize("alpha", [0.25, 1.0 / 3.0, 0.0, 1e-300, 0.1 + 2.0 ** -50])
+def test_march_alpha_values(alpha):
+    """FP64 march kernel (1024 x 48, above the cluster kernel's size) with
+    alpha at the stability limit, above it, zero, tiny (products deep in the
+    subnormal range) and 0.1 plus one unit in its last place; a mixed-sign
+    field, 1 and 3 steps, both buffers bit-exact."""
+    torch = torch_cuda()
+    nx, ny = 1024, 48
+    u0 = inputs.normal_f64(33, 4, nx * ny).reshape(ny, nx)
+    u0[ny // 2:, :] = np.abs(u0[ny // 2:, :])
+    for steps in (1, 3):
+        gu, gv = _run_gpu(torch, u0, steps, alpha=alpha)
+        ou, ov, _ = oracle.diffuse2d(u0, steps, alpha=alpha, return_both=True)
+        assert_bits_equal(gu, ou, what=f"u alpha={alpha} {steps}")
+        assert_bits_equal(gv, ov, what=f"v alpha={alpha} {steps}")
+
+
 def test_full_size_normal_field():
     """The 8192 x 8192 FP64 grid with interior N(0,1) values (mixed signs),
     20 steps, in the launch configuration the benchmark times, cell by cell

@@ -108,6 +108,23 @@ def test_fixed_point_sum_boundaries(shape):
         assert_bits_equal(gv, ov, nan_payloads=False, what=f"v {shape} {steps}")
 
 
+@pytest.mark.parametrize("alpha", [1.0 / 6.0, 0.25, 0.0, 1e-300])
+def test_fp64_alpha_values(alpha):
+    """FP64 register kernel with alpha at the 3D stability limit (1/6),
+    above it, zero and tiny, on a field whose upper half is positive (the
+    fixed-point sum) and lower half mixed in sign (the FP64 fallback); 1 and 3
+    steps, both buffers bit-exact."""
+    torch = torch_cuda()
+    shape = (20, 18, 66)
+    u0 = inputs.normal_f64(34, 5, int(np.prod(shape))).reshape(shape)
+    u0[shape[0] // 2:] = np.abs(u0[shape[0] // 2:])
+    for steps in (1, 3):
+        gu, gv = _run(torch, u0, steps, alpha=alpha)
+        ou, ov, _ = oracle.diffuse3d(u0, steps, alpha, return_both=True)
+        assert_bits_equal(gu, ou, what=f"u alpha={alpha} {steps}")
+        assert_bits_equal(gv, ov, what=f"v alpha={alpha} {steps}")
+
+
 @pytest.mark.parametrize("dt", [np.float64, np.float32])
 def test_impulse_and_special_values(dt):
     """A centre impulse (exact one-step values at alpha = 1/8), then a field
