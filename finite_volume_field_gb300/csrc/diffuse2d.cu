@@ -131,19 +131,32 @@ static __device__ __noinline__ uint64_t sum4_fp64_unit(uint64_t w, uint64_t e, u
                                emu::from_bits(n)));
 }
 
-template <typename T>
-__device__ __forceinline__ T update_frame(T c, T w, T e, T s, T n, T alpha) {
-    return update<T>(c, w, e, s, n, alpha);
-}
+// ZSLOT (0 = W, 1 = E, -1 = none): the neighbour that may be a zero the
+// frame still takes, the face-side neighbour of a cell next to an x edge
+// (with two cells per lane: W for the odd cell, E for the even one).  `face`
+// marks a cell whose result is discarded (an edge cell): it never calls the
+// fallback.  Together they keep the two warps of a row that hold an x edge
+// off the fallback on fields with zero edges.
+template <typename T, int ZSLOT>
+struct Frame {
+    static __device__ __forceinline__ T update(T c, T w, T e, T s, T n, T alpha, bool face) {
+        (void)face;
+        return ::fvf::update<T>(c, w, e, s, n, alpha);
+    }
+};
 
-template <>
-__device__ __forceinline__ double update_frame<double>(double c, double w, double e, double s,
-                                                       double n, double alpha) {
-    uint64_t sum;
-    if (!emu::sum4_one_sign_fast(emu::bits(w), emu::bits(e), emu::bits(s), emu::bits(n), &sum))
-        sum = sum4_fp64_unit(emu::bits(w), emu::bits(e), emu::bits(s), emu::bits(n));
-    return __dadd_rn(c, __dmul_rn(alpha, Rn<double>::sub4(emu::from_bits(sum), c)));
-}
+template <int ZSLOT>
+struct Frame<double, ZSLOT> {
+    static __device__ __forceinline__ double update(double c, double w, double e, double s,
+                                                    double n, double alpha, bool face) {
+        uint64_t sum;
+        if (!emu::sum4_one_sign_fast<ZSLOT>(emu::bits(w), emu::bits(e), emu::bits(s),
+                                            emu::bits(n), &sum) &&
+            !face)
+            sum = sum4_fp64_unit(emu::bits(w), emu::bits(e), emu::bits(s), emu::bits(n));
+        return __dadd_rn(c, __dmul_rn(alpha, Rn<double>::sub4(emu::from_bits(sum), c)));
+    }
+};
 
 // The same update for rows where some lane's operands differ in sign.  The
 // same-sign form above sends a pair of opposite signs to the complete
@@ -291,12 +304,19 @@ __device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int
 // come from L2 and the kernel is not bound by HBM.  Per 8192^2 step on
 // GB300: one wave 0.498 ms; bands of 32, 16, 12, 8 and 6 rows 0.424, 0.414,
 // 0.413, 0.415 and 0.419 ms (no register cap; a 40-register cap for 12
-// blocks per SM measured 0.416 ms at 12 rows).
+// blocks per SM measured 0.416 ms at 12 rows).  With the zero slots and the
+// edge cells kept off the fallback (march_rows), bands of 12 and 24 rows
+// measure within 0.2% of each other and one wave is still 14% slower.
 constexpr int kMarchF64Rows = 12;
-template <typename T>
-__global__ void __launch_bounds__(kMarchThreads)
-diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
-                     int64_t rows_per_block, T alpha) {
+// The rows of one band.  ZX: the block holds an x edge, and its frame sums
+// take the zero slots (the other blocks skip the zero tests, whose integer
+// instructions measured more than the edge warps' fallback calls cost: on
+// every block, 0.424 against 0.414 ms per 8192^2 step; on the edge blocks
+// only, 0.404).
+template <typename T, bool ZX>
+__device__ __forceinline__ void march_rows(const T *__restrict__ src, T *__restrict__ dst,
+                                           int64_t nx, int64_t ny, int64_t rows_per_block,
+                                           T alpha) {
     constexpr int V = Vec16<T>::n;
     const int lane = threadIdx.x & 31;
     const int64_t col = ((int64_t)blockIdx.x * kMarchThreads + threadIdx.x) * V;
@@ -331,7 +351,14 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
                 const T e = k < V - 1 ? rc.c.v[k + 1] : e_in;
                 const int64_t i = col + k;
                 const bool edge = edge_row || i == 0 || i == nx - 1;
-                out.v[k] = edge ? T(0) : update_frame<T>(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha);
+                // k is a constant in each unrolled copy
+                const T val =
+                    ZX && V == 2 && k == 0
+                        ? Frame<T, 1>::update(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha, edge)
+                    : ZX && V == 2
+                        ? Frame<T, 0>::update(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha, edge)
+                        : Frame<T, -1>::update(rc.c.v[k], w, e, rs.c.v[k], rn.c.v[k], alpha, edge);
+                out.v[k] = edge ? T(0) : val;
             }
         } else {
 #pragma unroll
@@ -350,6 +377,17 @@ diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx,
         rc = rn;
         rn = rnn;
     }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMarchThreads)
+diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
+                     int64_t rows_per_block, T alpha) {
+    // block-uniform: the first and last column blocks hold the x edges
+    if (sizeof(T) == 8 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1))
+        march_rows<T, true>(src, dst, nx, ny, rows_per_block, alpha);
+    else
+        march_rows<T, false>(src, dst, nx, ny, rows_per_block, alpha);
 }
 
 template <typename T>

@@ -48,12 +48,14 @@
 // How the FP64 update splits its work between the FP64 unit and the integer
 // pipes (fp64_emu.cuh): the five neighbour sums (W+E, +S, +N, +B, +T, in that
 // order) run in one fixed-point frame on the integer pipes where the six
-// operands have one sign and span at most 8 binades (emu::sum_one_sign_fast);
-// 6c, the subtraction, alpha * (...) and the last addition run on the FP64
-// unit (4 instructions per cell).  Per 512^3 step on GB300: 1.56 ms, against
-// 1.85 ms with two sums and both products on the integer pipes (1.68 ms with
-// the frame and both products there: the ALU pipe saturates).  Every split
-// gives the same bits.  Aligned FP32 grids take the bulk-copy kernel; FP64
+// operands have one sign and span at most 8 binades (emu::sum_one_sign_fast;
+// a zero W or E, the face-side neighbour of a cell next to an x face, is
+// taken too); 6c, the subtraction, alpha * (...) and the last addition run on
+// the FP64 unit (4 instructions per cell).  Per 512^3 step on GB300: 1.56 ms
+// before the zero slots (1.48 ms with them, in a build that measured the
+// former at 1.70), against 1.85 ms with two sums and both products on the
+// integer pipes (1.68 ms with the frame and both products there: the ALU
+// pipe saturates).  Every split gives the same bits.  Aligned FP32 grids take the bulk-copy kernel; FP64
 // takes the register march kernel, which measured faster there (FP64
 // arithmetic, not memory, bounds the FP64 update).
 
@@ -128,18 +130,31 @@ static __device__ __noinline__ uint64_t sum6_fp64_unit(uint64_t w, uint64_t e, u
     return emu::bits(__dadd_rn(x, emu::from_bits(t)));
 }
 
-template <>
-__device__ __forceinline__ double update3<double>(double c, double w, double e, double s,
-                                                  double n, double b, double t, double alpha) {
+// FP64 update.  ZSLOT (0 = W, 1 = E, -1 = none) is the neighbour that may be
+// a zero the frame still takes (the face-side neighbour of the cells next to
+// an x face: with two cells per lane that is W for the odd cell and E for the
+// even one).  `face` marks a cell whose result is discarded (a boundary
+// face cell): it never calls the fallback.  Per 512^3 step on GB300, in one
+// build: 1.703 ms with neither, 1.622 with the face cells' calls left out,
+// 1.485 with the zero slots too (bit-identical; the two warps of eight in a
+// 512-wide row that hold an x face no longer take the fallback).
+template <int ZSLOT>
+__device__ __forceinline__ double update3_fp64(double c, double w, double e, double s, double n,
+                                               double b, double t, double alpha, bool face) {
     const uint64_t X[6] = {emu::bits(w), emu::bits(e), emu::bits(s),
                            emu::bits(n), emu::bits(b), emu::bits(t)};
-    const int hw = __double2hiint(w);
-    const bool one_sign = ((hw ^ __double2hiint(e)) | (hw ^ __double2hiint(s)) |
-                           (hw ^ __double2hiint(n)) | (hw ^ __double2hiint(b)) |
-                           (hw ^ __double2hiint(t))) >= 0;
+    uint32_t h[6];
+#pragma unroll
+    for (int q = 0; q < 6; ++q) h[q] = (uint32_t)(X[q] >> 32);
+    // a zero in the slot takes its partner's sign for the test
+    if constexpr (ZSLOT >= 0) {
+        if (emu::is_zero_bits(X[ZSLOT])) h[ZSLOT] = h[1 - ZSLOT];
+    }
+    const bool one_sign = (int)((h[0] ^ h[1]) | (h[0] ^ h[2]) | (h[0] ^ h[3]) |
+                                (h[0] ^ h[4]) | (h[0] ^ h[5])) >= 0;
     uint64_t sum;
-    const bool ok = emu::sum_one_sign_fast<6>(X, &sum);
-    if (!(ok && one_sign)) sum = sum6_fp64_unit(X[0], X[1], X[2], X[3], X[4], X[5]);
+    const bool ok = emu::sum_one_sign_fast<6, ZSLOT>(X, &sum);
+    if (!(ok && one_sign) && !face) sum = sum6_fp64_unit(X[0], X[1], X[2], X[3], X[4], X[5]);
     return __dadd_rn(c, __dmul_rn(alpha, __dsub_rn(emu::from_bits(sum), __dmul_rn(6.0, c))));
 }
 
@@ -205,6 +220,10 @@ __device__ __forceinline__ void store_vec(T *p, const Vec<T, V> &x) {
 
 // FP64: at most 64 registers, 4 blocks of 256 threads per SM (1.56 against
 // 1.67 ms per 512^3 step at 74 registers and 3 blocks; 5 blocks spill).
+// Every block takes the zero slots: taking them only in the blocks that
+// hold an x face (a block-uniform branch between two copies of the loop)
+// spilled at the 64-register cap and measured 3% slower (1.529 against
+// 1.483 ms per step).
 template <typename T, int V>
 __global__ void __launch_bounds__(32 * kTY, sizeof(T) == 8 ? 4 : 0)
 diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
@@ -282,10 +301,23 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
                     const T ea = v == V - 1 ? elast : cur.v[v + 1];
                     const T so = rows[buf][w][lane * V + v];
                     const T no = rows[buf][w + 2][lane * V + v];
-                    out.v[v] = (i == 0 || i >= nx - 1)
-                                   ? T(0)
-                                   : update3<T>(cur.v[v], we, ea, so, no, prev.v[v], next.v[v],
-                                                alpha);
+                    const bool face = i == 0 || i >= nx - 1;
+                    T val;
+                    if constexpr (sizeof(T) == 8) {
+                        // v is a constant in each unrolled copy
+                        if (V == 2 && v == 0)
+                            val = update3_fp64<1>(cur.v[v], we, ea, so, no, prev.v[v], next.v[v],
+                                                  alpha, face);
+                        else if (V == 2)
+                            val = update3_fp64<0>(cur.v[v], we, ea, so, no, prev.v[v], next.v[v],
+                                                  alpha, face);
+                        else
+                            val = update3_fp64<-1>(cur.v[v], we, ea, so, no, prev.v[v],
+                                                   next.v[v], alpha, face);
+                    } else {
+                        val = update3<T>(cur.v[v], we, ea, so, no, prev.v[v], next.v[v], alpha);
+                    }
+                    out.v[v] = face ? T(0) : val;
                 }
             }
             store_row<T, V>(dst + j * nx + k * sxy, x0, lane, nx, out, j * nx + k * sxy, total);

@@ -287,7 +287,8 @@ FVF_HD uint64_t frame_add(uint64_t frame, uint32_t hi, uint32_t lo, uint32_t pw)
 }
 
 FVF_HD uint64_t round53_frame(uint64_t S) {
-    const uint32_t p = 11u - (uint32_t)clz32((uint32_t)(S >> 32));  // 1..11
+    // 1..11 (0 only for a single operand at s = 0, which the caller declines)
+    const uint32_t p = 11u - (uint32_t)clz32((uint32_t)(S >> 32));
     const uint32_t unit = 1u << p;
     const uint32_t lsb = ((uint32_t)S >> p) & 1u;
     // p <= 11, so the cleared bits lie in the low word: a 32-bit mask (a
@@ -296,19 +297,41 @@ FVF_HD uint64_t round53_frame(uint64_t S) {
     return (S + ((unit >> 1) - 1u + lsb)) & ~(uint64_t)(unit - 1u);
 }
 
+// True for +0 and -0.
+FVF_HD bool is_zero_bits(uint64_t x) {
+    return (((uint32_t)(x >> 32) & 0x7FFFFFFFu) | (uint32_t)x) == 0u;
+}
+
 // The sum of N operands of one sign in order, (((X0 + X1) + X2) + ...), in
 // one frame.  SH is the largest operand shift: 9 for up to four operands
 // (sum < 4 * 2^62 = 2^64), 8 for up to eight (sum < 8 * 2^61); the spread
 // limit is SH binades and the smallest accepted largest exponent SH + 1.
 // The rounding bound above holds for each: every exact partial sum is at
 // most N * (2^(53+SH) - 2^SH) and each rounding adds less than 2^11.
-template <int N>
+//
+// ZSLOT (0 or 1; -1 for none) names one operand of the first pair that may
+// be +0 or -0.  X0 + X1 is then the other operand exactly (whatever the
+// zero's sign, when the other is not zero), so the zero enters the frame
+// with weight 0 and takes its partner's high word for the largest exponent
+// (and, at the caller, for the sign test).  The first partial sum is then a
+// single operand, leading one at bit 52 + s: the rounding that follows needs
+// s >= 1 (p >= 1) and leaves such a value unchanged, so the zero's shift is
+// counted as its partner's minus one, which wraps below zero (declines) when
+// the partner sits at s = 0.  Used for the cells next to a zero boundary
+// face, whose face-side neighbour is the zero.
+template <int N, int ZSLOT = -1>
 FVF_HD bool sum_one_sign_fast(const uint64_t (&X)[N], uint64_t *out) {
     static_assert(N >= 2 && N <= 8, "frame sized for 2..8 operands");
+    static_assert(ZSLOT >= -1 && ZSLOT <= 1, "a zero is tolerated in operand 0 or 1 only");
     constexpr uint32_t SH = N <= 4 ? 9u : 8u;
     uint32_t h[N];
 #pragma unroll
     for (int q = 0; q < N; ++q) h[q] = (uint32_t)(X[q] >> 32);
+    bool zero = false;
+    if constexpr (ZSLOT >= 0) {
+        zero = is_zero_bits(X[ZSLOT]);
+        if (zero) h[ZSLOT] = h[1 - ZSLOT];
+    }
     uint32_t hmax = h[0];
 #pragma unroll
     for (int q = 1; q < N; ++q) hmax = hmax > h[q] ? hmax : h[q];
@@ -316,9 +339,10 @@ FVF_HD bool sum_one_sign_fast(const uint64_t (&X)[N], uint64_t *out) {
     uint32_t pw[N], any = 0;
 #pragma unroll
     for (int q = 0; q < N; ++q) {
-        const uint32_t sq = (h[q] >> 20) - top + SH;  // [0, SH] or wrapped below 0
+        uint32_t sq = (h[q] >> 20) - top + SH;       // [0, SH] or wrapped below 0
+        if (q == ZSLOT) sq -= (uint32_t)zero;
         any |= sq;
-        pw[q] = 1u << (sq & 15u);
+        pw[q] = (q == ZSLOT && zero) ? 0u : 1u << (sq & 15u);
     }
     const bool ok = any < 16u && (hmax & 0x7FFFFFFFu) - ((SH + 1u) << 20) <
                                      0x7FC00000u - ((SH + 1u) << 20);
@@ -334,20 +358,33 @@ FVF_HD bool sum_one_sign_fast(const uint64_t (&X)[N], uint64_t *out) {
 }
 
 // The four-operand form written out: the same arithmetic as
-// sum_one_sign_fast<4> (the host check compares both with the CPU), in the
-// form measured on GB300; the template instantiated for four operands made
-// the 2D FP64 step 11% slower (0.452 against 0.408 ms per 8192^2 step).
+// sum_one_sign_fast<4, ZSLOT> (the host check compares both with the CPU),
+// in the form measured on GB300; the template instantiated for four
+// operands made the 2D FP64 step 11% slower (0.452 against 0.408 ms per
+// 8192^2 step).
+template <int ZSLOT = -1>
 FVF_HD bool sum4_one_sign_fast(uint64_t A, uint64_t B, uint64_t C, uint64_t D, uint64_t *out) {
-    const uint32_t ah = (uint32_t)(A >> 32), bh = (uint32_t)(B >> 32);
+    static_assert(ZSLOT >= -1 && ZSLOT <= 1, "a zero is tolerated in operand 0 or 1 only");
+    uint32_t ah = (uint32_t)(A >> 32), bh = (uint32_t)(B >> 32);
     const uint32_t ch = (uint32_t)(C >> 32), dh = (uint32_t)(D >> 32);
+    bool zero = false;
+    if constexpr (ZSLOT == 0) {
+        zero = is_zero_bits(A);
+        if (zero) ah = bh;
+    } else if constexpr (ZSLOT == 1) {
+        zero = is_zero_bits(B);
+        if (zero) bh = ah;
+    }
     const uint32_t m1 = ah > bh ? ah : bh, m2 = ch > dh ? ch : dh, hmax = m1 > m2 ? m1 : m2;
     const uint32_t top = hmax >> 20;                 // sign and largest exponent
-    const uint32_t sa = (ah >> 20) - top + 9u, sb = (bh >> 20) - top + 9u;
+    const uint32_t sa = (ah >> 20) - top + 9u - (uint32_t)(ZSLOT == 0 && zero);
+    const uint32_t sb = (bh >> 20) - top + 9u - (uint32_t)(ZSLOT == 1 && zero);
     const uint32_t sc = (ch >> 20) - top + 9u, sd = (dh >> 20) - top + 9u;
     const bool ok = (sa | sb | sc | sd) < 16u &&
                     (hmax & 0x7FFFFFFFu) - 0x00A00000u < 0x7FC00000u - 0x00A00000u;
-    uint64_t s = frame_add(frame_add(0, ah, (uint32_t)A, 1u << (sa & 15u)), bh, (uint32_t)B,
-                           1u << (sb & 15u));
+    const uint32_t pa = (ZSLOT == 0 && zero) ? 0u : 1u << (sa & 15u);
+    const uint32_t pb = (ZSLOT == 1 && zero) ? 0u : 1u << (sb & 15u);
+    uint64_t s = frame_add(frame_add(0, ah, (uint32_t)A, pa), bh, (uint32_t)B, pb);
     s = round53_frame(s);
     s = round53_frame(frame_add(s, ch, (uint32_t)C, 1u << (sc & 15u)));
     s = round53_frame(frame_add(s, dh, (uint32_t)D, 1u << (sd & 15u)));

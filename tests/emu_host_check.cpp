@@ -2,8 +2,10 @@
 // (fp64_emu.cuh): every sum and product must be bit-identical to the host
 // CPU's IEEE 754 operation (round to nearest even), and so must the
 // fixed-point sum of four operands, ((a + b) + c) + d, wherever its fast
-// form accepts the operands.  Built with -O2 -ffp-contract=off; prints
-// "mismatches N cases M sum4_taken T".
+// form accepts the operands, and the six-operand sum of the 3D update with
+// and without a zero in its first pair (and the four-operand sum with such
+// a zero).  Built with -O2 -ffp-contract=off; prints "mismatches N cases M
+// sum4_taken T sum6_taken U sum6z_taken Z sum4z_taken Y".
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -115,6 +117,123 @@ static void check_sum6(const uint64_t (&X)[6]) {
     }
 }
 
+static uint64_t make(uint64_t sign, uint64_t exp, uint64_t frac) {
+    return (sign << 63) | ((exp & 0x7FF) << 52) | (frac & kFrac);
+}
+
+static uint64_t sum6z_taken = 0;
+
+// The same sum with a zero tolerated in operand ZSLOT (0 or 1): the caller's
+// sign test takes the partner's sign for a zero there.  Where the form
+// accepts a set without a zero in the slot it must also agree with the
+// plain form.
+template <int ZSLOT>
+static void check_sum6_zero_slot(const uint64_t (&X)[6]) {
+    uint64_t h[6];
+    for (int q = 0; q < 6; ++q) h[q] = X[q];
+    if (is_zero_bits(X[ZSLOT])) h[ZSLOT] = X[1 - ZSLOT];
+    for (int q = 1; q < 6; ++q)
+        if ((h[q] ^ h[0]) & kSign) return;
+    uint64_t got;
+    if (!sum_one_sign_fast<6, ZSLOT>(X, &got)) return;
+    ++cases;
+    if (is_zero_bits(X[ZSLOT])) ++sum6z_taken;
+    double want = from_bits(X[0]);
+    for (int q = 1; q < 6; ++q) want = native_add(want, from_bits(X[q]));
+    if (got != bits(want)) {
+        if (mismatches < 10)
+            std::printf("sum6 zero slot %d %016llx %016llx ... %016llx: got %016llx want %016llx\n", ZSLOT,
+                        (unsigned long long)X[0], (unsigned long long)X[1], (unsigned long long)X[5],
+                        (unsigned long long)got, (unsigned long long)bits(want));
+        ++mismatches;
+    }
+}
+
+static uint64_t sum4z_taken = 0;
+
+// The four-operand forms with a zero tolerated in operand ZSLOT: the
+// written-out form and the template must agree on acceptance and value.
+template <int ZSLOT>
+static void check_sum4_zero_slot(const uint64_t (&X)[6]) {
+    uint64_t h[4];
+    for (int q = 0; q < 4; ++q) h[q] = X[q];
+    if (is_zero_bits(X[ZSLOT])) h[ZSLOT] = X[1 - ZSLOT];
+    for (int q = 1; q < 4; ++q)
+        if ((h[q] ^ h[0]) & kSign) return;
+    const uint64_t Y[4] = {X[0], X[1], X[2], X[3]};
+    uint64_t got, tgot;
+    const bool ok = sum4_one_sign_fast<ZSLOT>(X[0], X[1], X[2], X[3], &got);
+    const bool tok = sum_one_sign_fast<4, ZSLOT>(Y, &tgot);
+    if (ok != tok || (ok && got != tgot)) {
+        if (mismatches < 10) std::printf("sum4 zero-slot forms disagree\n");
+        ++mismatches;
+    }
+    if (!ok) return;
+    ++cases;
+    if (is_zero_bits(X[ZSLOT])) ++sum4z_taken;
+    const double want = native_add(native_add(native_add(from_bits(X[0]), from_bits(X[1])), from_bits(X[2])),
+                                   from_bits(X[3]));
+    if (got != bits(want)) {
+        if (mismatches < 10)
+            std::printf("sum4 zero slot %d %016llx %016llx %016llx %016llx: got %016llx want %016llx\n", ZSLOT,
+                        (unsigned long long)X[0], (unsigned long long)X[1], (unsigned long long)X[2],
+                        (unsigned long long)X[3], (unsigned long long)got, (unsigned long long)bits(want));
+        ++mismatches;
+    }
+}
+
+template <int ZSLOT>
+static void check_zero_slot(const uint64_t (&X)[6]) {
+    check_sum6_zero_slot<ZSLOT>(X);
+    check_sum4_zero_slot<ZSLOT>(X);
+}
+
+// Sets for the zero-slot forms (four operands: the first four of each set): the slot set to +0 or -0 and its partner
+// at every shift the frame can give it (including s = 0, which the form
+// must decline, and beyond), zero or subnormal partners, a partner of the
+// other sign, smoothed-field values with a zero face neighbour, equal
+// values and ties, and largest exponents near both limits.
+template <int ZSLOT>
+static void zero_slot_cases(long n) {
+    constexpr int P = 1 - ZSLOT;
+    for (long i = 0; i < n; ++i) {
+        uint64_t X[6];
+        const uint64_t sg = next_u64() & 1, e0 = 1 + next_u64() % 2046;
+        const int spread = (int)(next_u64() % 11);
+        for (auto &x : X) {
+            int64_t e = (int64_t)e0 - (int64_t)(next_u64() % (spread + 1));
+            e = e < 0 ? 0 : e;
+            const uint64_t f = (next_u64() & 1) ? next_u64() : next_u64() & ~((1ull << (next_u64() % 53)) - 1);
+            x = make(sg, (uint64_t)e, f);
+        }
+        check_zero_slot<ZSLOT>(X);
+        X[ZSLOT] = make(next_u64() & 1, 0, 0);
+        check_zero_slot<ZSLOT>(X);
+        X[2] = make(sg, e0, next_u64());
+        for (uint64_t below = 6; below <= 11; ++below) {
+            X[P] = make(sg, e0 >= below ? e0 - below : 0, next_u64());
+            check_zero_slot<ZSLOT>(X);
+        }
+        X[P] = make(next_u64() & 1, 0, (next_u64() & 1) ? 0 : next_u64());
+        check_zero_slot<ZSLOT>(X);
+        X[P] = make(sg ^ 1, e0, next_u64());
+        check_zero_slot<ZSLOT>(X);
+        for (auto &x : X) x = bits((double)(next_u64() >> 11) * 0x1p-53);
+        X[ZSLOT] = 0;
+        check_zero_slot<ZSLOT>(X);
+        const uint64_t t = make(sg, 1 + next_u64() % 2046, (next_u64() & 1) ? kFrac : (next_u64() & 0xFFF0000000000ull));
+        for (auto &x : X) x = t;
+        X[ZSLOT] = make(next_u64() & 1, 0, 0);
+        check_zero_slot<ZSLOT>(X);
+        for (auto &x : X) x = make(sg, e0 + next_u64() % 2, (next_u64() & 1) ? 1 : (1ull << 51) | 1);
+        X[ZSLOT] = make(sg, 0, 0);
+        check_zero_slot<ZSLOT>(X);
+        for (auto &x : X) x = make(sg, (next_u64() & 1) ? 2037 + next_u64() % 10 : 5 + next_u64() % 10, next_u64());
+        X[ZSLOT] = make(sg, 0, 0);
+        check_zero_slot<ZSLOT>(X);
+    }
+}
+
 static void check(uint64_t A, uint64_t B) {
     const double a = from_bits(A), b = from_bits(B);
     const uint64_t want = bits(native_add(a, b));
@@ -158,9 +277,6 @@ static void check(uint64_t A, uint64_t B) {
     }
 }
 
-static uint64_t make(uint64_t sign, uint64_t exp, uint64_t frac) {
-    return (sign << 63) | ((exp & 0x7FF) << 52) | (frac & kFrac);
-}
 
 int main(int argc, char **argv) {
     const long n = argc > 1 ? std::atol(argv[1]) : 1000000;
@@ -322,7 +438,11 @@ int main(int argc, char **argv) {
         }
         check_sum6(X);
     }
-    std::printf("mismatches %llu cases %llu sum4_taken %llu sum6_taken %llu\n", (unsigned long long)mismatches,
-                (unsigned long long)cases, (unsigned long long)sum4_taken, (unsigned long long)sum6_taken);
+    // six-operand sums with a zero tolerated in the first or second slot
+    zero_slot_cases<0>(n / 2);
+    zero_slot_cases<1>(n / 2);
+    std::printf("mismatches %llu cases %llu sum4_taken %llu sum6_taken %llu sum6z_taken %llu sum4z_taken %llu\n",
+                (unsigned long long)mismatches, (unsigned long long)cases, (unsigned long long)sum4_taken,
+                (unsigned long long)sum6_taken, (unsigned long long)sum6z_taken, (unsigned long long)sum4z_taken);
     return mismatches != 0;
 }

@@ -11,8 +11,14 @@ the fixed-point sum of four same-sign operands, ((a + b) + c) + d, on every
 case its fast form accepts (about 5 million: spreads up to the 9-binade
 limit, ties in each partial sum, all-ones significands, sums near
 overflow, the diffusion's own value ranges; the written-out form and the
-N-operand template must agree), and the six-operand frame of the 3D update
-on about 3.8 million accepted sets."""
+N-operand template must agree), the six-operand frame of the 3D update on
+about 3.8 million accepted sets, and its forms that take a zero in the first
+or second operand (the face-side neighbour of the cells next to a zero
+face) on about 5.8 million accepted sets with that zero (and the four-operand
+forms of the 2D update with such a zero, written-out and template, on about
+7 million): partners at every
+shift including the one the form must decline, zero and subnormal partners,
+both zero signs, ties, and exponents near both limits."""
 from __future__ import annotations
 
 import re
@@ -39,3 +45,7 @@ def test_emulated_add_and_mul_match_ieee(tmp_path):
     assert taken > 4_000_000, r.stdout
     taken6 = int(re.search(r"sum6_taken (\d+)", r.stdout).group(1))
     assert taken6 > 3_000_000, r.stdout
+    taken6z = int(re.search(r"sum6z_taken (\d+)", r.stdout).group(1))
+    assert taken6z > 5_000_000, r.stdout
+    taken4z = int(re.search(r"sum4z_taken (\d+)", r.stdout).group(1))
+    assert taken4z > 6_000_000, r.stdout

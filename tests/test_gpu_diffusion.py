@@ -264,6 +264,56 @@ def test_fixed_point_sum_boundaries(nx, ny):
         assert_bits_equal(gv, ov, nan_payloads=False, what=f"v {nx}x{ny} {steps}")
 
 
+def _zero_slot_field(nx, ny, seed, sh=9):
+    """FP64 field in bands of 4 rows for the zero-tolerant neighbour sum of
+    the cells next to the x edges: positive rows with +0 edges, negative rows
+    with +0 edges, positive rows with -0 edges, rows whose columns 2 and
+    nx-3 (the zero's partner in the sum of columns 1 and nx-2) lie sh-1, sh
+    and sh+1 binades below their neighbours (the form must take the first
+    and decline the others), rows with +0 and -0 scattered inside, the same
+    with mixed signs, and rows with nonzero edge values."""
+    b = inputs.random_bits(seed, 5, 3 * nx * ny).reshape(3, ny, nx)
+    u0 = 0.5 + (b[0] >> np.uint64(11)).astype(np.float64) * 2.0 ** -54    # [0.5, 1)
+    mode = (np.arange(ny) // 4) % 7
+    zeros = (b[1] % np.uint64(7)) == 0
+    neg = (b[2] & np.uint64(1)).astype(bool)
+    for j in range(ny):
+        m = mode[j]
+        if m == 1:
+            u0[j] = -u0[j]
+        elif m == 3:
+            k = (sh - 1) + j % 3
+            u0[j, 2] *= 2.0 ** -k
+            u0[j, nx - 3] *= 2.0 ** -k
+        elif m in (4, 5):
+            if m == 5:
+                u0[j, neg[j]] = -u0[j, neg[j]]
+            z = zeros[j]
+            u0[j, z] = np.where(neg[j, z], -0.0, 0.0)
+    edge = np.where(mode == 2, -0.0, 0.0)
+    keep = mode == 6
+    u0[~keep, 0] = edge[~keep]
+    u0[~keep, nx - 1] = edge[~keep]
+    u0[0, :] = u0[-1, :] = 0.0
+    return u0
+
+
+@pytest.mark.parametrize("nx,ny", [(1024, 60), (1030, 33), (258, 140)])
+def test_zero_neighbour_slots(nx, ny):
+    """FP64 march kernel on fields that exercise the zero-tolerant neighbour
+    sum of the column blocks holding an x edge and the edge cells that skip
+    the fallback: +0 and -0 edges, negative fields, zero partners' binade
+    limit, scattered zeros of both signs; 1 and 2 steps, both buffers
+    bit-exact."""
+    torch = torch_cuda()
+    u0 = _zero_slot_field(nx, ny, 61)
+    for steps in (1, 2):
+        gu, gv = _run_gpu(torch, u0, steps)
+        ou, ov, _ = oracle.diffuse2d(u0, steps, return_both=True)
+        assert_bits_equal(gu, ou, what=f"u {nx}x{ny} {steps}")
+        assert_bits_equal(gv, ov, what=f"v {nx}x{ny} {steps}")
+
+
 @pytest.mark.parametrize("alpha", [0.25, 1.0 / 3.0, 0.0, 1e-300, 0.1 + 2.0 ** -50])
 def test_march_alpha_values(alpha):
     """FP64 march kernel (1024 x 48, above the cluster kernel's size) with

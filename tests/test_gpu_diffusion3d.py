@@ -108,6 +108,54 @@ def test_fixed_point_sum_boundaries(shape):
         assert_bits_equal(gv, ov, nan_payloads=False, what=f"v {shape} {steps}")
 
 
+def _zero_slot_field_3d(shape, seed):
+    """FP64 3D field in slabs of 2 planes for the zero-tolerant neighbour sum
+    of the cells next to the x faces: positive with +0 faces, negative with
+    +0 faces, -0 faces, the zero's partner (columns 2 and nx-3) 7, 8 and 9
+    binades below the other neighbours (taken, declined, declined), +0 and
+    -0 scattered inside, the same with mixed signs, nonzero x-face values."""
+    nz, ny, nx = shape
+    n = nz * ny * nx
+    b = inputs.random_bits(seed, 6, 3 * n).reshape(3, nz, ny, nx)
+    u0 = 0.5 + (b[0] >> np.uint64(11)).astype(np.float64) * 2.0 ** -54
+    zeros = (b[1] % np.uint64(7)) == 0
+    neg = (b[2] & np.uint64(1)).astype(bool)
+    for k in range(nz):
+        m = (k // 2) % 7
+        if m == 1:
+            u0[k] = -u0[k]
+        elif m == 3:
+            for j in range(ny):
+                s = 7 + j % 3
+                u0[k, j, 2] *= 2.0 ** -s
+                u0[k, j, nx - 3] *= 2.0 ** -s
+        elif m in (4, 5):
+            if m == 5:
+                u0[k][neg[k]] = -u0[k][neg[k]]
+            z = zeros[k]
+            u0[k][z] = np.where(neg[k][z], -0.0, 0.0)
+        if m != 6:
+            u0[k, :, 0] = u0[k, :, nx - 1] = -0.0 if m == 2 else 0.0
+    u0[0], u0[-1] = 0, 0
+    u0[:, 0], u0[:, -1] = 0, 0
+    return u0
+
+
+@pytest.mark.parametrize("shape", [(28, 10, 130), (15, 7, 200), (14, 5, 64)])
+def test_zero_neighbour_slots(shape):
+    """FP64 march kernel on fields that exercise the zero-tolerant W/E slot
+    of the six-operand sum and the face cells that skip the fallback: +0 and
+    -0 faces, negative fields, the partner's binade limit, scattered zeros
+    of both signs; 1 and 2 steps, both buffers bit-exact."""
+    torch = torch_cuda()
+    u0 = _zero_slot_field_3d(shape, 63)
+    for steps in (1, 2):
+        gu, gv = _run(torch, u0, steps)
+        ou, ov, _ = oracle.diffuse3d(u0, steps, 0.1, return_both=True)
+        assert_bits_equal(gu, ou, what=f"u {shape} {steps}")
+        assert_bits_equal(gv, ov, what=f"v {shape} {steps}")
+
+
 @pytest.mark.parametrize("alpha", [1.0 / 6.0, 0.25, 0.0, 1e-300])
 def test_fp64_alpha_values(alpha):
     """FP64 register kernel with alpha at the 3D stability limit (1/6),
