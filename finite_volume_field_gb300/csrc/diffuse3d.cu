@@ -11,8 +11,8 @@
 // even on its own in the order written; 6c is its own rounded product (6c is
 // not a power-of-two scaling, so no fused form is exact here).
 //
-// Kernels (both march along k; a block of kTY warps owns a tile of 32*V
-// cells along i by kTY rows along j, V = 4 FP32 or 2 FP64 cells per lane).
+// Kernels (both march along k; a block of warps owns a tile of 32*V cells
+// along i by one row along j per warp, V = 4 FP32 or 2 FP64 cells per lane).
 //   bulk   (FP32, rows 16-byte aligned: nx a multiple of 4, 16-byte
 //          buffers): the tile is 2*kTY rows (each warp computes two rows).
 //          One thread streams whole planes of the tile into a ring of
@@ -218,29 +218,37 @@ __device__ __forceinline__ void store_vec(T *p, const Vec<T, V> &x) {
     }
 }
 
-// FP64: at most 64 registers, 4 blocks of 256 threads per SM (1.56 against
-// 1.67 ms per 512^3 step at 74 registers and 3 blocks; 5 blocks spill).
+// Rows (warps) per block of the register march kernel.  FP64: 4, at most 64
+// registers, 8 blocks of 128 threads per SM.  Per 512^3 FP64 step on GB300,
+// runs of 16 planes: 1.405 ms with 4 rows, against 1.422 with 2, 1.484 with
+// 6, 1.492 with 8 and 1.740 with 16 (1024 threads per SM in each; 8 rows
+// with 74 registers and 3 blocks measured 1.67 against 1.56 ms capped, and
+// 5 blocks spill).  FP32 (rows that are not 16-byte aligned): 8.
+template <typename T>
+__host__ __device__ constexpr int march3_rows() { return sizeof(T) == 8 ? 4 : kTY; }
+
 // Every block takes the zero slots: taking them only in the blocks that
 // hold an x face (a block-uniform branch between two copies of the loop)
 // spilled at the 64-register cap and measured 3% slower (1.529 against
 // 1.483 ms per step).
 template <typename T, int V>
-__global__ void __launch_bounds__(32 * kTY, sizeof(T) == 8 ? 4 : 0)
+__global__ void __launch_bounds__(32 * march3_rows<T>(), sizeof(T) == 8 ? 8 : 0)
 diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                  int64_t nz, T alpha, int64_t kz_len) {
-    __shared__ T rows[2][kTY + 2][32 * V];
+    constexpr int kR = march3_rows<T>();
+    __shared__ T rows[2][kR + 2][32 * V];
     const int lane = threadIdx.x, w = threadIdx.y;
     const int64_t x0 = (int64_t)blockIdx.x * (32 * V);
-    const int64_t j0 = (int64_t)blockIdx.y * kTY;
+    const int64_t j0 = (int64_t)blockIdx.y * kR;
     const int64_t j = j0 + w;
     const int64_t kz0 = (int64_t)blockIdx.z * kz_len;
     const int64_t kz1 = kz0 + kz_len < nz ? kz0 + kz_len : nz;
     const int64_t sxy = nx * ny;
     const bool rowok = j < ny;
-    // halo rows of the tile: warp 0 also carries row j0-1, warp kTY-1 row j0+kTY
-    const int64_t jh = w == 0 ? j0 - 1 : j0 + kTY;
-    const bool hok = (w == 0 || w == kTY - 1) && jh >= 0 && jh < ny;
-    const int hslot = w == 0 ? 0 : kTY + 1;
+    // halo rows of the tile: warp 0 also carries row j0-1, warp kR-1 row j0+kR
+    const int64_t jh = w == 0 ? j0 - 1 : j0 + kR;
+    const bool hok = (w == 0 || w == kR - 1) && jh >= 0 && jh < ny;
+    const int hslot = w == 0 ? 0 : kR + 1;
     const int64_t klast = kz1 < nz ? kz1 : nz - 1;  // last plane this block reads
 
     Vec<T, V> prev, cur, next, nn, hcur, hnext, hnn;
@@ -614,7 +622,8 @@ template <typename T, int V>
 cudaError_t launch_typed(const T *src, T *dst, int64_t nx, int64_t ny, int64_t nz, T alpha,
                          cudaStream_t stream) {
     const int64_t gx = (nx + 32 * V - 1) / (32 * V);
-    const int64_t gy = (ny + kTY - 1) / kTY;
+    constexpr int kR = march3_rows<T>();
+    const int64_t gy = (ny + kR - 1) / kR;
     if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidValue;
     int64_t kz_len;
     if (sizeof(T) == 8) {
@@ -635,7 +644,7 @@ cudaError_t launch_typed(const T *src, T *dst, int64_t nx, int64_t ny, int64_t n
     }
     const int64_t gz = (nz + kz_len - 1) / kz_len;
     if (gz > 65535) return cudaErrorInvalidValue;
-    diffuse3d_kernel<T, V><<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), dim3(32, kTY), 0,
+    diffuse3d_kernel<T, V><<<dim3((unsigned)gx, (unsigned)gy, (unsigned)gz), dim3(32, kR), 0,
                              stream>>>(src, dst, nx, ny, nz, alpha, kz_len);
     return cudaSuccess;
 }
