@@ -24,7 +24,8 @@
 //          warp shuffle; the two warp-edge lanes load their outside
 //          neighbour together with the row.  FP32: the grid is one wave, as
 //          many blocks as fit on the SMs at once, each taking an equal band
-//          of rows; FP64: bands of 12 rows (many waves, see kMarchF64Rows).
+//          of rows; FP64: bands of 24 rows of 64-thread blocks (many waves,
+//          see kMarchF64Rows).
 //   scalar (any size or alignment): one thread per cell.
 //   blocked (FP32, nsteps >= 3): up to 8 steps per launch in shared memory.
 //   cluster (grids of up to 32K cells, nsteps >= 2): all steps in one
@@ -266,7 +267,11 @@ __device__ __forceinline__ void store16(T *p, const Vec16<T> &r) {
     }
 }
 
-constexpr int kMarchThreads = 128;
+// Threads per block: FP32 128; FP64 64 (per 8192^2 FP64 step on GB300,
+// with bands of 24 rows: 0.4018 ms, against 0.4037 with 128 threads and
+// 12 rows, 0.4076 with 256 or with 32 threads).
+template <typename T>
+__host__ __device__ constexpr int march_threads() { return sizeof(T) == 8 ? 64 : 128; }
 
 // One row of a thread's strip: the vector plus the two scalar neighbours
 // that lanes 0 and 31 fetch for the warp (unused in other lanes).
@@ -306,8 +311,9 @@ __device__ __forceinline__ MarchRow<T> march_load(const T *__restrict__ src, int
 // 0.413, 0.415 and 0.419 ms (no register cap; a 40-register cap for 12
 // blocks per SM measured 0.416 ms at 12 rows).  With the zero slots and the
 // edge cells kept off the fallback (march_rows), bands of 12 and 24 rows
-// measure within 0.2% of each other and one wave is still 14% slower.
-constexpr int kMarchF64Rows = 12;
+// measure within 0.2% of each other and one wave is still 14% slower; with
+// 64-thread blocks 24 rows measured 0.4018 ms against 0.4034 for 12.
+constexpr int kMarchF64Rows = 24;
 // The rows of one band.  ZX: the block holds an x edge, and its frame sums
 // take the zero slots (the other blocks skip the zero tests, whose integer
 // instructions measured more than the edge warps' fallback calls cost: on
@@ -319,7 +325,7 @@ __device__ __forceinline__ void march_rows(const T *__restrict__ src, T *__restr
                                            T alpha) {
     constexpr int V = Vec16<T>::n;
     const int lane = threadIdx.x & 31;
-    const int64_t col = ((int64_t)blockIdx.x * kMarchThreads + threadIdx.x) * V;
+    const int64_t col = ((int64_t)blockIdx.x * march_threads<T>() + threadIdx.x) * V;
     const bool active = col < nx;
     const int64_t j0 = (int64_t)blockIdx.y * rows_per_block;
     const int64_t j1 = min(j0 + rows_per_block, ny);
@@ -380,7 +386,7 @@ __device__ __forceinline__ void march_rows(const T *__restrict__ src, T *__restr
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kMarchThreads)
+__global__ void __launch_bounds__(march_threads<T>())
 diffuse_march_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                      int64_t rows_per_block, T alpha) {
     // block-uniform: the first and last column blocks hold the x edges
@@ -398,7 +404,7 @@ int march_blocks_per_sm() {
     int n = cached[d].load(std::memory_order_relaxed);
     if (n == 0) {
         const cudaError_t st = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, diffuse_march_kernel<T>, kMarchThreads, 0);
+            &n, diffuse_march_kernel<T>, march_threads<T>(), 0);
         if (st != cudaSuccess) cudaGetLastError();   // this query's own error only
         if (st != cudaSuccess || n <= 0) n = 8;
         cached[d].store(n, std::memory_order_relaxed);
@@ -798,7 +804,8 @@ struct SingleStep {
         vec_ok = (nx % V == 0) && ((uintptr_t)u % 16 == 0) && ((uintptr_t)v % 16 == 0) &&
                  nx >= 2 * V;
         if (vec_ok) {
-            const int64_t bx = (nx / V + kMarchThreads - 1) / kMarchThreads;
+            constexpr int kThreads = march_threads<T>();
+            const int64_t bx = (nx / V + kThreads - 1) / kThreads;
             int64_t by;
             if (sizeof(T) == 8) {
                 // bands of kMarchF64Rows rows (more where the grid's y
@@ -816,7 +823,7 @@ struct SingleStep {
             by = (ny + rows - 1) / rows;
             if (bx > 0x7fffffff || by > 65535) return cudaErrorInvalidValue;
             grid = dim3((unsigned)bx, (unsigned)by);
-            block = dim3(kMarchThreads);
+            block = dim3(kThreads);
         } else {
             const int64_t gy = (ny + kBy - 1) / kBy;
             grid = dim3((unsigned)((nx + kBx - 1) / kBx), (unsigned)(gy < 65535 ? gy : 65535));

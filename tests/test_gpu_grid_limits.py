@@ -62,9 +62,9 @@ def test_pack_copy_x_more_planes_than_grid_rows():
 
 
 def test_diffusion_fp64_bands_beyond_grid_rows():
-    """16 x 800010: ny / 12 > 65535, so the bands take 13 rows."""
+    """16 x 1600020: ny / 24 > 65535, so the bands take 25 rows."""
     torch = torch_cuda()
-    nx, ny = 16, 800010
+    nx, ny = 16, 1600020
     u0 = inputs.diffusion_field(nx, ny, np.float64, seed=inputs.config_seed(2), stream=7)
     for steps in (1, 2):
         u = to_dev(u0)
