@@ -35,20 +35,30 @@ namespace {
 constexpr int kMulMask = 7;
 constexpr int kMulMaskAcc = 15;
 
+// Threads per block, per form, as measured on GB300 at 8 x 201^3 and
+// 4800 x 1200 x 7 (one box, back to back): the assigning FP64 form at 128
+// (2-3.5% faster than 256 in every direction; 64 is slower in y), the
+// accumulating FP64 form at 64 (2-10% faster than 256, 1-2% than 128), the
+// FP32 form at 256 (within 1% of 64 and 128).
+template <bool ACC, typename T>
+__host__ __device__ constexpr int threads_of() {
+    return sizeof(T) == 4 ? 256 : (ACC ? 64 : 128);
+}
+
 // Minimum resident blocks per SM, per form (a register cap; 0 = none), as
-// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7: the FP32 form at 6
-// (more loads in flight for 4-byte elements: 0.099 ms at 4 blocks, 0.093 ms
-// at 6, 0.146 ms at 8, timed back to back), the assigning FP64 y form at 6
-// (5-7% faster despite a few spilled registers) and the accumulating one at
-// 5 (7%).  The other FP64 forms take none: a cap there
+// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7 with 256-thread
+// blocks, and kept at the same threads per SM for the smaller blocks: the
+// FP32 form at 6 (more loads in flight for 4-byte elements: 0.099 ms at 4
+// blocks, 0.093 ms at 6, 0.146 ms at 8, timed back to back), the assigning
+// FP64 y form at 6 (5-7% faster despite a few spilled registers) and the
+// accumulating one at 5 (7%).  The other FP64 forms take none: a cap there
 // measured 5-13% slower, and even a minimum of 1 changes the compiler's
 // register allocation (48 -> 64-84 registers, 9-43% slower).
 template <int DIR, bool ACC, typename T>
 constexpr int min_blocks() {
-    return sizeof(T) == 4 ? 6 : (DIR == 1 ? (ACC ? 5 : 6) : 0);
+    return (sizeof(T) == 4 ? 6 : (DIR == 1 ? (ACC ? 5 : 6) : 0)) * 256 / threads_of<ACC, T>();
 }
 
-constexpr int kThreads = 256;
 // variables per load batch: 4 FP64 or 8 FP32, 64 bytes of face loads each
 template <typename T>
 __host__ __device__ constexpr int group_of() { return sizeof(T) == 4 ? 8 : 4; }
@@ -94,12 +104,12 @@ __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, 
 // has a cell whatever n1 is: the kernel is bound by the FP64 unit, which
 // charges idle lanes.
 template <int DIR, bool ACC, typename Idx, typename Off, typename T>
-__global__ void __launch_bounds__(kThreads, min_blocks<DIR, ACC, T>())
+__global__ void __launch_bounds__(threads_of<ACC, T>(), min_blocks<DIR, ACC, T>())
 advect_rhs_kernel(const T *__restrict__ flux, const T *__restrict__ inv_d, int nv,
                   int64_t n1_, int64_t n2_, int64_t n3_, T *__restrict__ rhs) {
     const Idx n1 = (Idx)n1_, n2 = (Idx)n2_;
     const Idx plane = n1 * n2;
-    const Idx jk = (Idx)blockIdx.x * kThreads + threadIdx.x;
+    const Idx jk = (Idx)blockIdx.x * threads_of<ACC, T>() + threadIdx.x;
     if (jk >= plane) return;
     const Idx k = jk / n1, j = jk - k * n1;
     // flat offsets in Off: 32-bit when every element index of both arrays
@@ -178,6 +188,7 @@ template <int DIR, bool ACC, typename T>
 void launch_typed(const T *flux, const T *inv_d, int nv, const int64_t n[3], T *rhs,
                   cudaStream_t stream) {
     const int64_t plane = n[0] * n[1];
+    constexpr int kThreads = threads_of<ACC, T>();
     const dim3 grid((unsigned)((plane + kThreads - 1) / kThreads),
                     (unsigned)(n[2] < 65535 ? n[2] : 65535));
     // 32-bit (j, k) arithmetic while the plane index fits, and, for the
@@ -219,7 +230,8 @@ FVF_BOUNDS_READER(read_bounds_rhs)
 cudaError_t launch_advect_rhs(const void *flux, const void *inv_d, int nv, const int64_t n[3],
                               int dir, bool accumulate, bool fp32, void *rhs,
                               cudaStream_t stream, uint64_t *launches) {
-    const int64_t gx = (n[0] * n[1] + kThreads - 1) / kThreads;
+    // the smallest block (64 threads) gives the largest grid
+    const int64_t gx = (n[0] * n[1] + 63) / 64;
     if (gx > 0x7fffffff) return cudaErrorInvalidValue;
     if (fp32)
         launch_dir<float>(static_cast<const float *>(flux), static_cast<const float *>(inv_d), nv,
