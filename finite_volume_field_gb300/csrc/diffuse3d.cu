@@ -11,14 +11,14 @@
 // even on its own in the order written; 6c is its own rounded product (6c is
 // not a power-of-two scaling, so no fused form is exact here).
 //
-// Kernels (both march along k; a block of warps owns a tile of 32*V cells
-// along i by one row along j per warp, V = 4 FP32 or 2 FP64 cells per lane).
+// Kernels (both march along k; a block owns a tile of 32*V cells along i
+// by a few rows along j, V = 4 FP32 or 2 FP64 cells per lane).
 //   bulk   (FP32, rows 16-byte aligned: nx a multiple of 4, 16-byte
-//          buffers): the tile is 2*kTY rows (each warp computes two rows).
+//          buffers): 4 warps, a tile of 8 rows (each warp computes two).
 //          One thread streams whole planes of the tile into a ring of
 //          shared-memory slots with tensor-map bulk copies
 //          (cp.async.bulk.tensor), two planes ahead of the plane being
-//          computed.  A plane is one (32V+2V) x (2kTY+2) box: the tile's
+//          computed.  A plane is one (32V+2V) x 10 box: the tile's
 //          rows plus one halo row above and below, each widened by 16 bytes
 //          on both sides for the W/E neighbours; the copy engine zero-fills
 //          the parts outside the grid, and one mbarrier per slot counts the
@@ -62,7 +62,7 @@
 namespace fvf {
 namespace {
 
-constexpr int kTY = 8;  // warps (rows along j) per block
+constexpr int kTY = 4;  // warps per block of the bulk kernel
 
 __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
 __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
@@ -225,7 +225,7 @@ __device__ __forceinline__ void store_vec(T *p, const Vec<T, V> &x) {
 // with 74 registers and 3 blocks measured 1.67 against 1.56 ms capped, and
 // 5 blocks spill).  FP32 (rows that are not 16-byte aligned): 8.
 template <typename T>
-__host__ __device__ constexpr int march3_rows() { return sizeof(T) == 8 ? 4 : kTY; }
+__host__ __device__ constexpr int march3_rows() { return sizeof(T) == 8 ? 4 : 8; }
 
 // Every block takes the zero slots: taking them only in the blocks that
 // hold an x face (a block-uniform branch between two copies of the loop)
@@ -345,8 +345,14 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
 // Bulk-copy kernel
 // ---------------------------------------------------------------------------
 
-// Ring of 5 slots, 2 rows per warp and runs of 64 planes measured best at
-// 512^3 (0.216 ms per step, against 0.240 for 6 slots, 1 row, 32 planes).
+// Blocks of 4 warps, a ring of 5 slots, 2 rows per warp and runs of 64
+// planes measured best at 512^3 on GB300 (one box, back to back, 0.170 ms
+// per step: 72 registers and 27.7 KB of shared memory, 7 blocks per SM).
+// Against it: 8 warps 0.197; 4 warps with a ring of 4 or 6 slots 0.191 or
+// 0.206 (6 slots fit only 6 blocks); with a 64-register cap for 8 blocks
+// 0.182 (spills); with 3 or 4 rows per warp 0.182 or 0.199; 2 warps of 4
+// rows 0.189.  (Before the packed additions, 8 warps: 0.216 against 0.240
+// for 6 slots, 1 row, 32 planes.)
 constexpr int kRing = 5;                     // slots: planes k-1, k, k+1 and kRing-3 ahead
 constexpr int kRPW = 2;                      // rows per warp in the bulk kernel
 constexpr int64_t kRunPlanes = 64;           // planes per work item of the bulk kernel
@@ -562,7 +568,7 @@ EncodeTiledFn encode_tiled_fn() {
     return fn;
 }
 
-// Tensor map of a whole nx*ny*nz field, box (32V+2V) x (kTY+2) x 1.  False if
+// Tensor map of a whole nx*ny*nz field, box (32V+2V) x kRows x 1.  False if
 // the driver call is unavailable or refuses the map.
 template <typename T>
 bool encode_field_map(CUtensorMap *map, const T *base, int64_t nx, int64_t ny, int64_t nz) {
