@@ -218,12 +218,14 @@ __device__ __forceinline__ void store_vec(T *p, const Vec<T, V> &x) {
     }
 }
 
-// Rows (warps) per block of the register march kernel.  FP64: 4, at most 64
-// registers, 8 blocks of 128 threads per SM.  Per 512^3 FP64 step on GB300,
-// runs of 16 planes: 1.405 ms with 4 rows, against 1.422 with 2, 1.484 with
-// 6, 1.492 with 8 and 1.740 with 16 (1024 threads per SM in each; 8 rows
-// with 74 registers and 3 blocks measured 1.67 against 1.56 ms capped, and
-// 5 blocks spill).  FP32 (rows that are not 16-byte aligned): 8.
+// Rows (warps) per block of the register march kernel.  FP64: 4.  Per
+// 512^3 FP64 step on GB300, runs of 16 planes, 64 registers (8 blocks per
+// SM): 1.405 ms with 4 rows, against 1.422 with 2, 1.484 with 6, 1.492 with
+// 8 and 1.740 with 16 (1024 threads per SM in each).  With 4 rows and no
+// minimum-blocks bound the compiler takes 72 registers (7 blocks per SM):
+// 1.354 ms, against 1.377 with a minimum of 6 blocks (also 72 registers),
+// 1.406 with 8 (64), 1.409 with 5 (82) and 1.451 with 9 (56, spills).
+// FP32 (rows that are not 16-byte aligned): 8.
 template <typename T>
 __host__ __device__ constexpr int march3_rows() { return sizeof(T) == 8 ? 4 : 8; }
 
@@ -232,7 +234,7 @@ __host__ __device__ constexpr int march3_rows() { return sizeof(T) == 8 ? 4 : 8;
 // spilled at the 64-register cap and measured 3% slower (1.529 against
 // 1.483 ms per step).
 template <typename T, int V>
-__global__ void __launch_bounds__(32 * march3_rows<T>(), sizeof(T) == 8 ? 8 : 0)
+__global__ void __launch_bounds__(32 * march3_rows<T>())
 diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
                  int64_t nz, T alpha, int64_t kz_len) {
     constexpr int kR = march3_rows<T>();
