@@ -46,17 +46,18 @@ __host__ __device__ constexpr int threads_of() {
 }
 
 // Minimum resident blocks per SM, per form (a register cap; 0 = none), as
-// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7 with 256-thread
-// blocks, and kept at the same threads per SM for the smaller blocks: the
-// FP32 form at 6 (more loads in flight for 4-byte elements: 0.099 ms at 4
-// blocks, 0.093 ms at 6, 0.146 ms at 8, timed back to back), the assigning
-// FP64 y form at 6 (5-7% faster despite a few spilled registers) and the
-// accumulating one at 5 (7%).  The other FP64 forms take none: a cap there
-// measured 5-13% slower, and even a minimum of 1 changes the compiler's
-// register allocation (48 -> 64-84 registers, 9-43% slower).
+// measured on GB300 at 8 x 201^3 and 4800 x 1200 x 7: the FP32 form at 6
+// blocks of 256 threads (more loads in flight for 4-byte elements: 0.099 ms
+// at 4 blocks, 0.093 ms at 6, 0.146 ms at 8, timed back to back); the
+// assigning FP64 y form at 12 blocks of 128 threads (0.121 / 0.179 ms for
+// the 2D / 3D y sweeps, against 0.127 / 0.186 with no cap and 0.129-0.133 /
+// 0.189-0.193 with 8 or 10).  The other FP64 forms take none: with 256-thread
+// blocks a cap on x and z measured 5-13% slower, and on the accumulating y
+// form (64-thread blocks) a minimum of 20 blocks measured 0.182 / 0.286 ms
+// against 0.168 / 0.265 with none.
 template <int DIR, bool ACC, typename T>
 constexpr int min_blocks() {
-    return (sizeof(T) == 4 ? 6 : (DIR == 1 ? (ACC ? 5 : 6) : 0)) * 256 / threads_of<ACC, T>();
+    return sizeof(T) == 4 ? 6 : (DIR == 1 && !ACC ? 12 : 0);
 }
 
 // variables per load batch: 4 FP64 or 8 FP32, 64 bytes of face loads each
