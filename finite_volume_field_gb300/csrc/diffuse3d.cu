@@ -347,9 +347,11 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
 // Bulk-copy kernel
 // ---------------------------------------------------------------------------
 
-// Blocks of 4 warps, a ring of 5 slots, 2 rows per warp and runs of 64
-// planes measured best at 512^3 on GB300 (one box, back to back, 0.170 ms
-// per step: 72 registers and 27.7 KB of shared memory, 7 blocks per SM).
+// Blocks of 4 warps, a ring of 5 slots, 2 rows per warp and runs of 128
+// planes measured best at 512^3 on GB300 (one box, back to back, 0.169 ms
+// per step: 72 registers and 27.7 KB of shared memory, 7 blocks per SM;
+// runs of 64, 32 and 16 planes 0.170, 0.174 and 0.179 ms: every run re-reads
+// two halo planes).
 // Against it: 8 warps 0.197; 4 warps with a ring of 4 or 6 slots 0.191 or
 // 0.206 (6 slots fit only 6 blocks); with a 64-register cap for 8 blocks
 // 0.182 (spills); with 3 or 4 rows per warp 0.182 or 0.199; 2 warps of 4
@@ -357,7 +359,7 @@ diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int
 // for 6 slots, 1 row, 32 planes.)
 constexpr int kRing = 5;                     // slots: planes k-1, k, k+1 and kRing-3 ahead
 constexpr int kRPW = 2;                      // rows per warp in the bulk kernel
-constexpr int64_t kRunPlanes = 64;           // planes per work item of the bulk kernel
+constexpr int64_t kRunPlanes = 128;          // planes per work item of the bulk kernel
 constexpr int kBulkRows = kTY * kRPW;        // tile rows of a bulk block
 constexpr int kRows = kBulkRows + 2;         // tile rows plus one halo row each side
 
