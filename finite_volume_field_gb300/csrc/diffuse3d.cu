@@ -231,8 +231,9 @@ __host__ __device__ constexpr int march3_rows() { return sizeof(T) == 8 ? 4 : 8;
 
 // Every block takes the zero slots: taking them only in the blocks that
 // hold an x face (a block-uniform branch between two copies of the loop)
-// spilled at the 64-register cap and measured 3% slower (1.529 against
-// 1.483 ms per step).
+// measured slower, 1.529 against 1.483 ms per step with 8-row tiles (spills
+// at the 64-register cap) and 1.402 against 1.353 with 4-row tiles and no
+// cap.
 template <typename T, int V>
 __global__ void __launch_bounds__(32 * march3_rows<T>())
 diffuse3d_kernel(const T *__restrict__ src, T *__restrict__ dst, int64_t nx, int64_t ny,
